@@ -1,0 +1,144 @@
+/*
+ * spear.h -- C ABI of the GB300 (sm_103a) W4 + input-adaptive error-compensator
+ * linear layer.
+ *
+ * The layer ("SPEAR: A System for Post-Quantization Error-Adaptive Recovery",
+ * section 2.1A, Input-Adaptive Error Compensators, "Mechanism") applies to each
+ * token x the effective weight
+ *
+ *     W_q + alpha * B * diag(gamma(A x)) * A,
+ *
+ * i.e. y = W_q x + alpha * B (gamma(z) (.) z) with z = A x. W_q is a 4-bit
+ * weight with bf16 scales and integer zero points per group of 128 input
+ * channels or per output channel (section 1 and section 3.1 use 4-bit weights,
+ * per-channel being the hard case); A is rank x K, B is N x rank, gamma is the
+ * elementwise sigmoid (or the constant one, which gives the static low-rank
+ * correction W_q + alpha B A that section 1 contrasts with). Phase-aware
+ * dispatch (section 2.2A) is exposed as two entry points: a fused single-kernel
+ * decode path for M <= 32 tokens and a tensor-core prefill path for larger M.
+ *
+ * Conventions for every call:
+ *  - Device pointers are plain CUDA device addresses on the current device;
+ *    host pointers are ordinary (preferably pinned) host memory. No call takes
+ *    ownership of a caller's buffer.
+ *  - bf16 tensors are row-major and contiguous; x, y and every weight buffer
+ *    must be 16-byte aligned.
+ *  - Argument errors are reported synchronously and leave nothing enqueued.
+ *  - Forward calls only enqueue work on `stream` (no allocation, no
+ *    synchronisation). Errors detected on the device (a bounded wait that
+ *    timed out) are latched in the handle and reported by spear_linear_check.
+ *  - A handle is not safe for concurrent forwards (its workspace is shared);
+ *    distinct handles are independent.
+ */
+#ifndef SPEAR_H_
+#define SPEAR_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct spear_linear_s* spear_linear_t;
+
+typedef enum {
+  SPEAR_OK = 0,
+  SPEAR_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, M outside the entry point's range */
+  SPEAR_ERR_UNSUPPORTED = 2,   /* valid but outside what the kernels implement (see create) */
+  SPEAR_ERR_OOM = 3,           /* device allocation failed in create */
+  SPEAR_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+  SPEAR_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up (reported by check) */
+} spear_status_t;
+
+typedef enum {
+  SPEAR_GATE_SIGMOID = 0,      /* gamma(z) = 1 / (1 + exp(-z)), so gamma(z) * z = SiLU(z) */
+  SPEAR_GATE_ONE = 1           /* gamma = 1: static correction W_q + alpha B A */
+} spear_gate_t;
+
+typedef struct {
+  int32_t K;                   /* input features; multiple of 128 */
+  int32_t N;                   /* output features; multiple of 8 */
+  int32_t group_size;          /* 128, or 0 for one group per output channel (G = K) */
+  const uint8_t* qweight;      /* device, uint8 [N][K/2]: byte j of row n holds k = 2j in its
+                                  low nibble and k = 2j + 1 in its high nibble, codes 0..15 */
+  const void* scales;          /* device, bf16 [N][K/G] */
+  const uint8_t* zeros;        /* device, uint8 [N][K/G], values 0..15; NULL means z = 8 */
+  int32_t rank;                /* EC rank r: 0 (no compensator) or a multiple of 16, <= 256 */
+  const void* A;               /* device, bf16 [rank][K] (ignored when rank == 0) */
+  const void* B;               /* device, bf16 [N][rank] (ignored when rank == 0) */
+  float alpha;                 /* compensator strength */
+  spear_gate_t gate;
+  int32_t max_tokens;          /* largest M any forward on this handle will use (>= 1) */
+} spear_linear_desc_t;
+
+/* Build a handle from user-layout weights ("SPEAR", section 2.1A: the W_q of the
+ * effective weight and the compensator's A, B, alpha, gamma).
+ * Copies and re-lays-out every weight into handle-owned device memory on
+ * `stream`, then synchronises `stream`, so the caller may free or reuse its
+ * buffers as soon as this returns. On success *out holds the handle.
+ * Errors: INVALID_ARG (null desc/out/pointers, K % 128, N % 8, bad group size,
+ * rank not a multiple of 16 or > 256, max_tokens < 1), UNSUPPORTED (shape
+ * outside the kernels' limits: N > 16 * 16 * SM count for the decode path),
+ * OOM, CUDA. On error *out is left NULL and nothing is leaked. */
+spear_status_t spear_linear_create(const spear_linear_desc_t* desc, cudaStream_t stream,
+                                   spear_linear_t* out);
+
+/* Decode-phase forward ("SPEAR", section 2.2A: memory-bound, small M; the whole
+ * layer, compensator included, runs as one kernel).
+ *   x: device bf16 [M][K]; y: device bf16 [M][N] (must not overlap x).
+ * 1 <= M <= min(32, max_tokens); M == 0 is a no-op returning OK.
+ * y = bf16_RNE(W_q x + alpha B (gamma(Ax) (.) Ax)) with fp32 accumulation. */
+spear_status_t spear_linear_forward_decode(spear_linear_t h, const void* x, void* y, int32_t M,
+                                           cudaStream_t stream);
+
+/* Prefill-phase forward ("SPEAR", section 2.2A: compute-bound, M > 1): the
+ * main contraction runs on tcgen05 tensor cores with in-kernel INT4
+ * dequantisation; the compensator's down-projection and gate run in a small
+ * pre-kernel and its up-projection is folded into the same accumulator.
+ *   x: device bf16 [M][K]; y: device bf16 [M][N]; 1 <= M <= max_tokens
+ * (M == 0 is a no-op). Correct for every M; tuned for M >= 256. */
+spear_status_t spear_linear_forward_prefill(spear_linear_t h, const void* x, void* y, int32_t M,
+                                            cudaStream_t stream);
+
+/* Phase dispatch ("SPEAR", section 2.2A): decode path for M <= 32, prefill otherwise. */
+spear_status_t spear_linear_forward(spear_linear_t h, const void* x, void* y, int32_t M,
+                                    cudaStream_t stream);
+
+/* End-to-end forward on HOST buffers: copies x_host (bf16 [M][K]) to a
+ * handle-owned device buffer, runs spear_linear_forward, copies the result
+ * into y_host (bf16 [M][N]) and synchronises `stream`. Pinned host memory gives
+ * asynchronous copies. 1 <= M <= max_tokens. */
+spear_status_t spear_linear_forward_host(spear_linear_t h, const void* x_host, void* y_host,
+                                         int32_t M, cudaStream_t stream);
+
+/* Free every device allocation of the handle (synchronises the device first).
+ * NULL is accepted. */
+spear_status_t spear_linear_destroy(spear_linear_t h);
+
+/* Test surface: write the dequantised weight bf16_RNE((q - z) * s) as bf16
+ * [N][K] (device) by unpacking the kernel-side layout of `path`
+ * (0 = decode layout, 1 = prefill layout) with the kernels' own unpack code. */
+spear_status_t spear_linear_dequantize(spear_linear_t h, int32_t path, void* w_out,
+                                       cudaStream_t stream);
+
+/* Synchronise `stream` and report the handle's device status word: OK, or
+ * TIMEOUT if a bounded device-side wait gave up since the last check. A
+ * TIMEOUT clears the status and resets the handle's workspace so it is usable
+ * again. */
+spear_status_t spear_linear_check(spear_linear_t h, cudaStream_t stream);
+
+/* Test surface for the bounded waits: wait_ns sets the device-side wait limit
+ * (0 restores the default of 100 ms); skip_arrive != 0 makes the decode
+ * kernel's CTAs skip their "compensator projection done" arrival so that the
+ * wait must run out (the kernel then leaves the compensator out of y and
+ * latches TIMEOUT). */
+spear_status_t spear_linear_debug_set(spear_linear_t h, int64_t wait_ns, int32_t skip_arrive);
+
+/* Human-readable name of a status code (static storage). */
+const char* spear_status_string(spear_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEAR_H_ */

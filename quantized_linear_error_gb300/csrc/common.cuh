@@ -1,0 +1,173 @@
+// Shared device helpers for the sm_103a kernels: inline PTX for mbarriers,
+// bulk async copies, warp-level MMA, INT4 unpacking and bounded waits.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define SPEAR_DEVINL __device__ __forceinline__
+
+namespace spear {
+
+// Device status word bits (latched until spear_linear_check clears them).
+enum : unsigned {
+  kStatusTimeoutZ = 1u,      // grid-wide "compensator projection done" wait gave up
+  kStatusTimeoutPipe = 2u,   // an mbarrier wait in a pipeline gave up
+};
+
+// Workspace of one handle (device memory, zero-initialised at create).
+struct SyncWords {
+  unsigned arrive;     // CTAs that finished their share of z = A x
+  unsigned depart;     // CTAs that finished reading z
+  unsigned status;     // kStatus* bits
+  unsigned pad[29];    // keep the z buffer 128-byte aligned
+};
+
+SPEAR_DEVINL uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+SPEAR_DEVINL uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+SPEAR_DEVINL void mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+SPEAR_DEVINL void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+SPEAR_DEVINL void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+SPEAR_DEVINL void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+SPEAR_DEVINL void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+SPEAR_DEVINL bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete; gives up after `limit_ns`
+// (returns false) so that a broken pipeline can never hang the GPU.
+SPEAR_DEVINL bool mbar_wait_bounded(uint64_t* bar, unsigned parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > limit_ns) return false;
+  }
+}
+
+// ---------------------------------------------------------------- bulk copies
+// 1-D bulk copy global -> shared of the executing CTA, completion counted in
+// bytes on `bar`. dst, src 16-byte aligned, bytes a multiple of 16.
+SPEAR_DEVINL void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Same, with an L2 evict-first hint for data read exactly once (weights).
+SPEAR_DEVINL void bulk_g2s_stream(void* dst, const void* src, unsigned bytes, uint64_t* bar,
+                                  uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+      "%4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+SPEAR_DEVINL uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// ---------------------------------------------------------------- warp MMA
+// D = A(16x16, row) * B(16x8, col) + C, bf16 inputs, fp32 accumulate.
+SPEAR_DEVINL void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+SPEAR_DEVINL void ldmatrix_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(p)));
+}
+
+SPEAR_DEVINL void ldmatrix_x2(uint32_t& r0, uint32_t& r1, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(smem_u32(p)));
+}
+
+// ---------------------------------------------------------------- INT4 unpack
+// (w & 0x000F000F) | 0x43004300: the nibbles at bits 0..3 and 16..19 become the
+// low mantissa bits of two bf16 values 128 + code (exact: bf16 has 8
+// significant bits and 128..143 are integers in its [128, 256) binade).
+SPEAR_DEVINL uint32_t int4_pair_to_bf16x2_biased(uint32_t w) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "r"(0x000F000Fu), "r"(0x43004300u));
+  return r;
+}
+
+// a - b on bf16x2; exact here because both operands are integers in [128, 143].
+SPEAR_DEVINL uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// bf16 bits of (128 + z) in both halves.
+SPEAR_DEVINL uint32_t biased_zero_x2(uint32_t zbits16) { return zbits16 | (zbits16 << 16); }
+
+SPEAR_DEVINL float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+SPEAR_DEVINL uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Split v into bf16 hi + bf16 lo with hi + lo == v to ~2^-17 relative.
+SPEAR_DEVINL void split_bf16(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
+  hi = __float2bfloat16_rn(v);
+  lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
+SPEAR_DEVINL void red_add_v2(float* addr, float a, float b) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(addr), "f"(a), "f"(b) : "memory");
+}
+
+SPEAR_DEVINL unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+}  // namespace spear

@@ -1,0 +1,226 @@
+// One-time re-layout of user weights into the kernel layouts (run by
+// spear_linear_create), and the dequantisation export used to test the unpack
+// code of both layouts bit for bit.
+#include "internal.h"
+
+namespace spear {
+namespace {
+
+// Code of (row, k) from the user layout: byte k/2 of the row, even k low nibble.
+__device__ __forceinline__ uint32_t user_code(const uint8_t* q, int K, int N, int row, int k) {
+  if (row >= N) return 0u;
+  const uint8_t b = q[(size_t)row * (K / 2) + (k >> 1)];
+  return (k & 1) ? (b >> 4) : (b & 0xF);
+}
+
+__device__ __forceinline__ uint32_t user_sz(const uint16_t* s, const uint8_t* z, int n_groups, int N, int row,
+                                            int g) {
+  if (row >= N) return 0x4300u << 16;  // scale 0, zero 0: a padded row dequantises to 0
+  const uint32_t sb = s[(size_t)row * n_groups + g];
+  const uint32_t zp = z ? z[(size_t)row * n_groups + g] : 8u;
+  return sb | ((0x4300u | zp) << 16);
+}
+
+__global__ void repack_w_decode(const uint8_t* __restrict__ q, int K, int N, int nt16, uint4* __restrict__ out) {
+  const int kb64 = K / 64;
+  const long total = (long)nt16 * kb64 * 32;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+    const int lane = i % 32;
+    const int kb = (i / 32) % kb64;
+    const int tile = i / (32L * kb64);
+    const int g = lane >> 2, t = lane & 3;
+    const int r0 = tile * 16 + g, r1 = r0 + 8;
+    uint32_t w[4];
+    for (int s = 0; s < 4; ++s) {
+      const int k = kb * 64 + s * 16 + 2 * t;
+      w[s] = user_code(q, K, N, r0, k) | user_code(q, K, N, r1, k) << 4 | user_code(q, K, N, r0, k + 8) << 8 |
+             user_code(q, K, N, r1, k + 8) << 12 | user_code(q, K, N, r0, k + 1) << 16 |
+             user_code(q, K, N, r1, k + 1) << 20 | user_code(q, K, N, r0, k + 9) << 24 |
+             user_code(q, K, N, r1, k + 9) << 28;
+    }
+    out[i] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+__global__ void repack_w_prefill(const uint8_t* __restrict__ q, int K, int N, int nt128, uint32_t* __restrict__ out) {
+  const int kb64 = K / 64;
+  const long total = (long)nt128 * kb64 * 128 * 8;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+    const int c = i % 8;
+    const int rl = (i / 8) % 128;
+    const int kb = (i / 1024) % kb64;
+    const int tile = i / (1024L * kb64);
+    const int row = tile * 128 + rl;
+    const int k = kb * 64 + c * 8;
+    uint32_t w = 0;
+    // nibble slot j*4 holds channel 2j, slot 16 + j*4 holds channel 2j+1
+    for (int j = 0; j < 4; ++j) {
+      w |= user_code(q, K, N, row, k + 2 * j) << (4 * j);
+      w |= user_code(q, K, N, row, k + 2 * j + 1) << (16 + 4 * j);
+    }
+    out[i] = w;
+  }
+}
+
+__global__ void repack_sz(const uint16_t* __restrict__ s, const uint8_t* __restrict__ z, int n_groups, int N,
+                          int ntiles, int tile_rows, uint32_t* __restrict__ out) {
+  const long total = (long)ntiles * n_groups * tile_rows;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+    const int rl = i % tile_rows;
+    const int g = (i / tile_rows) % n_groups;
+    const int tile = i / ((long)tile_rows * n_groups);
+    out[i] = user_sz(s, z, n_groups, N, tile * tile_rows + rl, g);
+  }
+}
+
+// bf16 matrix [rows][cols] into m16n8k16 A-fragment order [rows/16][cols/16][32] uint4.
+__global__ void repack_frag(const uint16_t* __restrict__ m, int rows, int cols, int row_tiles,
+                            uint4* __restrict__ out) {
+  const int ks = cols / 16;
+  const long total = (long)row_tiles * ks * 32;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+    const int lane = i % 32;
+    const int kk = (i / 32) % ks;
+    const int tile = i / (32L * ks);
+    const int g = lane >> 2, t = lane & 3;
+    const int r0 = tile * 16 + g, r1 = r0 + 8;
+    const int k = kk * 16 + 2 * t;
+    auto at = [&](int r, int c) -> uint32_t { return r < rows ? (uint32_t)m[(size_t)r * cols + c] : 0u; };
+    out[i] = make_uint4(at(r0, k) | at(r0, k + 1) << 16, at(r1, k) | at(r1, k + 1) << 16,
+                        at(r0, k + 8) | at(r0, k + 9) << 16, at(r1, k + 8) | at(r1, k + 9) << 16);
+  }
+}
+
+// Copy a bf16 [rows][cols] matrix into [rows_pad][cols], zero rows past `rows`.
+__global__ void copy_pad_rows(const uint16_t* __restrict__ m, int rows, int rows_pad, int cols,
+                              uint16_t* __restrict__ out) {
+  const long total = (long)rows_pad * cols;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x)
+    out[i] = (i / cols) < rows ? m[i] : (uint16_t)0;
+}
+
+// (q - z) * s with one rounding: the exact integer difference comes from the
+// kernels' own unpack (biased bf16 pair minus biased zero), the product of an
+// integer |d| <= 15 and a bf16 scale is exact in fp32, and the conversion to
+// bf16 rounds once to nearest even.
+__device__ __forceinline__ __nv_bfloat16 scaled(uint32_t diff_bits16, float s) {
+  return __float2bfloat16_rn(bf16_bits_to_float(diff_bits16) * s);
+}
+
+__global__ void dequant_from_decode(const uint4* __restrict__ wq, const uint32_t* __restrict__ sz, int K, int N,
+                                    int nt16, int G, int n_groups, __nv_bfloat16* __restrict__ out) {
+  const int kb64 = K / 64;
+  const long total = (long)nt16 * kb64 * 32;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+    const int lane = i % 32;
+    const int kb = (i / 32) % kb64;
+    const int tile = i / (32L * kb64);
+    const int g = lane >> 2, t = lane & 3;
+    const int grp = (kb * 64) / G;
+    const uint32_t sz0 = sz[((size_t)tile * n_groups + grp) * 16 + g];
+    const uint32_t sz1 = sz[((size_t)tile * n_groups + grp) * 16 + g + 8];
+    const uint32_t zz0 = biased_zero_x2(sz0 >> 16), zz1 = biased_zero_x2(sz1 >> 16);
+    const float s0 = bf16_bits_to_float(sz0 & 0xFFFF), s1 = bf16_bits_to_float(sz1 & 0xFFFF);
+    const uint4 v = wq[i];
+    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+    const int r0 = tile * 16 + g, r1 = r0 + 8;
+    for (int s = 0; s < 4; ++s) {
+      const uint32_t w = words[s];
+      const uint32_t d0 = bf16x2_sub(int4_pair_to_bf16x2_biased(w), zz0);        // (r0, k), (r0, k+1)
+      const uint32_t d1 = bf16x2_sub(int4_pair_to_bf16x2_biased(w >> 4), zz1);   // (r1, k), (r1, k+1)
+      const uint32_t d2 = bf16x2_sub(int4_pair_to_bf16x2_biased(w >> 8), zz0);   // (r0, k+8), (r0, k+9)
+      const uint32_t d3 = bf16x2_sub(int4_pair_to_bf16x2_biased(w >> 12), zz1);  // (r1, k+8), (r1, k+9)
+      const int k = kb * 64 + s * 16 + 2 * t;
+      if (r0 < N) {
+        out[(size_t)r0 * K + k] = scaled(d0 & 0xFFFF, s0);
+        out[(size_t)r0 * K + k + 1] = scaled(d0 >> 16, s0);
+        out[(size_t)r0 * K + k + 8] = scaled(d2 & 0xFFFF, s0);
+        out[(size_t)r0 * K + k + 9] = scaled(d2 >> 16, s0);
+      }
+      if (r1 < N) {
+        out[(size_t)r1 * K + k] = scaled(d1 & 0xFFFF, s1);
+        out[(size_t)r1 * K + k + 1] = scaled(d1 >> 16, s1);
+        out[(size_t)r1 * K + k + 8] = scaled(d3 & 0xFFFF, s1);
+        out[(size_t)r1 * K + k + 9] = scaled(d3 >> 16, s1);
+      }
+    }
+  }
+}
+
+__global__ void dequant_from_prefill(const uint32_t* __restrict__ wq, const uint32_t* __restrict__ sz, int K,
+                                     int N, int nt128, int G, int n_groups, __nv_bfloat16* __restrict__ out) {
+  const int kb64 = K / 64;
+  const long total = (long)nt128 * kb64 * 1024;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+    const int c = i % 8;
+    const int rl = (i / 8) % 128;
+    const int kb = (i / 1024) % kb64;
+    const int tile = i / (1024L * kb64);
+    const int row = tile * 128 + rl;
+    if (row >= N) continue;
+    const int k = kb * 64 + c * 8;
+    const uint32_t szw = sz[((size_t)tile * n_groups + k / G) * 128 + rl];
+    const uint32_t zz = biased_zero_x2(szw >> 16);
+    const float s = bf16_bits_to_float(szw & 0xFFFF);
+    const uint32_t w = wq[i];
+    __align__(16) __nv_bfloat16 v[8];
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t d = bf16x2_sub(int4_pair_to_bf16x2_biased(w >> (4 * j)), zz);
+      v[2 * j] = scaled(d & 0xFFFF, s);
+      v[2 * j + 1] = scaled(d >> 16, s);
+    }
+    *reinterpret_cast<uint4*>(out + (size_t)row * K + k) = *reinterpret_cast<uint4*>(v);
+  }
+}
+
+inline int grid_for(long total, int threads) {
+  long b = (total + threads - 1) / threads;
+  return (int)(b < 1 ? 1 : (b > 65535L * 8 ? 65535L * 8 : b));
+}
+
+}  // namespace
+}  // namespace spear
+
+using namespace spear;
+
+spear_status_t spear_build_layouts(spear_linear_s* h, const spear_linear_desc_t* d, cudaStream_t st) {
+  const int K = h->K, N = h->N, r = h->rank;
+  const uint16_t* s = static_cast<const uint16_t*>(d->scales);
+  const int T = 256;
+  long n;
+  n = (long)h->nt16 * (K / 64) * 32;
+  repack_w_decode<<<grid_for(n, T), T, 0, st>>>(d->qweight, K, N, h->nt16, h->wq_dec);
+  n = (long)h->nt16 * h->n_groups * 16;
+  repack_sz<<<grid_for(n, T), T, 0, st>>>(s, d->zeros, h->n_groups, N, h->nt16, 16, h->sz_dec);
+  n = (long)h->nt128 * (K / 64) * 1024;
+  repack_w_prefill<<<grid_for(n, T), T, 0, st>>>(d->qweight, K, N, h->nt128, h->wq_pre);
+  n = (long)h->nt128 * h->n_groups * 128;
+  repack_sz<<<grid_for(n, T), T, 0, st>>>(s, d->zeros, h->n_groups, N, h->nt128, 128, h->sz_pre);
+  if (r > 0) {
+    const uint16_t* A = static_cast<const uint16_t*>(d->A);
+    const uint16_t* B = static_cast<const uint16_t*>(d->B);
+    n = (long)(r / 16) * (K / 16) * 32;
+    repack_frag<<<grid_for(n, T), T, 0, st>>>(A, r, K, r / 16, h->a_dec);
+    n = (long)h->nt16 * (r / 16) * 32;
+    repack_frag<<<grid_for(n, T), T, 0, st>>>(B, N, r, h->nt16, h->b_dec);
+    n = (long)r * K;
+    copy_pad_rows<<<grid_for(n, T), T, 0, st>>>(A, r, r, K, reinterpret_cast<uint16_t*>(h->a_pre));
+    n = (long)h->nt128 * 128 * r;
+    copy_pad_rows<<<grid_for(n, T), T, 0, st>>>(B, N, h->nt128 * 128, r, reinterpret_cast<uint16_t*>(h->b_pre));
+  }
+  return cudaGetLastError() == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
+}
+
+spear_status_t spear_launch_dequant(spear_linear_s* h, int path, __nv_bfloat16* out, cudaStream_t st) {
+  const int T = 256;
+  if (path == 0) {
+    long n = (long)h->nt16 * (h->K / 64) * 32;
+    dequant_from_decode<<<grid_for(n, T), T, 0, st>>>(h->wq_dec, h->sz_dec, h->K, h->N, h->nt16, h->G,
+                                                      h->n_groups, out);
+  } else {
+    long n = (long)h->nt128 * (h->K / 64) * 1024;
+    dequant_from_prefill<<<grid_for(n, T), T, 0, st>>>(h->wq_pre, h->sz_pre, h->K, h->N, h->nt128, h->G,
+                                                       h->n_groups, out);
+  }
+  return cudaGetLastError() == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
+}

@@ -1,0 +1,209 @@
+// C ABI of the library: argument checking, handle lifetime, phase dispatch.
+// All arithmetic of the layer runs in the kernels of decode.cu, prefill.cu and
+// layout.cu; this file only validates, allocates at create and launches.
+#include <new>
+
+#include "internal.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <typename T>
+cudaError_t alloc(T** p, size_t bytes) {
+  *p = nullptr;
+  if (bytes == 0) return cudaSuccess;
+  return cudaMalloc(reinterpret_cast<void**>(p), bytes);
+}
+
+void free_all(spear_linear_s* h) {
+  void* ptrs[] = {h->wq_dec, h->sz_dec, h->a_dec, h->b_dec, h->wq_pre, h->sz_pre,
+                  h->a_pre,  h->b_pre,  h->ws,    h->x_stage, h->y_stage};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+}
+
+spear_status_t validate(const spear_linear_desc_t* d) {
+  if (!d) return SPEAR_ERR_INVALID_ARG;
+  if (d->K <= 0 || d->N <= 0 || d->K % 128 != 0 || d->N % 8 != 0) return SPEAR_ERR_INVALID_ARG;
+  if (d->group_size != 0 && d->group_size != 128) return SPEAR_ERR_INVALID_ARG;
+  if (!d->qweight || !d->scales) return SPEAR_ERR_INVALID_ARG;
+  if (d->rank < 0 || d->rank > 256 || d->rank % 16 != 0) return SPEAR_ERR_INVALID_ARG;
+  if (d->rank > 0 && (!d->A || !d->B)) return SPEAR_ERR_INVALID_ARG;
+  if (d->gate != SPEAR_GATE_SIGMOID && d->gate != SPEAR_GATE_ONE) return SPEAR_ERR_INVALID_ARG;
+  if (d->max_tokens < 1) return SPEAR_ERR_INVALID_ARG;
+  return SPEAR_OK;
+}
+
+spear_status_t check_io(spear_linear_t h, const void* x, void* y, int32_t M) {
+  if (!h || M < 0) return SPEAR_ERR_INVALID_ARG;
+  if (M == 0) return SPEAR_OK;
+  if (!x || !y || M > h->max_tokens) return SPEAR_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y)) return SPEAR_ERR_INVALID_ARG;
+  const char* xb = static_cast<const char*>(x);
+  const char* yb = static_cast<const char*>(y);
+  const size_t xs = (size_t)M * h->K * 2, ys = (size_t)M * h->N * 2;
+  if (xb < yb + ys && yb < xb + xs) return SPEAR_ERR_INVALID_ARG;  // y overlaps x
+  return SPEAR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t stream, spear_linear_t* out) {
+  if (!out) return SPEAR_ERR_INVALID_ARG;
+  *out = nullptr;
+  spear_status_t v = validate(d);
+  if (v != SPEAR_OK) return v;
+
+  spear_linear_s* h = new (std::nothrow) spear_linear_s();
+  if (!h) return SPEAR_ERR_OOM;
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+    delete h;
+    return SPEAR_ERR_CUDA;
+  }
+  h->K = d->K;
+  h->N = d->N;
+  h->per_channel = d->group_size == 0;
+  h->G = h->per_channel ? d->K : d->group_size;
+  h->n_groups = h->K / h->G;
+  h->rank = d->rank;
+  h->alpha = d->alpha;
+  h->gate = d->gate;
+  h->max_tokens = d->max_tokens;
+  h->nt16 = (h->N + 15) / 16;
+  h->nt128 = (h->N + 127) / 128;
+  if ((h->nt16 + h->sm_count - 1) / h->sm_count > kDecodeMaxTilesPerCta) {
+    delete h;
+    return SPEAR_ERR_UNSUPPORTED;
+  }
+
+  const size_t K = h->K, r = h->rank, mt = h->max_tokens;
+  const size_t ws_bytes = sizeof(spear::SyncWords) + kZDecFloats * 4 + mt * r * 4 + mt * r * 2 + 256;
+  cudaError_t e = cudaSuccess;
+  auto A = [&](cudaError_t x) {
+    if (e == cudaSuccess) e = x;
+  };
+  A(alloc(&h->wq_dec, (size_t)h->nt16 * (K / 64) * 32 * 16));
+  A(alloc(&h->sz_dec, (size_t)h->nt16 * h->n_groups * 16 * 4));
+  A(alloc(&h->wq_pre, (size_t)h->nt128 * (K / 64) * 1024 * 4));
+  A(alloc(&h->sz_pre, (size_t)h->nt128 * h->n_groups * 128 * 4));
+  if (r > 0) {
+    A(alloc(&h->a_dec, (r / 16) * (K / 16) * 32 * 16));
+    A(alloc(&h->b_dec, (size_t)h->nt16 * (r / 16) * 32 * 16));
+    A(alloc(&h->a_pre, r * K * 2));
+    A(alloc(&h->b_pre, (size_t)h->nt128 * 128 * r * 2));
+  }
+  A(alloc(&h->ws, ws_bytes));
+  A(alloc(&h->x_stage, mt * K * 2));
+  A(alloc(&h->y_stage, mt * (size_t)h->N * 2));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    free_all(h);
+    delete h;
+    return e == cudaErrorMemoryAllocation ? SPEAR_ERR_OOM : SPEAR_ERR_CUDA;
+  }
+  char* w = static_cast<char*>(h->ws);
+  h->sync = reinterpret_cast<spear::SyncWords*>(w);
+  h->z_dec = reinterpret_cast<float*>(w + sizeof(spear::SyncWords));
+  h->z_pre = h->z_dec + kZDecFloats;
+  h->u_pre = reinterpret_cast<__nv_bfloat16*>(h->z_pre + mt * r);
+
+  spear_status_t st = SPEAR_OK;
+  if (cudaMemsetAsync(h->ws, 0, ws_bytes, stream) != cudaSuccess) st = SPEAR_ERR_CUDA;
+  if (st == SPEAR_OK) st = spear_build_layouts(h, d, stream);
+  if (st == SPEAR_OK && cudaStreamSynchronize(stream) != cudaSuccess) st = SPEAR_ERR_CUDA;
+  if (st != SPEAR_OK) {
+    cudaGetLastError();
+    free_all(h);
+    delete h;
+    return st;
+  }
+  *out = h;
+  return SPEAR_OK;
+}
+
+spear_status_t spear_linear_forward_decode(spear_linear_t h, const void* x, void* y, int32_t M,
+                                           cudaStream_t stream) {
+  spear_status_t v = check_io(h, x, y, M);
+  if (v != SPEAR_OK || M == 0) return v;
+  if (M > kDecodeMaxTokens) return SPEAR_ERR_INVALID_ARG;
+  return spear_launch_decode(h, static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), M, stream);
+}
+
+spear_status_t spear_linear_forward_prefill(spear_linear_t h, const void* x, void* y, int32_t M,
+                                            cudaStream_t stream) {
+  spear_status_t v = check_io(h, x, y, M);
+  if (v != SPEAR_OK || M == 0) return v;
+  return spear_launch_prefill(h, static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), M,
+                              stream);
+}
+
+spear_status_t spear_linear_forward(spear_linear_t h, const void* x, void* y, int32_t M, cudaStream_t stream) {
+  if (M <= kDecodeMaxTokens) return spear_linear_forward_decode(h, x, y, M, stream);
+  return spear_linear_forward_prefill(h, x, y, M, stream);
+}
+
+spear_status_t spear_linear_forward_host(spear_linear_t h, const void* x_host, void* y_host, int32_t M,
+                                         cudaStream_t stream) {
+  if (!h || M < 0) return SPEAR_ERR_INVALID_ARG;
+  if (M == 0) return SPEAR_OK;
+  if (!x_host || !y_host || M > h->max_tokens) return SPEAR_ERR_INVALID_ARG;
+  const size_t xb = (size_t)M * h->K * 2, yb = (size_t)M * h->N * 2;
+  if (cudaMemcpyAsync(h->x_stage, x_host, xb, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return SPEAR_ERR_CUDA;
+  spear_status_t s = spear_linear_forward(h, h->x_stage, h->y_stage, M, stream);
+  if (s != SPEAR_OK) return s;
+  if (cudaMemcpyAsync(y_host, h->y_stage, yb, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return SPEAR_ERR_CUDA;
+  return cudaStreamSynchronize(stream) == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
+}
+
+spear_status_t spear_linear_destroy(spear_linear_t h) {
+  if (!h) return SPEAR_OK;
+  cudaDeviceSynchronize();
+  free_all(h);
+  delete h;
+  return SPEAR_OK;
+}
+
+spear_status_t spear_linear_dequantize(spear_linear_t h, int32_t path, void* w_out, cudaStream_t stream) {
+  if (!h || !w_out || (path != 0 && path != 1) || !aligned16(w_out)) return SPEAR_ERR_INVALID_ARG;
+  return spear_launch_dequant(h, path, static_cast<__nv_bfloat16*>(w_out), stream);
+}
+
+spear_status_t spear_linear_check(spear_linear_t h, cudaStream_t stream) {
+  if (!h) return SPEAR_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return SPEAR_ERR_CUDA;
+  unsigned status = 0;
+  if (cudaMemcpy(&status, &h->sync->status, sizeof status, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SPEAR_ERR_CUDA;
+  if (status == 0) return SPEAR_OK;
+  // Reset the workspace (counters, status, z accumulators) so the handle is usable again.
+  if (cudaMemset(h->sync, 0, sizeof(spear::SyncWords) + kZDecFloats * 4) != cudaSuccess) return SPEAR_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SPEAR_ERR_CUDA;
+  return SPEAR_ERR_TIMEOUT;
+}
+
+spear_status_t spear_linear_debug_set(spear_linear_t h, int64_t wait_ns, int32_t skip_arrive) {
+  if (!h || wait_ns < 0) return SPEAR_ERR_INVALID_ARG;
+  h->wait_ns = wait_ns == 0 ? 100000000ull : (uint64_t)wait_ns;
+  h->skip_arrive = skip_arrive != 0;
+  return SPEAR_OK;
+}
+
+const char* spear_status_string(spear_status_t s) {
+  switch (s) {
+    case SPEAR_OK: return "SPEAR_OK";
+    case SPEAR_ERR_INVALID_ARG: return "SPEAR_ERR_INVALID_ARG";
+    case SPEAR_ERR_UNSUPPORTED: return "SPEAR_ERR_UNSUPPORTED";
+    case SPEAR_ERR_OOM: return "SPEAR_ERR_OOM";
+    case SPEAR_ERR_CUDA: return "SPEAR_ERR_CUDA";
+    case SPEAR_ERR_TIMEOUT: return "SPEAR_ERR_TIMEOUT";
+  }
+  return "SPEAR_ERR_UNKNOWN";
+}
+
+}  // extern "C"

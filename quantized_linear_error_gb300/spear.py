@@ -1,0 +1,176 @@
+"""Thin ctypes binding of ``include/spear.h``.
+
+Argument marshalling only: every step of the layer runs in the CUDA kernels of
+``libspear_gb300.so``. The functions keep the C names; :class:`SpearLinear`
+is a convenience owner of one handle that takes torch tensors for device
+memory and streams. There is no CPU fallback: loading fails loudly when the
+library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import re
+from ctypes import POINTER, byref, c_char_p, c_float, c_int, c_int32, c_int64, c_void_p
+from pathlib import Path
+
+PKG = Path(__file__).resolve().parent
+LIB_PATH = PKG / "libspear_gb300.so"
+HEADER = PKG.parent / "include" / "spear.h"
+
+SPEAR_OK, SPEAR_ERR_INVALID_ARG, SPEAR_ERR_UNSUPPORTED, SPEAR_ERR_OOM, SPEAR_ERR_CUDA, SPEAR_ERR_TIMEOUT = range(6)
+SPEAR_GATE_SIGMOID, SPEAR_GATE_ONE = 0, 1
+DECODE_MAX_TOKENS = 32
+
+
+class spear_linear_desc_t(ctypes.Structure):
+    _fields_ = [("K", c_int32), ("N", c_int32), ("group_size", c_int32),
+                ("qweight", c_void_p), ("scales", c_void_p), ("zeros", c_void_p),
+                ("rank", c_int32), ("A", c_void_p), ("B", c_void_p),
+                ("alpha", c_float), ("gate", c_int), ("max_tokens", c_int32)]
+
+
+class SpearError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+_lib = None
+
+
+def header_functions() -> list[str]:
+    """Names of the functions ``include/spear.h`` declares."""
+    text = HEADER.read_text()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]*?\b(spear_\w+)\s*\(", text, re.M)))
+
+
+def load(path: Path | None = None):
+    """Load the library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = Path(path or LIB_PATH)
+    if not p.exists():
+        raise RuntimeError(f"{p} is missing: build it with quantized_linear_error_gb300.build.build()")
+    L = ctypes.CDLL(str(p))
+    H = c_void_p  # opaque handle / stream
+    L.spear_linear_create.argtypes = [POINTER(spear_linear_desc_t), H, POINTER(c_void_p)]
+    L.spear_linear_forward_decode.argtypes = [H, c_void_p, c_void_p, c_int32, H]
+    L.spear_linear_forward_prefill.argtypes = [H, c_void_p, c_void_p, c_int32, H]
+    L.spear_linear_forward.argtypes = [H, c_void_p, c_void_p, c_int32, H]
+    L.spear_linear_forward_host.argtypes = [H, c_void_p, c_void_p, c_int32, H]
+    L.spear_linear_destroy.argtypes = [H]
+    L.spear_linear_dequantize.argtypes = [H, c_int32, c_void_p, H]
+    L.spear_linear_check.argtypes = [H, H]
+    L.spear_linear_debug_set.argtypes = [H, c_int64, c_int32]
+    L.spear_status_string.argtypes = [c_int]
+    L.spear_status_string.restype = c_char_p
+    for name in ("spear_linear_create", "spear_linear_forward_decode", "spear_linear_forward_prefill",
+                 "spear_linear_forward", "spear_linear_forward_host", "spear_linear_destroy",
+                 "spear_linear_dequantize", "spear_linear_check", "spear_linear_debug_set"):
+        getattr(L, name).restype = c_int
+    _lib = L
+    return L
+
+
+def status_string(s: int) -> str:
+    return load().spear_status_string(s).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != SPEAR_OK:
+        raise SpearError(status, what)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+class SpearLinear:
+    """Owner of one ``spear_linear_t``.
+
+    ``qweight`` uint8 [N][K/2], ``scales`` bf16 [N][K/G], ``zeros`` uint8
+    [N][K/G] or None, ``A`` bf16 [r][K], ``B`` bf16 [N][r] (None when r = 0):
+    CUDA tensors in the layout ``spear_linear_desc_t`` documents. The library
+    copies them; the tensors may be freed after construction.
+    """
+
+    def __init__(self, K, N, group_size, qweight, scales, zeros=None, A=None, B=None,
+                 alpha=1.0, gate=SPEAR_GATE_SIGMOID, max_tokens=32, stream=None):
+        L = load()
+        rank = 0 if A is None else int(A.shape[0])
+        d = spear_linear_desc_t(int(K), int(N), int(group_size), _ptr(qweight), _ptr(scales), _ptr(zeros),
+                                rank, _ptr(A), _ptr(B), float(alpha), int(gate), int(max_tokens))
+        h = c_void_p()
+        _check(L.spear_linear_create(byref(d), _stream(stream), byref(h)), "spear_linear_create")
+        self.h = h
+        self.K, self.N, self.rank, self.max_tokens = int(K), int(N), rank, int(max_tokens)
+
+    def _io(self, fn, x, y, M, stream, what):
+        _check(fn(self.h, _ptr(x), _ptr(y), int(M), _stream(stream)), what)
+
+    def forward_decode(self, x, y, stream=None):
+        self._io(load().spear_linear_forward_decode, x, y, x.shape[0], stream, "spear_linear_forward_decode")
+        return y
+
+    def forward_prefill(self, x, y, stream=None):
+        self._io(load().spear_linear_forward_prefill, x, y, x.shape[0], stream, "spear_linear_forward_prefill")
+        return y
+
+    def forward(self, x, y, stream=None):
+        self._io(load().spear_linear_forward, x, y, x.shape[0], stream, "spear_linear_forward")
+        return y
+
+    def forward_host(self, x_host, y_host, stream=None):
+        self._io(load().spear_linear_forward_host, x_host, y_host, x_host.shape[0], stream,
+                 "spear_linear_forward_host")
+        return y_host
+
+    def dequantize(self, out, path=0, stream=None):
+        _check(load().spear_linear_dequantize(self.h, int(path), _ptr(out), _stream(stream)),
+               "spear_linear_dequantize")
+        return out
+
+    def check(self, stream=None) -> int:
+        return load().spear_linear_check(self.h, _stream(stream))
+
+    def debug_set(self, wait_ns: int = 0, skip_arrive: bool = False) -> None:
+        _check(load().spear_linear_debug_set(self.h, int(wait_ns), int(bool(skip_arrive))), "spear_linear_debug_set")
+
+    def close(self) -> None:
+        if getattr(self, "h", None) and self.h.value:
+            load().spear_linear_destroy(self.h)
+            self.h = c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def from_weights(w, device="cuda", max_tokens=32, alpha=None, gate=None, stream=None) -> SpearLinear:
+    """Build a :class:`SpearLinear` from ``workload.LinearWeights`` (host numpy)."""
+    import numpy as np
+    import torch
+
+    def dev(a, dt):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).view(dt).to(device)
+
+    sp = w.spec
+    q = dev(w.q, torch.uint8)
+    s = dev(w.s.view(np.int16), torch.bfloat16)
+    z = dev(w.z, torch.uint8)
+    A = dev(w.A.view(np.int16), torch.bfloat16) if sp.rank else None
+    B = dev(w.B.view(np.int16), torch.bfloat16) if sp.rank else None
+    lin = SpearLinear(sp.K, sp.N, sp.group_size, q, s, z, A, B,
+                      sp.alpha if alpha is None else alpha, sp.gate if gate is None else gate,
+                      max_tokens, stream)
+    return lin

@@ -1,0 +1,57 @@
+"""C-ABI boundary checks that need no GPU: the library builds, loads, exports
+every function the header declares, and rejects bad arguments before touching
+the device."""
+import ctypes
+
+import pytest
+
+from quantized_linear_error_gb300 import build, spear
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return spear.load()
+
+
+def test_exports_every_header_function(L):
+    names = spear.header_functions()
+    assert {"spear_linear_create", "spear_linear_forward_decode", "spear_linear_forward_prefill",
+            "spear_linear_destroy"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in spear.h but not exported"
+
+
+def test_status_strings(L):
+    assert [spear.status_string(i) for i in range(6)] == [
+        "SPEAR_OK", "SPEAR_ERR_INVALID_ARG", "SPEAR_ERR_UNSUPPORTED", "SPEAR_ERR_OOM", "SPEAR_ERR_CUDA",
+        "SPEAR_ERR_TIMEOUT"]
+
+
+def _desc(**kw):
+    d = dict(K=256, N=64, group_size=128, qweight=16, scales=16, zeros=None, rank=0, A=None, B=None,
+             alpha=1.0, gate=0, max_tokens=4)
+    d.update(kw)
+    return spear.spear_linear_desc_t(*[d[f] for f, _ in spear.spear_linear_desc_t._fields_])
+
+
+@pytest.mark.parametrize("bad", [dict(K=100), dict(K=0), dict(N=12), dict(group_size=64), dict(qweight=None),
+                                 dict(scales=None), dict(rank=8), dict(rank=272), dict(rank=16),
+                                 dict(max_tokens=0), dict(gate=7)])
+def test_create_rejects_bad_descriptor(L, bad):
+    h = ctypes.c_void_p(1234)
+    assert L.spear_linear_create(ctypes.byref(_desc(**bad)), None, ctypes.byref(h)) == spear.SPEAR_ERR_INVALID_ARG
+    assert h.value is None
+
+
+def test_null_arguments(L):
+    h = ctypes.c_void_p()
+    assert L.spear_linear_create(None, None, ctypes.byref(h)) == spear.SPEAR_ERR_INVALID_ARG
+    assert L.spear_linear_create(ctypes.byref(_desc()), None, None) == spear.SPEAR_ERR_INVALID_ARG
+    for fn in (L.spear_linear_forward_decode, L.spear_linear_forward_prefill, L.spear_linear_forward):
+        assert fn(None, 16, 32, 1, None) == spear.SPEAR_ERR_INVALID_ARG
+    assert L.spear_linear_forward_host(None, 16, 32, 1, None) == spear.SPEAR_ERR_INVALID_ARG
+    assert L.spear_linear_dequantize(None, 0, 16, None) == spear.SPEAR_ERR_INVALID_ARG
+    assert L.spear_linear_check(None, None) == spear.SPEAR_ERR_INVALID_ARG
+    assert L.spear_linear_debug_set(None, 0, 0) == spear.SPEAR_ERR_INVALID_ARG
+    assert L.spear_linear_destroy(None) == spear.SPEAR_OK
