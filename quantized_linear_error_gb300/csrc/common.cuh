@@ -1,6 +1,7 @@
 // Shared device helpers for the sm_103a kernels: inline PTX for mbarriers,
 // bulk async copies, warp-level MMA, INT4 unpacking and bounded waits.
 #pragma once
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -99,16 +100,49 @@ SPEAR_DEVINL void bulk_g2s_stream(void* dst, const void* src, unsigned bytes, ui
       : "memory");
 }
 
+// 3-D tiled tensor copy global -> shared (box shape fixed by the map), counted
+// on `bar`. c0 is the innermost coordinate; c0 * element size must be a
+// multiple of 16 bytes.
+SPEAR_DEVINL void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Warm L2 with [src, src + bytes) (16-byte aligned, multiple of 16 bytes).
+SPEAR_DEVINL void prefetch_l2(const void* src, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 SPEAR_DEVINL uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 
+// ---------------------------------------------------------------- shared loads
+// Explicit shared-space loads on 32-bit shared addresses (generic loads of
+// shared memory take the slower L1TEX path). Volatile so that they stay
+// between the mbarrier wait and arrival that bracket their data.
+SPEAR_DEVINL uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+SPEAR_DEVINL uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
 // ---------------------------------------------------------------- warp MMA
 // D = A(16x16, row) * B(16x8, col) + C, bf16 inputs, fp32 accumulate.
+// Not volatile: a pure register operation the compiler may schedule freely.
 SPEAR_DEVINL void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])

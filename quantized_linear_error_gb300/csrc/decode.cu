@@ -3,38 +3,41 @@
 // Recovery", section 2.2A: in the memory-bound decode phase the compensator is
 // fused into the low-bit GEMM so the correction path is a single kernel).
 //
-// Design (one CTA per SM, persistent; 8 consumer warps + 1 producer warp):
-//  * The CTA owns P consecutive 16-row tiles of W. A producer warp streams,
-//    stage by stage along K, the tiles' packed codes, their scale/zero words
-//    and the matching slice of x into shared memory with bulk async copies
-//    (cp.async.bulk + mbarrier transaction counts).
+// Design (one CTA per SM; 8 or 16 consumer warps + 1 producer warp):
+//  * The CTA owns P consecutive 16-row tiles of W. A producer warp streams K
+//    in stages: per stage one bulk copy brings the tiles' packed codes and
+//    scale/zero words (laid out at create as one contiguous run per CTA and
+//    stage, since every bulk copy has a fixed issue cost) and one 3-D tensor
+//    copy brings x[0:Mp, k-slice] with a 128-byte swizzle (tokens past M are
+//    zero-filled by the copy engine), both counted on one mbarrier.
 //  * Consumer warps turn each 32-bit word into four bf16 A-fragment registers
 //    with one LOP3 per pair (codes land in the mantissa of 128 + code) and one
 //    bf16x2 subtraction of 128 + zero, which leaves the exact integer q - z.
 //    Warp MMA (m16n8k16, fp32 accumulate) takes x as the 8-wide N operand
 //    (tokens), and the group scale is applied once per group to the fp32
 //    partial sum.
-//  * The compensator's down-projection z = A x is split over all CTAs before
-//    they start on W; partial sums are added into a workspace with vector
-//    atomics and each CTA then bumps an arrival counter. After its W tiles a
-//    CTA waits (bounded by %globaltimer) for all arrivals, applies the gate
-//    u = alpha * gamma(z) * z, splits u into bf16 hi + lo and adds B u to its
-//    fp32 accumulators with two more MMAs per step, then rounds y to bf16
-//    once. The last CTA to read z clears it for the next call. HBM traffic is
-//    W, scales/zeros, A and B once each.
+//  * A separate compensator warp per CTA runs concurrently with the W stream:
+//    it computes the CTA's share of the down-projection z = A x (split over
+//    all CTAs), adds it into a workspace with vector atomics, bumps an arrival
+//    counter, waits (bounded by %globaltimer) for every CTA's arrival, applies
+//    the gate u = alpha * gamma(z) * z, splits u into bf16 hi + lo in shared
+//    memory and signals the consumers through an mbarrier. The last CTA to
+//    read z clears it for the next call. After their W tiles the consumer
+//    warps add B u to the fp32 accumulators with two more MMAs per step and
+//    round y to bf16 once. HBM traffic is W, scales/zeros, A and B once each.
 #include "internal.h"
 
 namespace spear {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxStages = 8;
+constexpr int kEcWarps = 4;  // compensator warps per CTA
 constexpr int kBarrierBytes = 1024;
+constexpr size_t kSmemCap = 200 * 1024;
 
 struct DecodeParams {
-  const uint4* wq;
-  const uint32_t* sz;
+  const uint8_t* wq;     // decode layout runs
+  const uint32_t* sz;    // per-channel scale/zero words [nt16][16]
   const uint4* a_frag;
   const uint4* b_frag;
   const __nv_bfloat16* x;
@@ -44,16 +47,18 @@ struct DecodeParams {
   int K, N, M, n_groups, rank, gate;
   float alpha;
   int nt16, P, KW, KC, NS, n_stages;
-  uint32_t bytes_x, bytes_w, bytes_sz, stage_bytes;
-  int xs_stride;  // bf16 elements per token row of a staged x slice
+  uint32_t bytes_x, stage_bytes;  // x box bytes (KC * Mp * 2), bytes per stage buffer
   uint64_t wait_ns;
   int skip_arrive;
 };
 
-SPEAR_DEVINL void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory"); }
+template <int NW>
+SPEAR_DEVINL void consumer_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory");
+}
 
 // B fragments (k16 x n8, col) for MT token tiles from a token-major smem
-// buffer: base[token * stride + k].
+// buffer: base[token * stride + k] (used for the gate output u).
 template <int MT>
 SPEAR_DEVINL void load_token_frags(const __nv_bfloat16* base, int stride, int koff, int lane,
                                    uint32_t (&b)[MT][2]) {
@@ -70,6 +75,31 @@ SPEAR_DEVINL void load_token_frags(const __nv_bfloat16* base, int stride, int ko
   }
 }
 
+// B fragments of x from a staged box laid out [k64 block][token][64] with the
+// 128-byte swizzle (16-byte chunk c of token row r sits at chunk c ^ (r & 7)).
+// Plain 32-bit shared loads, which the compiler can schedule around the MMAs
+// (the mbarrier wait and arrival, which clobber memory, still bound them).
+// Lane (g, t) reads token 8n + g at k = koff + 2t and koff + 2t + 8; the XOR
+// with g puts the 8 rows on 8 different chunks, so 32 lanes hit 32 banks.
+// All fragments of one 128-channel unit (8 k16 steps) at once, so that one
+// load latency covers the unit. `lane_base[c]` = box base + 128 g + 4 t +
+// 16 (c ^ g): the lane's address of swizzled chunk c in token row g of the
+// unit's first k64 block; everything else is a compile-time offset.
+template <int MT>
+SPEAR_DEVINL void load_unit_x_frags(const uint32_t (&lane_base)[8], uint32_t (&b)[8][MT][2]) {
+  constexpr int Mp = 8 * MT;
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const int c = (2 * kk) & 7;               // chunk of k16 step kk inside its k64 block
+    const uint32_t blk = (kk >> 2) * Mp * 128;  // second k64 block for kk >= 4
+#pragma unroll
+    for (int n = 0; n < MT; ++n) {
+      b[kk][n][0] = lds32(lane_base[c] + blk + n * 1024);
+      b[kk][n][1] = lds32(lane_base[c + 1] + blk + n * 1024);
+    }
+  }
+}
+
 SPEAR_DEVINL uint32_t word_of(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
@@ -80,16 +110,16 @@ SPEAR_DEVINL float gate_apply(float z, int gate) {
 
 // z += A[:, this CTA's share] x, via warp MMA with A rows as the M side.
 template <int MT>
-SPEAR_DEVINL void ec_project(const DecodeParams& p, int warp, int lane) {
+SPEAR_DEVINL void ec_project(const DecodeParams& p, int ew, int lane) {
   const int kb128 = p.K / 128;
   const int units = (p.rank / 16) * kb128;
   const int u0 = (int)((long)blockIdx.x * units / gridDim.x);
   const int u1 = (int)((long)(blockIdx.x + 1) * units / gridDim.x);
   const int g = lane >> 2, tq = lane & 3;
-  for (int ua = u0 + warp; ua < u1; ua += kConsumerWarps) {
+  for (int ua = u0 + ew; ua < u1; ua += kEcWarps) {
     const int at = ua / kb128, kb = ua % kb128;
-    float c[MT][4] = {};
-#pragma unroll 2
+    float c[2][MT][4] = {};
+#pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       const int k16 = kb * 8 + kk;
       const uint4 af = __ldg(p.a_frag + ((size_t)at * (p.K / 16) + k16) * 32 + lane);
@@ -103,83 +133,176 @@ SPEAR_DEVINL void ec_project(const DecodeParams& p, int warp, int lane) {
           b0 = __ldg(xr);
           b1 = __ldg(xr + 4);
         }
-        mma_bf16_16816(c[n], a, b0, b1);
+        mma_bf16_16816(c[kk & 1][n], a, b0, b1);
       }
     }
 #pragma unroll
     for (int n = 0; n < MT; ++n) {
-      red_add_v2(p.z + (16 * at + g) * 32 + 8 * n + 2 * tq, c[n][0], c[n][1]);
-      red_add_v2(p.z + (16 * at + g + 8) * 32 + 8 * n + 2 * tq, c[n][2], c[n][3]);
+      red_add_v2(p.z + (16 * at + g) * 32 + 8 * n + 2 * tq, c[0][n][0] + c[1][n][0], c[0][n][1] + c[1][n][1]);
+      red_add_v2(p.z + (16 * at + g + 8) * 32 + 8 * n + 2 * tq, c[0][n][2] + c[1][n][2], c[0][n][3] + c[1][n][3]);
     }
   }
 }
 
-template <int MT, int T, bool PC, bool EC>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
+template <int NW, int MT, int T, bool PC, bool EC>
+__global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
+    decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap xmap) {
+  // independent accumulator chains per tile (k16 step kk goes to chain kk % NC)
+  constexpr int NC = (MT == 4 ? 2 : 4) / T > 0 ? (MT == 4 ? 2 : 4) / T : 1;
+  constexpr int Mp = 8 * MT;
+  extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + 16;
   uint64_t* szbar = full + 32;
-  volatile int* flag = reinterpret_cast<volatile int*>(smem + 512);
-  uint8_t* stages = smem + kBarrierBytes;
+  uint64_t* ubar = full + 33;  // compensator warp -> consumers: u is in shared memory
+  // stage buffers start on a 1024-byte boundary (the swizzle pattern of the x
+  // box is defined on absolute shared-memory address bits)
+  const uint32_t s0 = smem_u32(smem + kBarrierBytes);
+  uint8_t* stages = smem + kBarrierBytes + (((s0 + 1023u) & ~1023u) - s0);
   uint32_t* szpc = reinterpret_cast<uint32_t*>(stages + (size_t)p.NS * p.stage_bytes);
+  const int us = p.rank + 8;  // bf16 elements per token row of u
+  __nv_bfloat16* uh = reinterpret_cast<__nv_bfloat16*>(szpc + (PC ? p.P * 16 : 0));
+  __nv_bfloat16* ul = uh + Mp * us;
 
-  constexpr int Mp = 8 * MT;
+  const uint32_t stages_s = smem_u32(stages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile0 = blockIdx.x * p.P;
   const int Pc = min(p.P, p.nt16 - tile0);
   const int K = p.K, KC = p.KC;
+  const DecodeLayout L{K, p.nt16, p.P, PC};
+  const size_t run_full = (size_t)Pc * L.stage_tile_bytes(kDecodeRun);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
+      mbar_init(&empty[s], NW);
     }
     mbar_init(szbar, 1);
+    mbar_init(ubar, kEcWarps);
     fence_mbar_init();
   }
-  // Token rows M..Mp-1 of every staged x slice stay zero (never copied).
-  for (int s = 0; s < p.NS; ++s) {
-    __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(stages + (size_t)s * p.stage_bytes);
-    for (int i = threadIdx.x; i < (Mp - p.M) * p.xs_stride; i += blockDim.x)
-      xs[p.M * p.xs_stride + i] = __float2bfloat16_rn(0.f);
-  }
+  // Token rows M..Mp-1 of the staged x boxes are zero-filled by the copy
+  // engine; in any case they only feed MMA output columns M..Mp-1, which are
+  // never stored.
   __syncthreads();
+  // Let the next kernel in the stream launch now; it only touches its own
+  // weights until its griddepcontrol.wait, which waits for this grid.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // ------------------------------------------------------------ producer warp
-  if (warp == kConsumerWarps) {
-    const uint64_t pol = policy_evict_first();
-    if (PC) {
-      if (lane == 0) mbar_arrive_expect_tx(szbar, Pc * 64);
-      __syncwarp();
-      if (lane < Pc) bulk_g2s(szpc + lane * 16, p.sz + (size_t)(tile0 + lane) * 16, 64, szbar);
-    }
-    for (int i = 0; i < p.n_stages; ++i) {
-      const int slot = i % p.NS;
-      if (i >= p.NS && !mbar_wait_bounded(&empty[slot], ((i / p.NS) - 1) & 1, p.wait_ns)) {
-        if (lane == 0) atomicOr(&p.sync->status, kStatusTimeoutPipe);
-        return;
+  if (warp == NW) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      if (PC) {
+        mbar_arrive_expect_tx(szbar, Pc * 64);
+        bulk_g2s(szpc, p.sz + (size_t)tile0 * 16, Pc * 64, szbar);
       }
-      const int kc = i * KC;
-      const int kcw = min(KC, K - kc);
-      const int units = kcw / 128;
-      const uint32_t bytes = (uint32_t)(p.M * kcw * 2 + Pc * (kcw / 64) * 512 + (PC ? 0 : Pc * units * 64));
-      uint8_t* st = stages + (size_t)slot * p.stage_bytes;
-      if (lane == 0) mbar_arrive_expect_tx(&full[slot], bytes);
+      // Weights (constant since create) of the first NS stages go out before
+      // the wait on the previous kernel; x, which that kernel may produce, after.
+      const int prefetch = min(p.NS, p.n_stages);
+      auto issue_weights = [&](int i) {
+        const int slot = i % p.NS;
+        const uint32_t run = (uint32_t)(Pc * L.stage_tile_bytes(min(KC, K - i * KC)));
+        mbar_arrive_expect_tx(&full[slot], run + p.bytes_x);
+        bulk_g2s_stream(stages + (size_t)slot * p.stage_bytes + p.bytes_x,
+                        p.wq + L.run_offset(blockIdx.x, i * (KC / kDecodeRun)), run, &full[slot], pol);
+      };
+      auto issue_x = [&](int i) {
+        const int slot = i % p.NS;
+        tma_load_3d(stages + (size_t)slot * p.stage_bytes, &xmap, 0, 0, i * (KC / 64), &full[slot]);
+      };
+      for (int i = 0; i < prefetch; ++i) issue_weights(i);
+      if (EC) {
+        // B rows of this CTA's tiles are read with ordinary loads at the end:
+        // start pulling them into L2 now.
+        prefetch_l2(p.b_frag + (size_t)tile0 * (p.rank / 16) * 32, Pc * (p.rank / 16) * 512);
+      }
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      for (int i = 0; i < prefetch; ++i) issue_x(i);
+      for (int i = prefetch; i < p.n_stages; ++i) {
+        const int slot = i % p.NS;
+        if (!mbar_wait_bounded(&empty[slot], ((i / p.NS) - 1) & 1, p.wait_ns)) {
+          atomicOr(&p.sync->status, kStatusTimeoutPipe);
+          break;
+        }
+        issue_weights(i);
+        issue_x(i);
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ compensator warps
+  if (warp > NW) {
+    if constexpr (EC) {
+      const int ew = warp - NW - 1;
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      ec_project<MT>(p, ew, lane);
       __syncwarp();
-      const int ncopies = p.M + Pc * (PC ? 1 : 2);
-      for (int c = lane; c < ncopies; c += 32) {
-        if (c < p.M) {
-          bulk_g2s(st + (size_t)c * p.xs_stride * 2, p.x + (size_t)c * K + kc, kcw * 2, &full[slot]);
-        } else if (c < p.M + Pc) {
-          const int t = c - p.M;
-          bulk_g2s_stream(st + p.bytes_x + (size_t)t * (KC / 64) * 512,
-                          p.wq + ((size_t)(tile0 + t) * (K / 64) + kc / 64) * 32, (kcw / 64) * 512, &full[slot],
-                          pol);
-        } else {
-          const int t = c - p.M - Pc;
-          bulk_g2s(st + p.bytes_x + p.bytes_w + (size_t)t * (KC / 128) * 64,
-                   p.sz + ((size_t)(tile0 + t) * p.n_groups + kc / 128) * 16, units * 64, &full[slot]);
+      if (lane == 0 && !p.skip_arrive) {
+        __threadfence();
+        atomicAdd(&p.sync->arrive, 1u);
+      }
+      bool arrived = false;
+      if (lane == 0) {
+        const unsigned target = gridDim.x * kEcWarps;
+        arrived = ld_acquire_gpu(&p.sync->arrive) >= target;
+        if (!arrived) {
+          const uint64_t t0 = globaltimer();
+          while (!(arrived = ld_acquire_gpu(&p.sync->arrive) >= target))
+            if (globaltimer() - t0 > p.wait_ns) break;
+        }
+        if (!arrived) atomicOr(&p.sync->status, kStatusTimeoutZ);
+      }
+      arrived = __shfl_sync(0xffffffffu, arrived ? 1 : 0, 0) != 0;
+      // u = alpha * gamma(z) * z for 4 tokens per float4 of z ([rank][32] fp32),
+      // eight independent loads in flight per lane
+      const int nv = p.rank * (Mp / 4);
+      for (int base = ew * 32 + lane; base < nv; base += kEcWarps * 32 * 8) {
+        float4 v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int idx = base + q * kEcWarps * 32;
+          v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (arrived && idx < nv)
+            v[q] = __ldcg(reinterpret_cast<const float4*>(p.z + (idx / (Mp / 4)) * 32 + (idx % (Mp / 4)) * 4));
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int idx = base + q * kEcWarps * 32;
+          if (idx < nv) {
+            const int j = idx / (Mp / 4), m0 = (idx % (Mp / 4)) * 4;
+            const float zz[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float uval = (m0 + e < p.M) ? p.alpha * gate_apply(zz[e], p.gate) : 0.f;
+              __nv_bfloat16 hi, lo;
+              split_bf16(uval, hi, lo);
+              uh[(m0 + e) * us + j] = hi;
+              ul[(m0 + e) * us + j] = lo;
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ubar);  // release: this warp's share of u is visible to the consumers
+      // The last compensator warp (over all CTAs) to have read z clears it and
+      // the counters for the next call.
+      int last = 0;
+      if (lane == 0 && arrived) {
+        __threadfence();
+        last = atomicAdd(&p.sync->depart, 1u) == gridDim.x * kEcWarps - 1;
+        __threadfence();
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        for (int idx = lane; idx < p.rank * 32; idx += 32) p.z[idx] = 0.f;
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          p.sync->arrive = 0;
+          p.sync->depart = 0;
+          __threadfence();
         }
       }
     }
@@ -189,24 +312,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   // ------------------------------------------------------------ consumer warps
   const int pw_i = warp / p.KW, kw_i = warp % p.KW;
   const int g = lane >> 2, tq = lane & 3;
-
-  if constexpr (EC) {
-    ec_project<MT>(p, warp, lane);
-    consumer_bar();
-    if (threadIdx.x == 0 && !p.skip_arrive) {
-      __threadfence();
-      atomicAdd(&p.sync->arrive, 1u);
-    }
-  }
+  // x box addressing: token row g, byte 4 t, and the swizzled chunk offsets
+  const uint32_t lane_off = g * 128 + 4 * tq;
+  uint32_t swz[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) swz[c] = (uint32_t)((c ^ g) << 4);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   float acc[T][MT][4];
-  float accg[T][MT][4];
+  float accg[T][NC][MT][4];
 #pragma unroll
   for (int t = 0; t < T; ++t)
 #pragma unroll
     for (int n = 0; n < MT; ++n)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[t][n][e] = accg[t][n][e] = 0.f;
+      for (int e = 0; e < 4; ++e) {
+        acc[t][n][e] = 0.f;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) accg[t][c][n][e] = 0.f;
+      }
 
   uint32_t zzpc[T][2];
   float spc[T][2];
@@ -230,12 +354,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       ok = false;
       break;
     }
-    const uint8_t* st = stages + (size_t)slot * p.stage_bytes;
-    const __nv_bfloat16* xs = reinterpret_cast<const __nv_bfloat16*>(st);
-    const uint4* wsm = reinterpret_cast<const uint4*>(st + p.bytes_x);
-    const uint32_t* szs = reinterpret_cast<const uint32_t*>(st + p.bytes_x + p.bytes_w);
-    const int units = min(KC, K - i * KC) / 128;
-    for (int u = kw_i; u < units; u += p.KW) {
+    const uint32_t st = stages_s + (uint32_t)slot * p.stage_bytes;
+    const int kcw = min(KC, K - i * KC);
+    const int units = kcw / 128;
+    // unit u of stage i is unit i * (KC / 128) + u of the whole K range; the
+    // KW warps of a row group take those round-robin
+    int u0 = kw_i - (i * (KC / 128)) % p.KW;
+    if (u0 < 0) u0 += p.KW;
+    for (int u = u0; u < units; u += p.KW) {
+      // unit u is half uin of layout run sr inside this stage
+      const int sr = u >> 1, uin = u & 1;
+      const int kcw_r = min(kDecodeRun, kcw - sr * kDecodeRun);
+      const uint32_t wsm = st + p.bytes_x + sr * (uint32_t)run_full;
+      const uint32_t szs = wsm + (uint32_t)(Pc * (kcw_r / 64) * 512);
       uint4 wv[T][2];
       uint32_t zz[T][2];
       float sc[T][2];
@@ -243,11 +374,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       for (int t = 0; t < T; ++t) {
         const int tl = pw_i * T + t;
         if (tl < Pc) {
-          wv[t][0] = wsm[(tl * (KC / 64) + 2 * u) * 32 + lane];
-          wv[t][1] = wsm[(tl * (KC / 64) + 2 * u + 1) * 32 + lane];
+          wv[t][0] = lds128(wsm + ((tl * (kcw_r / 64) + 2 * uin) * 32 + lane) * 16);
+          wv[t][1] = lds128(wsm + ((tl * (kcw_r / 64) + 2 * uin + 1) * 32 + lane) * 16);
           if constexpr (!PC) {
-            const uint32_t w0 = szs[(tl * (KC / 128) + u) * 16 + g];
-            const uint32_t w1 = szs[(tl * (KC / 128) + u) * 16 + g + 8];
+            const uint32_t w0 = lds32(szs + ((tl * (kcw_r / 128) + uin) * 16 + g) * 4);
+            const uint32_t w1 = lds32(szs + ((tl * (kcw_r / 128) + uin) * 16 + g + 8) * 4);
             zz[t][0] = biased_zero_x2(w0 >> 16);
             zz[t][1] = biased_zero_x2(w1 >> 16);
             sc[t][0] = bf16_bits_to_float(w0 & 0xFFFF);
@@ -258,10 +389,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
           }
         }
       }
+      uint32_t lane_base[8];
+      const uint32_t ub = st + (uint32_t)(2 * u) * (Mp * 128) + lane_off;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) lane_base[c] = ub + swz[c];
+      uint32_t bb[8][MT][2];
+      load_unit_x_frags<MT>(lane_base, bb);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        uint32_t b[MT][2];
-        load_token_frags<MT>(xs, p.xs_stride, u * 128 + kk * 16, lane, b);
+        const uint32_t(&b)[MT][2] = bb[kk];
 #pragma unroll
         for (int t = 0; t < T; ++t) {
           const int tl = pw_i * T + t;
@@ -272,23 +408,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
                                    bf16x2_sub(int4_pair_to_bf16x2_biased(w >> 8), zz[t][0]),
                                    bf16x2_sub(int4_pair_to_bf16x2_biased(w >> 12), zz[t][1])};
 #pragma unroll
-            for (int n = 0; n < MT; ++n) mma_bf16_16816(PC ? acc[t][n] : accg[t][n], a, b[n][0], b[n][1]);
+            for (int n = 0; n < MT; ++n) mma_bf16_16816(accg[t][kk % NC][n], a, b[n][0], b[n][1]);
           }
         }
       }
-      if constexpr (!PC) {
+      // fold the chains; grouped scales apply once per group here
 #pragma unroll
-        for (int t = 0; t < T; ++t)
+      for (int t = 0; t < T; ++t)
 #pragma unroll
-          for (int n = 0; n < MT; ++n) {
-            acc[t][n][0] = fmaf(sc[t][0], accg[t][n][0], acc[t][n][0]);
-            acc[t][n][1] = fmaf(sc[t][0], accg[t][n][1], acc[t][n][1]);
-            acc[t][n][2] = fmaf(sc[t][1], accg[t][n][2], acc[t][n][2]);
-            acc[t][n][3] = fmaf(sc[t][1], accg[t][n][3], acc[t][n][3]);
+        for (int n = 0; n < MT; ++n)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) accg[t][n][e] = 0.f;
+          for (int e = 0; e < 4; ++e) {
+            float v = accg[t][0][n][e];
+#pragma unroll
+            for (int c = 1; c < NC; ++c) v += accg[t][c][n][e];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) accg[t][c][n][e] = 0.f;
+            if constexpr (PC)
+              acc[t][n][e] += v;
+            else
+              acc[t][n][e] = fmaf(sc[t][e >> 1], v, acc[t][n][e]);
           }
-      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
@@ -299,18 +439,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
 #pragma unroll
     for (int t = 0; t < T; ++t)
 #pragma unroll
-      for (int n = 0; n < MT; ++n) {
-        acc[t][n][0] *= spc[t][0];
-        acc[t][n][1] *= spc[t][0];
-        acc[t][n][2] *= spc[t][1];
-        acc[t][n][3] *= spc[t][1];
-      }
+      for (int n = 0; n < MT; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[t][n][e] *= spc[t][e >> 1];
   }
 
   // ------------------------------------------------------------ reduction over K warps
-  consumer_bar();  // every warp is done with the stages: reuse them
+  consumer_bar<NW>();  // every warp is done with the stages: reuse them
   float* red = reinterpret_cast<float*>(stages);
-  const size_t red_floats = (size_t)p.P * p.KW * 32 * 4 * MT;
 #pragma unroll
   for (int t = 0; t < T; ++t) {
     const int tl = pw_i * T + t;
@@ -323,59 +459,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     }
   }
 
-  // ------------------------------------------------------------ compensator gate
-  const int us = p.rank + 8;  // bf16 elements per token row of u
-  __nv_bfloat16* uh = reinterpret_cast<__nv_bfloat16*>(red + red_floats);
-  __nv_bfloat16* ul = uh + Mp * us;
+  // ------------------------------------------------------------ compensator term
   bool ec_ok = false;
-  if constexpr (EC) {
-    if (threadIdx.x == 0) {
-      bool arrived = ld_acquire_gpu(&p.sync->arrive) >= gridDim.x;
-      if (!arrived) {
-        const uint64_t t0 = globaltimer();
-        while (!(arrived = ld_acquire_gpu(&p.sync->arrive) >= gridDim.x))
-          if (globaltimer() - t0 > p.wait_ns) break;
-      }
-      if (!arrived) atomicOr(&p.sync->status, kStatusTimeoutZ);
-      flag[0] = arrived ? 1 : 0;
-    }
-    consumer_bar();
-    ec_ok = flag[0] != 0;
-    for (int idx = threadIdx.x; idx < Mp * p.rank; idx += kConsumerWarps * 32) {
-      const int m = idx / p.rank, j = idx % p.rank;
-      float v = 0.f;
-      if (ec_ok && m < p.M) v = p.alpha * gate_apply(__ldcg(p.z + j * 32 + m), p.gate);
-      __nv_bfloat16 hi, lo;
-      split_bf16(v, hi, lo);
-      uh[m * us + j] = hi;
-      ul[m * us + j] = lo;
-    }
-    consumer_bar();
-    if (threadIdx.x == 0) {
-      int last = 0;
-      if (ec_ok) {
-        __threadfence();
-        last = atomicAdd(&p.sync->depart, 1u) == gridDim.x - 1;
-        __threadfence();
-      }
-      flag[1] = last;
-    }
-    consumer_bar();
-    if (flag[1]) {  // last reader: clear z and the counters for the next call
-      for (int idx = threadIdx.x; idx < p.rank * 32; idx += kConsumerWarps * 32) p.z[idx] = 0.f;
-      consumer_bar();
-      if (threadIdx.x == 0) {
-        p.sync->arrive = 0;
-        p.sync->depart = 0;
-        __threadfence();
-      }
-    }
-  } else {
-    consumer_bar();
-  }
+  if constexpr (EC) ec_ok = mbar_wait_bounded(ubar, 0, 2 * p.wait_ns);
+  consumer_bar<NW>();  // partial sums of all K warps are in shared memory
 
   // ------------------------------------------------------------ finalize tiles
-  for (int tl = warp; tl < Pc; tl += kConsumerWarps) {
+  for (int tl = warp; tl < Pc; tl += NW) {
     float c[MT][4];
 #pragma unroll
     for (int n = 0; n < MT; ++n)
@@ -421,23 +511,36 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   }
 }
 
-template <int MT, int T, bool PC, bool EC>
-cudaError_t launch_one(const DecodeParams& p, int grid, size_t smem, cudaStream_t st) {
+template <int NW, int MT, int T, bool PC, bool EC>
+cudaError_t launch_one(const DecodeParams& p, const CUtensorMap& xmap, int grid, size_t smem, cudaStream_t st) {
   static bool configured = false;
-  auto k = decode_kernel<MT, T, PC, EC>;
+  auto k = decode_kernel<NW, MT, T, PC, EC>;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  k<<<grid, kThreads, smem, st>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3((NW + 1 + kEcWarps) * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, p, xmap);
 }
 
-template <int MT, int T>
-cudaError_t launch_mt_t(const DecodeParams& p, bool pc, bool ec, int grid, size_t smem, cudaStream_t st) {
-  if (pc) return ec ? launch_one<MT, T, true, true>(p, grid, smem, st) : launch_one<MT, T, true, false>(p, grid, smem, st);
-  return ec ? launch_one<MT, T, false, true>(p, grid, smem, st) : launch_one<MT, T, false, false>(p, grid, smem, st);
+template <int NW, int MT, int T>
+cudaError_t launch_t(const DecodeParams& p, const CUtensorMap& m, bool pc, bool ec, int grid, size_t smem,
+                     cudaStream_t st) {
+  if (pc)
+    return ec ? launch_one<NW, MT, T, true, true>(p, m, grid, smem, st)
+              : launch_one<NW, MT, T, true, false>(p, m, grid, smem, st);
+  return ec ? launch_one<NW, MT, T, false, true>(p, m, grid, smem, st)
+            : launch_one<NW, MT, T, false, false>(p, m, grid, smem, st);
 }
 
 }  // namespace
@@ -451,14 +554,12 @@ spear_status_t spear_launch_decode(spear_linear_s* h, const __nv_bfloat16* x, __
   const int MT = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
   const int Mp = 8 * MT;
   const bool ec = h->rank > 0;
-  const int P = (h->nt16 + h->sm_count - 1) / h->sm_count;
+  const int P = h->dec_P;
+  int NW, T, KW, KC;
+  decode_plan(P, h->K, M, &NW, &T, &KW, &KC);
+  if (P > T * NW) return SPEAR_ERR_UNSUPPORTED;
   const int grid = (h->nt16 + P - 1) / P;
-  const int T = P > 4 ? 2 : 1;
-  int pw = 1;
-  while (pw < (P + T - 1) / T) pw *= 2;
-  const int KW = kConsumerWarps / pw;
-  int KC = 128 * KW < 256 ? 256 : 128 * KW;
-  if (KC > h->K) KC = h->K;
+  const DecodeLayout L{h->K, h->nt16, P, h->per_channel};
 
   p.wq = h->wq_dec;
   p.sz = h->sz_dec;
@@ -479,11 +580,8 @@ spear_status_t spear_launch_decode(spear_linear_s* h, const __nv_bfloat16* x, __
   p.P = P;
   p.KW = KW;
   p.KC = KC;
-  p.xs_stride = KC + 8;
-  p.bytes_x = (uint32_t)(((size_t)Mp * p.xs_stride * 2 + 127) / 128 * 128);
-  p.bytes_w = (uint32_t)((size_t)P * (KC / 64) * 512);
-  p.bytes_sz = h->per_channel ? 0u : (uint32_t)((size_t)P * (KC / 128) * 64);
-  p.stage_bytes = (p.bytes_x + p.bytes_w + p.bytes_sz + 127) / 128 * 128;
+  p.bytes_x = (uint32_t)(KC * Mp * 2);
+  p.stage_bytes = (uint32_t)((p.bytes_x + P * L.stage_tile_bytes(KC) + 1023) / 1024 * 1024);
   p.n_stages = (h->K + KC - 1) / KC;
   p.wait_ns = h->wait_ns;
   p.skip_arrive = h->skip_arrive;
@@ -491,24 +589,29 @@ spear_status_t spear_launch_decode(spear_linear_s* h, const __nv_bfloat16* x, __
   const size_t red_bytes = (size_t)P * KW * 32 * 4 * MT * 4;
   const size_t u_bytes = ec ? (size_t)2 * Mp * (h->rank + 8) * 2 : 0;
   const size_t pc_bytes = h->per_channel ? (size_t)P * 64 : 0;
-  const size_t budget = 227 * 1024 - kBarrierBytes - pc_bytes;
+  // barriers, alignment slack, per-channel words, u (hi and lo)
+  const size_t fixed = kBarrierBytes + 1024 + pc_bytes + u_bytes;
+  const size_t budget = kSmemCap > fixed ? kSmemCap - fixed : 0;
   int NS = (int)(budget / p.stage_bytes);
   if (NS > kMaxStages) NS = kMaxStages;
-  if (NS > p.n_stages) NS = p.n_stages > 1 ? p.n_stages : 1;
-  while ((size_t)NS * p.stage_bytes < red_bytes + u_bytes && (size_t)(NS + 1) * p.stage_bytes <= budget) ++NS;
-  if (NS < 1 || (size_t)NS * p.stage_bytes < red_bytes + u_bytes) return SPEAR_ERR_UNSUPPORTED;
+  if (NS > p.n_stages) NS = p.n_stages;
+  while ((size_t)NS * p.stage_bytes < red_bytes) ++NS;  // the reduction reuses the stage area
+  if (NS < 1 || fixed + (size_t)NS * p.stage_bytes > 227 * 1024) return SPEAR_ERR_UNSUPPORTED;
   p.NS = NS;
-  const size_t smem = kBarrierBytes + (size_t)NS * p.stage_bytes + pc_bytes;
+  const size_t smem = fixed + (size_t)NS * p.stage_bytes;
 
+  CUtensorMap xmap;
+  if (!encode_x_map(&xmap, x, M, h->K, Mp, KC)) return SPEAR_ERR_CUDA;
+
+  const bool pc = h->per_channel;
   cudaError_t e;
+  // 16 consumer warps hold at most 16 tiles with T = 1 (create limits P to 16)
   if (MT == 1)
-    e = T == 1 ? launch_mt_t<1, 1>(p, h->per_channel, ec, grid, smem, stream)
-               : launch_mt_t<1, 2>(p, h->per_channel, ec, grid, smem, stream);
+    e = launch_t<16, 1, 1>(p, xmap, pc, ec, grid, smem, stream);
   else if (MT == 2)
-    e = T == 1 ? launch_mt_t<2, 1>(p, h->per_channel, ec, grid, smem, stream)
-               : launch_mt_t<2, 2>(p, h->per_channel, ec, grid, smem, stream);
+    e = launch_t<16, 2, 1>(p, xmap, pc, ec, grid, smem, stream);
   else
-    e = T == 1 ? launch_mt_t<4, 1>(p, h->per_channel, ec, grid, smem, stream)
-               : launch_mt_t<4, 2>(p, h->per_channel, ec, grid, smem, stream);
+    e = T == 1 ? launch_t<8, 4, 1>(p, xmap, pc, ec, grid, smem, stream)
+               : launch_t<8, 4, 2>(p, xmap, pc, ec, grid, smem, stream);
   return e == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
 }

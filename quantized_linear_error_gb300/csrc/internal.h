@@ -12,14 +12,25 @@
 //
 // Decode layout (warp MMA m16n8k16 fragments). Rows are grouped in tiles of
 // 16. For a tile and a block of 64 input channels, lane l = 4g + t holds one
-// uint4; word s (k16 step s of the block) packs the eight codes that lane
-// feeds to the MMA A fragment, nibble i at bits 4i..4i+3:
+// uint4 (a 512-byte "k64 block" per tile); word s (k16 step s of the block)
+// packs the eight codes that lane feeds to the MMA A fragment, nibble i at
+// bits 4i..4i+3:
 //   i: 0 (g, 2t)  1 (g+8, 2t)  2 (g, 2t+8)  3 (g+8, 2t+8)
 //      4 (g, 2t+1) 5 (g+8, 2t+1) 6 (g, 2t+9) 7 (g+8, 2t+9)
 // (row within the tile, k within the 16-step), so (w >> 4j) & 0x000F000F
-// yields A-fragment register j as a bf16 pair.
-//   wq_dec  uint4 [nt16][K/64][32]
-//   sz_dec  u32   [nt16][n_groups][16]   bits 0..15 bf16 scale, 16..31 bf16(128 + zero)
+// yields A-fragment register j as a bf16 pair. Scale/zero words are u32:
+// bits 0..15 bf16 scale, 16..31 bf16(128 + zero), one 64-byte block of 16 rows
+// per (tile, group).
+//
+// The blocks are ordered for the decode kernel's schedule, fixed at create:
+// CTA c owns tiles [c*P, c*P + Pc) and reads K in runs of 256 channels;
+// everything one CTA needs for one run is contiguous,
+//   [W: Pc tiles x kcw/64 k64 blocks][S: Pc tiles x kcw/128 group blocks]
+// (kcw = channels in the run, 256 except maybe the last; S absent for
+// per-channel scales), and a CTA's runs follow each other in K order, so a
+// pipeline stage of any whole number of runs is a single bulk copy.
+//   wq_dec  bytes, nt16 * dec_tile_bytes
+//   sz_dec  u32 [nt16][16] (per-channel only)
 //   a_dec   uint4 [rank/16][K/16][32]    A in A-fragment order (bf16 pairs)
 //   b_dec   uint4 [nt16][rank/16][32]    B in A-fragment order (bf16 pairs)
 //
@@ -41,7 +52,10 @@ struct spear_linear_s {
   bool per_channel = false;
 
   int nt16 = 0, nt128 = 0;
-  uint4* wq_dec = nullptr;
+  // decode schedule (see the layout comment)
+  int dec_P = 0;
+  size_t dec_tile_bytes = 0;  // one tile over all of K: W blocks plus (grouped) scale blocks
+  uint8_t* wq_dec = nullptr;
   uint32_t* sz_dec = nullptr;
   uint4* a_dec = nullptr;
   uint4* b_dec = nullptr;
@@ -65,8 +79,61 @@ struct spear_linear_s {
 };
 
 constexpr int kDecodeMaxTokens = 32;
-constexpr int kDecodeMaxTilesPerCta = 16;
+
+constexpr int kDecodeRun = 256;  // channels per layout run
+
+// Byte offset, inside wq_dec, of tile `tile`'s k64 block `kb` (lane data
+// follows at 16 bytes per lane) and of its scale block for group `grp`.
+struct DecodeLayout {
+  int K, nt16, P;
+  bool per_channel;
+  static constexpr int KC = kDecodeRun;
+  __host__ __device__ size_t stage_tile_bytes(int kcw) const {
+    return (size_t)(kcw / 64) * 512 + (per_channel ? 0 : (size_t)(kcw / 128) * 64);
+  }
+  __host__ __device__ size_t tile_bytes() const { return stage_tile_bytes(K); }
+  __host__ __device__ int pc(int cta) const { return min(P, nt16 - cta * P); }
+  // start of (cta, stage) run
+  __host__ __device__ size_t run_offset(int cta, int stage) const {
+    return (size_t)cta * P * tile_bytes() + (size_t)pc(cta) * stage * stage_tile_bytes(KC);
+  }
+  __host__ __device__ int kcw(int stage) const { return min(KC, K - stage * KC); }
+  __host__ __device__ size_t w_offset(int tile, int kb) const {
+    const int cta = tile / P, tl = tile % P, stage = (kb * 64) / KC, kin = kb - stage * (KC / 64);
+    return run_offset(cta, stage) + ((size_t)tl * (kcw(stage) / 64) + kin) * 512;
+  }
+  __host__ __device__ size_t sz_offset(int tile, int grp) const {
+    const int cta = tile / P, tl = tile % P, stage = (grp * 128) / KC, gin = grp - stage * (KC / 128);
+    const int w = kcw(stage);
+    return run_offset(cta, stage) + (size_t)pc(cta) * (w / 64) * 512 + ((size_t)tl * (w / 128) + gin) * 64;
+  }
+};
+
+// Tiles of 16 rows per CTA (grid <= SM count); fixed at create.
+inline int decode_tiles_per_cta(int nt16, int sm_count) { return (nt16 + sm_count - 1) / sm_count; }
+
+// Per-call decode schedule: NW consumer warps (16 when M <= 16, else 8), T
+// tiles per warp, KW warps splitting K, KC channels per pipeline stage (a
+// whole number of layout runs).
+inline void decode_plan(int P, int K, int M, int* NW, int* T, int* KW, int* KC) {
+  *NW = M <= 16 ? 16 : 8;
+  *T = P > *NW ? 2 : 1;
+  const int pw = (P + *T - 1) / *T;  // warps along rows
+  *KW = *NW / pw;                    // warps along K; 128-channel units go round-robin
+  // Two units per K warp per stage: measured faster than smaller stages,
+  // whose fixed per-stage costs (two copies, barrier round trips) dominate.
+  int kc = kDecodeRun * *KW;
+  const int kr = (K + kDecodeRun - 1) / kDecodeRun * kDecodeRun;
+  if (kc > kr) kc = kr;
+  *KC = kc;
+}
+constexpr int kDecodeMaxTilesPerCta = 16;  // 8 warps x T = 2 tiles (M > 16)
 constexpr size_t kZDecFloats = 256 * 32;
+
+// Tensor map over x [M][K] bf16 viewed as {64, M, K/64} (strides K*2 and 128
+// bytes) with box {64, Mp, KC/64} and the 128-byte swizzle. Returns false if
+// the driver entry point is unavailable or rejects the map.
+bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int Mp, int KC);
 
 spear_status_t spear_launch_decode(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,
                                    cudaStream_t stream);

@@ -21,9 +21,9 @@ __device__ __forceinline__ uint32_t user_sz(const uint16_t* s, const uint8_t* z,
   return sb | ((0x4300u | zp) << 16);
 }
 
-__global__ void repack_w_decode(const uint8_t* __restrict__ q, int K, int N, int nt16, uint4* __restrict__ out) {
+__global__ void repack_w_decode(const uint8_t* __restrict__ q, int K, int N, DecodeLayout L, uint8_t* __restrict__ out) {
   const int kb64 = K / 64;
-  const long total = (long)nt16 * kb64 * 32;
+  const long total = (long)L.nt16 * kb64 * 32;
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
     const int lane = i % 32;
     const int kb = (i / 32) % kb64;
@@ -38,7 +38,18 @@ __global__ void repack_w_decode(const uint8_t* __restrict__ q, int K, int N, int
              user_code(q, K, N, r1, k + 1) << 20 | user_code(q, K, N, r0, k + 9) << 24 |
              user_code(q, K, N, r1, k + 9) << 28;
     }
-    out[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(out + L.w_offset(tile, kb) + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+__global__ void repack_sz_decode(const uint16_t* __restrict__ s, const uint8_t* __restrict__ z, int n_groups, int N,
+                                 DecodeLayout L, uint8_t* __restrict__ out) {
+  const long total = (long)L.nt16 * n_groups * 16;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+    const int rl = i % 16;
+    const int g = (i / 16) % n_groups;
+    const int tile = i / (16L * n_groups);
+    *reinterpret_cast<uint32_t*>(out + L.sz_offset(tile, g) + rl * 4) = user_sz(s, z, n_groups, N, tile * 16 + rl, g);
   }
 }
 
@@ -107,21 +118,21 @@ __device__ __forceinline__ __nv_bfloat16 scaled(uint32_t diff_bits16, float s) {
   return __float2bfloat16_rn(bf16_bits_to_float(diff_bits16) * s);
 }
 
-__global__ void dequant_from_decode(const uint4* __restrict__ wq, const uint32_t* __restrict__ sz, int K, int N,
-                                    int nt16, int G, int n_groups, __nv_bfloat16* __restrict__ out) {
+__global__ void dequant_from_decode(const uint8_t* __restrict__ wq, const uint32_t* __restrict__ sz_pc, int K, int N,
+                                    DecodeLayout L, __nv_bfloat16* __restrict__ out) {
   const int kb64 = K / 64;
-  const long total = (long)nt16 * kb64 * 32;
+  const long total = (long)L.nt16 * kb64 * 32;
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
     const int lane = i % 32;
     const int kb = (i / 32) % kb64;
     const int tile = i / (32L * kb64);
     const int g = lane >> 2, t = lane & 3;
-    const int grp = (kb * 64) / G;
-    const uint32_t sz0 = sz[((size_t)tile * n_groups + grp) * 16 + g];
-    const uint32_t sz1 = sz[((size_t)tile * n_groups + grp) * 16 + g + 8];
+    const uint32_t* szb = L.per_channel ? sz_pc + (size_t)tile * 16
+                                        : reinterpret_cast<const uint32_t*>(wq + L.sz_offset(tile, (kb * 64) / 128));
+    const uint32_t sz0 = szb[g], sz1 = szb[g + 8];
     const uint32_t zz0 = biased_zero_x2(sz0 >> 16), zz1 = biased_zero_x2(sz1 >> 16);
     const float s0 = bf16_bits_to_float(sz0 & 0xFFFF), s1 = bf16_bits_to_float(sz1 & 0xFFFF);
-    const uint4 v = wq[i];
+    const uint4 v = *reinterpret_cast<const uint4*>(wq + L.w_offset(tile, kb) + lane * 16);
     const uint32_t words[4] = {v.x, v.y, v.z, v.w};
     const int r0 = tile * 16 + g, r1 = r0 + 8;
     for (int s = 0; s < 4; ++s) {
@@ -188,10 +199,16 @@ spear_status_t spear_build_layouts(spear_linear_s* h, const spear_linear_desc_t*
   const uint16_t* s = static_cast<const uint16_t*>(d->scales);
   const int T = 256;
   long n;
+  const DecodeLayout L{K, h->nt16, h->dec_P, h->per_channel};
   n = (long)h->nt16 * (K / 64) * 32;
-  repack_w_decode<<<grid_for(n, T), T, 0, st>>>(d->qweight, K, N, h->nt16, h->wq_dec);
-  n = (long)h->nt16 * h->n_groups * 16;
-  repack_sz<<<grid_for(n, T), T, 0, st>>>(s, d->zeros, h->n_groups, N, h->nt16, 16, h->sz_dec);
+  repack_w_decode<<<grid_for(n, T), T, 0, st>>>(d->qweight, K, N, L, h->wq_dec);
+  if (h->per_channel) {
+    n = (long)h->nt16 * 16;
+    repack_sz<<<grid_for(n, T), T, 0, st>>>(s, d->zeros, 1, N, h->nt16, 16, h->sz_dec);
+  } else {
+    n = (long)h->nt16 * h->n_groups * 16;
+    repack_sz_decode<<<grid_for(n, T), T, 0, st>>>(s, d->zeros, h->n_groups, N, L, h->wq_dec);
+  }
   n = (long)h->nt128 * (K / 64) * 1024;
   repack_w_prefill<<<grid_for(n, T), T, 0, st>>>(d->qweight, K, N, h->nt128, h->wq_pre);
   n = (long)h->nt128 * h->n_groups * 128;
@@ -214,9 +231,9 @@ spear_status_t spear_build_layouts(spear_linear_s* h, const spear_linear_desc_t*
 spear_status_t spear_launch_dequant(spear_linear_s* h, int path, __nv_bfloat16* out, cudaStream_t st) {
   const int T = 256;
   if (path == 0) {
+    const DecodeLayout L{h->K, h->nt16, h->dec_P, h->per_channel};
     long n = (long)h->nt16 * (h->K / 64) * 32;
-    dequant_from_decode<<<grid_for(n, T), T, 0, st>>>(h->wq_dec, h->sz_dec, h->K, h->N, h->nt16, h->G,
-                                                      h->n_groups, out);
+    dequant_from_decode<<<grid_for(n, T), T, 0, st>>>(h->wq_dec, h->sz_dec, h->K, h->N, L, out);
   } else {
     long n = (long)h->nt128 * (h->K / 64) * 1024;
     dequant_from_prefill<<<grid_for(n, T), T, 0, st>>>(h->wq_pre, h->sz_pre, h->K, h->N, h->nt128, h->G,

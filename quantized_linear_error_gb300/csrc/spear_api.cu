@@ -1,9 +1,33 @@
 // C ABI of the library: argument checking, handle lifetime, phase dispatch.
 // All arithmetic of the layer runs in the kernels of decode.cu, prefill.cu and
 // layout.cu; this file only validates, allocates at create and launches.
+#include <cudaTypedefs.h>
+
+#include <mutex>
 #include <new>
 
 #include "internal.h"
+
+bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int Mp, int KC) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!encode) return false;
+  const cuuint64_t dims[3] = {64, (cuuint64_t)M, (cuuint64_t)(K / 64)};
+  const cuuint64_t strides[2] = {(cuuint64_t)K * 2, 128};
+  const cuuint32_t box[3] = {64, (cuuint32_t)Mp, (cuuint32_t)(KC / 64)};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 namespace {
 
@@ -79,6 +103,8 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
     delete h;
     return SPEAR_ERR_UNSUPPORTED;
   }
+  h->dec_P = decode_tiles_per_cta(h->nt16, h->sm_count);
+  h->dec_tile_bytes = DecodeLayout{h->K, h->nt16, h->dec_P, h->per_channel}.tile_bytes();
 
   const size_t K = h->K, r = h->rank, mt = h->max_tokens;
   const size_t ws_bytes = sizeof(spear::SyncWords) + kZDecFloats * 4 + mt * r * 4 + mt * r * 2 + 256;
@@ -86,8 +112,8 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
   auto A = [&](cudaError_t x) {
     if (e == cudaSuccess) e = x;
   };
-  A(alloc(&h->wq_dec, (size_t)h->nt16 * (K / 64) * 32 * 16));
-  A(alloc(&h->sz_dec, (size_t)h->nt16 * h->n_groups * 16 * 4));
+  A(alloc(&h->wq_dec, (size_t)h->nt16 * h->dec_tile_bytes));
+  if (h->per_channel) A(alloc(&h->sz_dec, (size_t)h->nt16 * 16 * 4));
   A(alloc(&h->wq_pre, (size_t)h->nt128 * (K / 64) * 1024 * 4));
   A(alloc(&h->sz_pre, (size_t)h->nt128 * h->n_groups * 128 * 4));
   if (r > 0) {
