@@ -135,6 +135,12 @@ constexpr size_t kZDecFloats = 256 * 32;
 // the driver entry point is unavailable or rejects the map.
 bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int Mp, int KC);
 
+// 2-D tensor map over a row-major bf16 matrix (`inner` elements per row,
+// `rows` rows, `row_bytes` apart) with a {box_inner, box_rows} box and the
+// 128-byte swizzle; out-of-range elements read as zero.
+bool encode_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                    uint32_t box_inner, uint32_t box_rows);
+
 spear_status_t spear_launch_decode(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,
                                    cudaStream_t stream);
 spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,

@@ -1,4 +1,372 @@
+// Prefill-phase path ("SPEAR: A System for Post-Quantization Error-Adaptive
+// Recovery", section 2.2A: for M > 1 the layer is compute-bound, and the
+// compensator runs as a separate small kernel next to the low-bit GEMM).
+//
+// Two launches of one warp-specialised tcgen05 GEMM kernel, D = A B^T with
+// bf16 operands in 128-byte-swizzled shared memory and an fp32 accumulator
+// in tensor memory (128 rows x TN columns, one tile per CTA):
+//
+//  1. Compensator pre-kernel (rank > 0): A = x (128 tokens per tile), B = the
+//     compensator's A matrix (rank rows), both by TMA; the epilogue applies
+//     the gate and writes u' = bf16(alpha * gamma(z) * z), z = A x, [M][rank].
+//  2. Main kernel: A = W rows, dequantised in the CTA: the TMA warp brings
+//     the packed INT4 tile and its scale/zero words, four warps turn them into
+//     bf16 (q - z) * s (one rounding, the exported dequantised value) and
+//     write the swizzled A tile; B = x tokens by TMA. After the K blocks of W
+//     come ceil(rank / 64) more K blocks with A = rows of the compensator's B
+//     matrix and B = u', both by TMA: since W x + B u' = [W | B] [x ; u'],
+//     the same accumulator absorbs the compensator term. The epilogue reads
+//     TMEM (lane = output row n, column = token) and stores y in bf16.
+//
+// Warp roles: warp 0 issues TMA (one thread) and owns the TMEM allocation,
+// warp 1 issues tcgen05.mma (one thread), warps 2-5 dequantise and then run
+// the epilogue (warp w reads TMEM lanes 32 (w % 4) .. + 31). Every mbarrier
+// wait is bounded; a timeout latches the handle's status word.
+#include <cstring>
+
 #include "internal.h"
-spear_status_t spear_launch_prefill(spear_linear_s*, const __nv_bfloat16*, __nv_bfloat16*, int, cudaStream_t) {
-  return SPEAR_ERR_UNSUPPORTED;
+#include "tcgen05.cuh"
+
+namespace spear {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kATileBytes = 128 * 128;         // 128 rows x 64 bf16
+constexpr int kRawWBytes = 128 * 8 * 4;        // 128 rows x 64 codes, packed
+constexpr int kRawBytes = kRawWBytes + 128 * 4;  // plus one scale/zero word per row
+constexpr int kBarrierBytes = 1024;
+constexpr int kMaxStages = 6;
+
+struct GemmParams {
+  int kblocks;      // K blocks of 64 from the main operands
+  int tail_blocks;  // compensator K blocks (A from mapAt, B from mapBt)
+  int TN;           // B rows per tile = MMA N (multiple of 16, <= 256)
+  int a_rows;       // rows of the A operand (W rows, or tokens for the pre-kernel)
+  int b_rows;       // rows of the B operand (tokens, or rank for the pre-kernel)
+  int K;
+  const uint32_t* wq;  // prefill-layout packed W
+  const uint32_t* sz;  // prefill-layout scale/zero words
+  int n_groups, G;
+  __nv_bfloat16* out;
+  int ld_out;
+  float alpha;
+  int gate;
+  unsigned* status;
+  uint64_t wait_ns;
+  int NS;
+  uint32_t a_bytes, b_bytes, raw_bytes, stage_bytes;
+  uint32_t tmem_cols;
+};
+
+SPEAR_DEVINL void fail(const GemmParams& p) { atomicOr(p.status, kStatusTimeoutPipe); }
+
+SPEAR_DEVINL void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+SPEAR_DEVINL uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+SPEAR_DEVINL float gate_apply(float z, int gate) {
+  return gate == SPEAR_GATE_ONE ? z : z * (1.0f / (1.0f + expf(-z)));
+}
+
+template <bool DEQ, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                const __grid_constant__ CUtensorMap mapAt, const __grid_constant__ CUtensorMap mapBt) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
+  uint64_t* full_tma = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* full_a = full_tma + 8;
+  uint64_t* empty = full_tma + 16;
+  uint64_t* acc_full = full_tma + 24;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 256);
+  uint8_t* stages = smem + kBarrierBytes;
+  const uint32_t stages_s = smem_u32(stages);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int a0 = blockIdx.x * 128;
+  const int b0 = blockIdx.y * p.TN;
+  const int total = p.kblocks + p.tail_blocks;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.NS; ++s) {
+      mbar_init(&full_tma[s], 1);
+      mbar_init(&full_a[s], 4);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_d = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      for (int it = 0; it < total; ++it) {
+        const int s = it % p.NS;
+        if (it >= p.NS && !mbar_wait_bounded(&empty[s], ((it / p.NS) - 1) & 1, p.wait_ns)) {
+          fail(p);
+          break;
+        }
+        uint8_t* st = stages + (size_t)s * p.stage_bytes;
+        uint8_t* A = st;
+        uint8_t* B = st + p.a_bytes;
+        uint8_t* raw = B + p.b_bytes;
+        if (it < p.kblocks) {
+          if constexpr (DEQ) {
+            mbar_arrive_expect_tx(&full_tma[s], kRawBytes + p.b_bytes);
+            bulk_g2s(raw, p.wq + ((size_t)blockIdx.x * p.kblocks + it) * 1024, kRawWBytes, &full_tma[s]);
+            bulk_g2s(raw + kRawWBytes, p.sz + ((size_t)blockIdx.x * p.n_groups + (it * 64) / p.G) * 128, 512,
+                     &full_tma[s]);
+          } else {
+            mbar_arrive_expect_tx(&full_tma[s], kATileBytes + p.b_bytes);
+            tma_load_2d(A, &mapA, it * 64, a0, &full_tma[s]);
+          }
+          tma_load_2d(B, &mapB, it * 64, b0, &full_tma[s]);
+        } else {
+          const int t = it - p.kblocks;
+          mbar_arrive_expect_tx(&full_tma[s], kATileBytes + p.b_bytes);
+          tma_load_2d(A, &mapAt, t * 64, a0, &full_tma[s]);
+          tma_load_2d(B, &mapBt, t * 64, b0, &full_tma[s]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, p.TN);
+      for (int it = 0; it < total; ++it) {
+        const int s = it % p.NS;
+        const unsigned par = (it / p.NS) & 1;
+        if (!mbar_wait_bounded(&full_tma[s], par, p.wait_ns)) {
+          fail(p);
+          break;
+        }
+        if (DEQ && it < p.kblocks && !mbar_wait_bounded(&full_a[s], par, p.wait_ns)) {
+          fail(p);
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t a_s = stages_s + s * p.stage_bytes;
+        const uint32_t b_s = a_s + p.a_bytes;
+#pragma unroll
+        for (int k16 = 0; k16 < 4; ++k16)
+          umma_bf16(tmem_d, sw128_kmajor_desc(a_s + 32 * k16), sw128_kmajor_desc(b_s + 32 * k16), idesc,
+                    (it | k16) != 0);
+        umma_commit(&empty[s]);
+      }
+      umma_commit(acc_full);  // the accumulator is complete once every MMA above has finished
+    }
+  } else {
+    // ---------------------------------------------------------- dequantisers
+    const int r = threadIdx.x - 64;  // A row of this thread (0..127)
+    if constexpr (DEQ) {
+      for (int it = 0; it < p.kblocks; ++it) {
+        const int s = it % p.NS;
+        if (!mbar_wait_bounded(&full_tma[s], (it / p.NS) & 1, p.wait_ns)) {
+          fail(p);
+          break;
+        }
+        const uint32_t a_s = stages_s + s * p.stage_bytes;
+        const uint32_t raw_sa = a_s + p.a_bytes + p.b_bytes;
+        const uint4 w0 = lds128(raw_sa + r * 32), w1 = lds128(raw_sa + r * 32 + 16);
+        const uint32_t szw = lds32(raw_sa + kRawWBytes + r * 4);
+        const uint32_t zz = biased_zero_x2(szw >> 16);
+        const uint32_t sc = (szw & 0xFFFFu) | (szw << 16);
+        const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t w = words[c];
+          uint32_t v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[j] = bf16x2_mul(bf16x2_sub(int4_pair_to_bf16x2_biased(w >> (4 * j)), zz), sc);
+          st_shared_v4(a_s + r * 128 + ((c ^ (r & 7)) << 4), v[0], v[1], v[2], v[3]);
+        }
+        fence_proxy_async_smem();  // make the generic-proxy tile visible to the tensor cores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full_a[s]);
+      }
+    }
+
+    // ---------------------------------------------------------- epilogue
+    const bool ok = mbar_wait_bounded(acc_full, 0, 4 * p.wait_ns);
+    if (!ok && lane == 0) fail(p);
+    tc_fence_after_sync();
+    const int q = warp & 3;
+    const int row = a0 + 32 * q + lane;
+    if (ok) {
+      for (int c0 = 0; c0 < p.TN; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld_x16(tmem_d + ((uint32_t)(32 * q) << 16) + c0, v);
+        tmem_ld_wait();
+        if constexpr (EPI == 0) {
+          // y[m][n]: lane = n, columns = tokens
+          if (row < p.a_rows) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int m = b0 + c0 + j;
+              if (m < p.b_rows) p.out[(size_t)m * p.ld_out + row] = __float2bfloat16_rn(__uint_as_float(v[j]));
+            }
+          }
+        } else {
+          // u'[m][j] = bf16(alpha * gamma(z) * z): lane = token m, columns = rank index
+          if (row < p.a_rows) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              pk[j] = pack_bf16x2(p.alpha * gate_apply(__uint_as_float(v[2 * j]), p.gate),
+                                  p.alpha * gate_apply(__uint_as_float(v[2 * j + 1]), p.gate));
+            uint4* dst = reinterpret_cast<uint4*>(p.out + (size_t)row * p.ld_out + c0);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem_d, p.tmem_cols);
+}
+
+uint32_t tmem_cols_for(int n) {
+  uint32_t c = 32;
+  while (c < (uint32_t)n) c <<= 1;
+  return c;
+}
+
+template <bool DEQ, int EPI>
+cudaError_t launch(const GemmParams& p, dim3 grid, size_t smem, cudaStream_t st, const CUtensorMap& mA,
+                   const CUtensorMap& mB, const CUtensorMap& mAt, const CUtensorMap& mBt) {
+  static bool configured = false;
+  auto k = gemm_kernel<DEQ, EPI>;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, p, mA, mB, mAt, mBt);
+}
+
+// Stages that fit next to the barriers (one A tile, one B tile, raw W).
+int stages_for(uint32_t stage_bytes) {
+  const size_t budget = 227 * 1024 - kBarrierBytes - 1024;
+  int ns = (int)(budget / stage_bytes);
+  return ns > kMaxStages ? kMaxStages : ns;
+}
+
+}  // namespace
+}  // namespace spear
+
+using namespace spear;
+
+// Tokens per tile: the fewest tiles of at most 256 tokens, split evenly and
+// rounded up to the MMA's multiple of 16.
+static int prefill_tn(int M) {
+  const int tiles = (M + 255) / 256;
+  int tn = (M + tiles - 1) / tiles;
+  tn = (tn + 15) / 16 * 16;
+  return tn < 16 ? 16 : tn;
+}
+
+spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,
+                                    cudaStream_t stream) {
+  const int K = h->K, N = h->N, r = h->rank;
+  CUtensorMap none;
+  memset(&none, 0, sizeof none);
+  cudaError_t e;
+
+  if (r > 0) {
+    // ---- compensator projection and gate: u' [M][r]
+    CUtensorMap mx, ma;
+    if (!encode_2d_bf16(&mx, x, K, M, (uint64_t)K * 2, 64, 128) ||
+        !encode_2d_bf16(&ma, h->a_pre, K, r, (uint64_t)K * 2, 64, r))
+      return SPEAR_ERR_CUDA;
+    GemmParams p{};
+    p.kblocks = K / 64;
+    p.tail_blocks = 0;
+    p.TN = r;
+    p.a_rows = M;
+    p.b_rows = r;
+    p.K = K;
+    p.out = h->u_pre;
+    p.ld_out = r;
+    p.alpha = h->alpha;
+    p.gate = h->gate;
+    p.status = &h->sync->status;
+    p.wait_ns = h->wait_ns;
+    p.a_bytes = kATileBytes;
+    p.b_bytes = (uint32_t)(r * 128 + 1023) / 1024 * 1024;
+    p.raw_bytes = 0;
+    p.stage_bytes = p.a_bytes + p.b_bytes;
+    p.NS = stages_for(p.stage_bytes);
+    p.tmem_cols = tmem_cols_for(r);
+    const size_t smem = kBarrierBytes + 1024 + (size_t)p.NS * p.stage_bytes;
+    e = launch<false, 1>(p, dim3((M + 127) / 128, 1), smem, stream, mx, ma, none, none);
+    if (e != cudaSuccess) return SPEAR_ERR_CUDA;
+  }
+
+  // ---- main contraction with the compensator K-tail
+  const int TN = prefill_tn(M);
+  CUtensorMap mx, mbt, mut;
+  if (!encode_2d_bf16(&mx, x, K, M, (uint64_t)K * 2, 64, TN)) return SPEAR_ERR_CUDA;
+  if (r > 0) {
+    if (!encode_2d_bf16(&mbt, h->b_pre, r, (uint64_t)h->nt128 * 128, (uint64_t)r * 2, 64, 128) ||
+        !encode_2d_bf16(&mut, h->u_pre, r, M, (uint64_t)r * 2, 64, TN))
+      return SPEAR_ERR_CUDA;
+  } else {
+    mbt = none;
+    mut = none;
+  }
+  GemmParams p{};
+  p.kblocks = K / 64;
+  p.tail_blocks = (r + 63) / 64;
+  p.TN = TN;
+  p.a_rows = N;
+  p.b_rows = M;
+  p.K = K;
+  p.wq = h->wq_pre;
+  p.sz = h->sz_pre;
+  p.n_groups = h->n_groups;
+  p.G = h->G;
+  p.out = y;
+  p.ld_out = N;
+  p.alpha = h->alpha;
+  p.gate = h->gate;
+  p.status = &h->sync->status;
+  p.wait_ns = h->wait_ns;
+  p.a_bytes = kATileBytes;
+  p.b_bytes = (uint32_t)(TN * 128 + 1023) / 1024 * 1024;
+  p.raw_bytes = kRawBytes;
+  p.stage_bytes = (p.a_bytes + p.b_bytes + kRawBytes + 1023) / 1024 * 1024;
+  p.NS = stages_for(p.stage_bytes);
+  p.tmem_cols = tmem_cols_for(TN);
+  const size_t smem = kBarrierBytes + 1024 + (size_t)p.NS * p.stage_bytes;
+  e = launch<true, 0>(p, dim3(h->nt128, (M + TN - 1) / TN), smem, stream, none, mx, mbt, mut);
+  return e == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
 }

@@ -8,7 +8,7 @@
 
 #include "internal.h"
 
-bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int Mp, int KC) {
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -19,6 +19,24 @@ bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int Mp, int KC)
         q == cudaDriverEntryPointSuccess)
       encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   });
+  return encode;
+}
+
+bool encode_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                    uint32_t box_inner, uint32_t box_rows) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_x_map(CUtensorMap* map, const void* x, int M, int K, int Mp, int KC) {
+  auto encode = tensor_map_encoder();
   if (!encode) return false;
   const cuuint64_t dims[3] = {64, (cuuint64_t)M, (cuuint64_t)(K / 64)};
   const cuuint64_t strides[2] = {(cuuint64_t)K * 2, 128};
