@@ -1,0 +1,397 @@
+"""Benchmark of the W4 + input-adaptive error-compensator linear on GB300.
+
+Workload (the decode layer set of a Llama-7B-shaped block, 4-bit group-128
+weights, compensator rank 64 on all seven projections): one step runs the
+seven linears q, k, v, o (4096 -> 4096), gate, up (4096 -> 11008) and down
+(11008 -> 4096) through the fused decode kernel at each of M = 1, 8 and 32
+tokens, i.e. 21 forward calls and 41 tokens. Weights rotate over four copies
+(about 460 MB, more than the 129 MB L2) so that every pass streams its
+weights from HBM. Steps are replayed from CUDA graphs; timing uses CUDA
+events on the launch stream.
+
+Also reported: the same kernels with the compensator disabled (rank 0), the
+end-to-end rate through spear_linear_forward_host (pinned host buffers, copies
+inside the timed region), the prefill path on the Llama-3-8B MLP at M = 2048,
+the roofline of the decode kernel against the measured HBM copy bandwidth, SM
+clocks sampled during the timed region, and the fp64 CPU oracle timed on a
+bounded sample of the same workload.
+
+Usage: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+DECODE_TOKENS = (1, 8, 32)
+COPIES = 4
+METRIC = "W4+EC linear: decode tokens/s & HBM GB/s (M=1–32); prefill TFLOP/s vs roofline"
+WORKLOAD = "llama7b decode layer set (q,k,v,o 4096x4096; gate,up 4096->11008; down 11008->4096), INT4 g128, EC r64"
+
+
+def peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.device = device
+        self.proc = None
+        self.path = Path(tempfile.mkstemp(prefix="clocks_", suffix=".csv")[1])
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.path.read_text().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        self.path.unlink(missing_ok=True)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ helpers
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def decode_bytes(specs, ec=True):
+    from quantized_linear_error_gb300 import workload as wl
+    total = 0
+    for M in DECODE_TOKENS:
+        for sp in specs:
+            s = sp if ec else wl.LinearSpec(sp.name, sp.K, sp.N, sp.group_size, 0)
+            total += s.algorithmic_bytes(M)
+    return total
+
+
+def traffic_from_profile(kernel_src: Path, summary: Path):
+    """dram bytes per launch recorded by an ncu capture, if it was taken on the
+    current kernel source (the summary stores the source's SHA-256)."""
+    if not summary.exists():
+        return None
+    try:
+        d = json.loads(summary.read_text())
+    except ValueError:
+        return None
+    if d.get("kernel_source_sha256") != hashlib.sha256(kernel_src.read_bytes()).hexdigest():
+        return None
+    return d.get("dram_bytes_per_step")
+
+
+# ------------------------------------------------------------------ CPU oracle
+def cpu_oracle_rate(sample_rows: int = 256, seed: int = 0):
+    """Time the fp64 oracle on all seven linears at M = 1, 8, 32 for the first
+    `sample_rows` output rows of each, and scale to tokens/s of the full step."""
+    from oracle import ref
+    from quantized_linear_error_gb300 import workload as wl
+    ref.build()
+    specs = wl.config_linears(2)
+    ws = [wl.make_weights(sp, seed) for sp in specs]
+    t_full = 0.0
+    for M in DECODE_TOKENS:
+        for w in ws:
+            x = wl.make_x(w.spec.K, M, w.outliers, seed, w.spec.name)
+            rows = slice(0, min(sample_rows, w.spec.N))
+            sub = wl.LinearWeights(w.spec, w.q[rows], w.s[rows], w.z[rows], w.A, w.B[rows], w.outliers)
+            t0 = time.perf_counter()
+            ref.forward(sub.q, sub.s, sub.z, w.spec.K, w.spec.G, sub.A, sub.B, w.spec.alpha, w.spec.gate, x)
+            dt = time.perf_counter() - t0
+            t_full += dt * w.spec.N / (rows.stop - rows.start)
+    tokens = sum(DECODE_TOKENS)
+    return {"value": tokens / t_full, "unit": "tokens/s", "cores": ref.max_threads(), "kind": "oracle",
+            "sample": f"fp64 oracle, all 7 linears at M=1,8,32, first {sample_rows} output rows each, "
+                      f"time scaled by N/{sample_rows} to the full layer set"}, t_full
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle as it stands, same metric and config."""
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        cpu_oracle_rate(sample_rows=32)
+    vals = []
+    for _ in range(args.steps):
+        cb, t_full = cpu_oracle_rate(sample_rows=64)
+        vals.append(cb["value"])
+    value = statistics.median(vals)
+    cb["value"] = value
+    cb["sample"] = cb["sample"].replace("first 256", "first 64")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sum(DECODE_TOKENS) / value * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "tokens_per_step": list(DECODE_TOKENS)},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    from quantized_linear_error_gb300 import build, spear
+    from quantized_linear_error_gb300 import workload as wl
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    build.build()
+    spear.load()
+    hbm_peak, bf16_peak, bf16_sust, peak_src = peaks()
+    specs = wl.config_linears(2)
+    stream = torch.cuda.Stream()
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+    # --- handles: COPIES copies of the layer set, with and without the compensator
+    handles = {True: [], False: []}
+    for c in range(COPIES):
+        for sp in specs:
+            w = wl.make_weights(sp, 100 * rank + c)
+            handles[True].append(spear.from_weights(w, max_tokens=32, stream=stream))
+            w0 = wl.LinearWeights(wl.LinearSpec(sp.name, sp.K, sp.N, sp.group_size, 0), w.q, w.s, w.z, None, None,
+                                  w.outliers)
+            handles[False].append(spear.from_weights(w0, max_tokens=32, stream=stream))
+    outl = {sp.K: wl.outlier_channels(sp.K, 0, sp.name) for sp in specs}
+    xs = {(M, K): dev(wl.make_x(K, M, outl[K], rank, f"bench/x{K}")) for M in DECODE_TOKENS for K in (4096, 11008)}
+    ys = {(M, N): torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for M in DECODE_TOKENS for N in (4096, 11008)}
+
+    def capture(ec, copy, ms=DECODE_TOKENS):
+        g = torch.cuda.CUDAGraph()
+        hs = handles[ec][copy * 7:(copy + 1) * 7]
+        with torch.cuda.stream(stream):
+            for M in ms:  # warm (configures the kernels outside capture)
+                for h, sp in zip(hs, specs):
+                    h.forward_decode(xs[(M, sp.K)], ys[(M, sp.N)], stream=stream)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for M in ms:
+                for h, sp in zip(hs, specs):
+                    h.forward_decode(xs[(M, sp.K)], ys[(M, sp.N)], stream=stream)
+        return g
+
+    def time_graphs(graphs, steps, warmup):
+        for i in range(warmup):
+            graphs[i % len(graphs)].replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(steps):
+                graphs[i % len(graphs)].replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return e0.elapsed_time(e1) / steps  # ms per step
+
+    graphs_ec = [capture(True, c) for c in range(COPIES)]
+    graphs_noec = [capture(False, c) for c in range(COPIES)]
+
+    with ClockSampler(local) as clk:
+        ms_step = time_graphs(graphs_ec, args.steps, args.warmup)
+    clocks = clk.summary()
+    ms_step = max_over_ranks(ms_step, world)
+    ms_noec = max_over_ranks(time_graphs(graphs_noec, args.steps, args.warmup), world)
+    for h in handles[True] + handles[False]:
+        st = h.check()
+        if st != spear.SPEAR_OK:
+            raise SystemExit(f"device status {spear.status_string(st)}")
+
+    tokens = sum(DECODE_TOKENS)
+    value = tokens * world / (ms_step / 1e3)
+    bytes_step = decode_bytes(specs, True)
+    per_m = {}
+    for M in DECODE_TOKENS:
+        gm = [capture(True, c, (M,)) for c in range(COPIES)]
+        t = time_graphs(gm, max(4, args.steps // 2), 2)
+        b = sum(sp.algorithmic_bytes(M) for sp in specs)
+        per_m[str(M)] = {"tokens_per_s": M / (t / 1e3), "us_per_layer_set": t * 1e3, "hbm_gbs": b / (t / 1e3) / 1e9,
+                         "frac_hbm": b / (t / 1e3) / 1e9 / hbm_peak}
+        del gm
+
+    # --- end to end through the host-buffer entry point
+    hx = {k: v.cpu().pin_memory() for k, v in xs.items()}
+    hy = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in ys.items()}
+    h2d = sum(M * sp.K * 2 for M in DECODE_TOKENS for sp in specs)
+    d2h = sum(M * sp.N * 2 for M in DECODE_TOKENS for sp in specs)
+
+    def e2e_step(i):
+        hs = handles[True][(i % COPIES) * 7:(i % COPIES + 1) * 7]
+        for M in DECODE_TOKENS:
+            for h, sp in zip(hs, specs):
+                h.forward_host(hx[(M, sp.K)], hy[(M, sp.N)], stream=stream)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        e2e_step(i)
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, world)
+    e2e = {"value": tokens * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "call": "spear_linear_forward_host per linear (pinned host x/y, synchronous)"}
+
+    # --- prefill: Llama-3-8B MLP at M = 2048 (gate, up 4096->14336; down 14336->4096), EC rank 128
+    prefill = None
+    if not args.skip_prefill:
+        pspecs = wl.config_linears(3)
+        Mp = 2048
+        pl = [spear.from_weights(wl.make_weights(sp, 0), max_tokens=Mp, stream=stream) for sp in pspecs]
+        px = {K: torch.randn(Mp, K, device="cuda").to(torch.bfloat16) for K in (4096, 14336)}
+        py = {N: torch.empty(Mp, N, device="cuda", dtype=torch.bfloat16) for N in (4096, 14336)}
+        with torch.cuda.stream(stream):
+            for h, sp in zip(pl, pspecs):
+                h.forward_prefill(px[sp.K], py[sp.N], stream=stream)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for h, sp in zip(pl, pspecs):
+                h.forward_prefill(px[sp.K], py[sp.N], stream=stream)
+        tp = time_graphs([g], max(3, args.steps // 4), 2)
+        flops = sum(sp.flops(Mp) for sp in pspecs)
+        tflops = flops / (tp / 1e3) / 1e12
+        prefill = {"workload": "llama3-8b MLP, M=2048, INT4 g128, EC r128", "ms": tp, "tflops": tflops,
+                   "frac_bf16_peak": tflops / bf16_peak, "peak_tflops": bf16_peak, "peak_source": peak_src,
+                   "tokens_per_s": Mp / (tp / 1e3)}
+        for h in pl:
+            if h.check() != spear.SPEAR_OK:
+                raise SystemExit("prefill device status error")
+
+    # --- roofline of the decode kernel (the only kernel in the step)
+    launches = len(DECODE_TOKENS) * len(specs)
+    achieved = bytes_step / (ms_step / 1e3) / 1e9
+    traffic = traffic_from_profile(ROOT / "quantized_linear_error_gb300" / "csrc" / "decode.cu",
+                                   ROOT / "profiles" / "decode_kernel_traffic.json")
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                "traffic": None if traffic is None else traffic / launches,
+                "kernel": "decode_kernel (all 21 launches of a step)",
+                "algorithmic_bytes_per_launch": bytes_step / launches, "peak_source": peak_src}
+
+    cpu = None
+    if rank == 0 and not args.skip_cpu:
+        cpu, _ = cpu_oracle_rate()
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+            "config": {"workload": WORKLOAD, "tokens_per_step": list(DECODE_TOKENS), "linears_per_step": 21,
+                       "l2": f"{COPIES} rotating weight copies (~{COPIES * 115} MB) > 129 MB L2",
+                       "graphs": "each step replayed from a CUDA graph", "parallelism": "replicas"},
+            "hbm_gbs": achieved, "per_batch": per_m,
+            "ec_off": {"ms_per_step": ms_noec, "tokens_per_s": tokens * world / (ms_noec / 1e3),
+                       "hbm_gbs": decode_bytes(specs, False) / (ms_noec / 1e3) / 1e9,
+                       "ec_overhead": ms_step / ms_noec - 1.0},
+            "prefill": prefill, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches * args.steps, "clocks": clocks}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    for h in handles[True] + handles[False]:
+        h.close()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        world, rank = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
+        run_reference(args, world, rank)
+        return
+    world, rank, local = dist_setup(args)
+    run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
