@@ -135,6 +135,31 @@ spear_status_t spear_linear_check(spear_linear_t h, cudaStream_t stream);
  * latches TIMEOUT). */
 spear_status_t spear_linear_debug_set(spear_linear_t h, int64_t wait_ns, int32_t skip_arrive);
 
+/* Decode forward that allocates nothing (the paper has no counterpart; this is
+ * a deployment convenience). For callers that cannot call cudaMalloc at all,
+ * for instance a process whose device memory is entirely reserved up front by
+ * another allocator, or a serving loop in which a device allocation (which may
+ * synchronise the device) is not allowed: such callers cannot create a handle,
+ * so this call takes everything from the caller.
+ *   desc: the same descriptor spear_linear_create takes (device pointers to
+ *         the user-layout q, scales, zeros, A, B; max_tokens is ignored);
+ *   x: device bf16 [M][K]; y: device bf16 [M][N]; 1 <= M <= 32 (0 is a no-op).
+ * Result: y = bf16_RNE(W_q x + alpha B (gamma(Ax) (.) Ax)), fp32 accumulation,
+ * as spear_linear_forward_decode computes (summation order differs).
+ * Scratch: the compensator projection z and an arrival counter live in one
+ * static device array of the library (33,024 bytes, held on every GPU that
+ * loads the library until the process exits); it bounds rank <= 256 and
+ * M <= 32, and larger values return SPEAR_ERR_INVALID_ARG. The first call on a
+ * device looks the array's address up (cudaGetSymbolAddress) and caches it;
+ * make that first call before any stream capture. Every call clears the
+ * counters (cudaMemsetAsync on `stream`), then launches one kernel; no
+ * allocation, no synchronisation. All calls share the array, so calls that
+ * overlap on the GPU (different streams, or devices' streams racing on one
+ * device) race with each other: serialise them. Slower than the handle-based
+ * decode path (it reads the unpacked user layout on CUDA cores). */
+spear_status_t spear_linear_forward_decode_noalloc(const spear_linear_desc_t* desc, const void* x, void* y,
+                                                   int32_t M, cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* spear_status_string(spear_status_t s);
 

@@ -63,6 +63,8 @@ def load(path: Path | None = None):
     L.spear_linear_dequantize.argtypes = [H, c_int32, c_void_p, H]
     L.spear_linear_check.argtypes = [H, H]
     L.spear_linear_debug_set.argtypes = [H, c_int64, c_int32]
+    L.spear_linear_forward_decode_noalloc.argtypes = [POINTER(spear_linear_desc_t), c_void_p, c_void_p, c_int32, H]
+    L.spear_linear_forward_decode_noalloc.restype = c_int
     L.spear_status_string.argtypes = [c_int]
     L.spear_status_string.restype = c_char_p
     for name in ("spear_linear_create", "spear_linear_forward_decode", "spear_linear_forward_prefill",
