@@ -371,6 +371,35 @@ def run_ours(args, world, rank, local):
         h.close()
 
 
+def run_case(case: str, reps: int = 5):
+    """Run one small named case `reps` times and exit (a target for profilers):
+    decode/<proj>/<M>[/noec] on the decode layer set, prefill/<proj>/<M>[/noec]
+    on the Llama-3-8B MLP (proj in q,k,v,o,gate,up,down)."""
+    import torch
+
+    from quantized_linear_error_gb300 import build, spear
+    from quantized_linear_error_gb300 import workload as wl
+    parts = case.split("/")
+    path, proj, M = parts[0], parts[1], int(parts[2])
+    ec = not (len(parts) > 3 and parts[3] == "noec")
+    specs = wl.config_linears(2 if path == "decode" else 3)
+    sp = next(s for s in specs if s.name.endswith("/" + proj))
+    if not ec:
+        sp = wl.LinearSpec(sp.name, sp.K, sp.N, sp.group_size, 0)
+    build.build()
+    w = wl.make_weights(sp, 0)
+    lin = spear.from_weights(w, max_tokens=max(M, 32))
+    x = torch.from_numpy(wl.make_x(sp.K, M, w.outliers, 0, sp.name).view("int16")).view(torch.bfloat16).cuda()
+    y = torch.empty((M, sp.N), dtype=torch.bfloat16, device="cuda")
+    for _ in range(reps):
+        getattr(lin, f"forward_{path}")(x, y)
+    torch.cuda.synchronize()
+    st = lin.check()
+    if st != spear.SPEAR_OK:
+        raise SystemExit(f"device status {spear.status_string(st)}")
+    print(f"case {case}: ok")
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -379,7 +408,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--case", help="run one small named case 5 times and exit (profiling target), "
+                                   "e.g. decode/q/1, decode/gate/32/noec, prefill/gate/2048")
     args = ap.parse_args()
+    if args.case:
+        run_case(args.case)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
