@@ -372,18 +372,17 @@ def run_ours(args, world, rank, local):
 
 
 def run_case(case: str, reps: int = 5):
-    """Run one small named case `reps` times and exit (a target for profilers):
-    decode/<proj>/<M>[/noec] on the decode layer set, prefill/<proj>/<M>[/noec]
-    on the Llama-3-8B MLP (proj in q,k,v,o,gate,up,down)."""
+    """Run one named linear `reps` times and exit (a target for profilers):
+    <decode|prefill>:<linear>:<M>[:noec], <linear> a workload linear name such
+    as c2/q, c2/gate, c3/gate, c4/up."""
     import torch
 
     from quantized_linear_error_gb300 import build, spear
     from quantized_linear_error_gb300 import workload as wl
-    parts = case.split("/")
-    path, proj, M = parts[0], parts[1], int(parts[2])
+    parts = case.split(":")
+    path, name, M = parts[0], parts[1], int(parts[2])
     ec = not (len(parts) > 3 and parts[3] == "noec")
-    specs = wl.config_linears(2 if path == "decode" else 3)
-    sp = next(s for s in specs if s.name.endswith("/" + proj))
+    sp = next(s for c in (1, 2, 3, 4) for s in wl.config_linears(c) if s.name == name)
     if not ec:
         sp = wl.LinearSpec(sp.name, sp.K, sp.N, sp.group_size, 0)
     build.build()
@@ -409,7 +408,7 @@ def main():
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--case", help="run one small named case 5 times and exit (profiling target), "
-                                   "e.g. decode/q/1, decode/gate/32/noec, prefill/gate/2048")
+                                   "e.g. decode:c2/q:1, decode:c4/up:16:noec, prefill:c3/gate:2048")
     args = ap.parse_args()
     if args.case:
         run_case(args.case)

@@ -59,6 +59,15 @@ SPEAR_DEVINL void consumer_bar() {
 
 // B fragments (k16 x n8, col) for MT token tiles from a token-major smem
 // buffer: base[token * stride + k] (used for the gate output u).
+SPEAR_DEVINL void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+SPEAR_DEVINL void ldsm_x2(uint32_t& r0, uint32_t& r1, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
 template <int MT>
 SPEAR_DEVINL void load_token_frags(const __nv_bfloat16* base, int stride, int koff, int lane,
                                    uint32_t (&b)[MT][2]) {
@@ -81,21 +90,26 @@ SPEAR_DEVINL void load_token_frags(const __nv_bfloat16* base, int stride, int ko
 // (the mbarrier wait and arrival, which clobber memory, still bound them).
 // Lane (g, t) reads token 8n + g at k = koff + 2t and koff + 2t + 8; the XOR
 // with g puts the 8 rows on 8 different chunks, so 32 lanes hit 32 banks.
-// All fragments of one 128-channel unit (8 k16 steps) at once, so that one
-// load latency covers the unit. `lane_base[c]` = box base + 128 g + 4 t +
-// 16 (c ^ g): the lane's address of swizzled chunk c in token row g of the
-// unit's first k64 block; everything else is a compile-time offset.
+// All x fragments of one 128-channel unit (8 k16 steps) at once, so that one
+// load latency covers the unit, with ldmatrix on the swizzled box: lane l
+// gives the row address of matrix l / 8 (token tile pair half l / 16, k half
+// (l / 8) % 2), row l % 8; `lane_base[c]` is that address for chunk c of the
+// unit's first k64 block (the chunk XOR-ed with the token row, l % 8).
+// ldmatrix matrices: (tokens 8n.., k lo) -> b0 of n-tile n, (k hi) -> b1.
 template <int MT>
 SPEAR_DEVINL void load_unit_x_frags(const uint32_t (&lane_base)[8], uint32_t (&b)[8][MT][2]) {
   constexpr int Mp = 8 * MT;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    const int c = (2 * kk) & 7;               // chunk of k16 step kk inside its k64 block
+    const int c = (2 * kk) & 7;                 // chunk of k16 step kk inside its k64 block
     const uint32_t blk = (kk >> 2) * Mp * 128;  // second k64 block for kk >= 4
+    if constexpr (MT == 1) {
+      ldsm_x2(b[kk][0][0], b[kk][0][1], lane_base[c] + blk);
+    } else {
 #pragma unroll
-    for (int n = 0; n < MT; ++n) {
-      b[kk][n][0] = lds32(lane_base[c] + blk + n * 1024);
-      b[kk][n][1] = lds32(lane_base[c + 1] + blk + n * 1024);
+      for (int pr = 0; pr < MT / 2; ++pr)
+        ldsm_x4(b[kk][2 * pr][0], b[kk][2 * pr][1], b[kk][2 * pr + 1][0], b[kk][2 * pr + 1][1],
+                lane_base[c] + blk + pr * 16 * 128);
     }
   }
 }
@@ -148,7 +162,10 @@ template <int NW, int MT, int T, bool PC, bool EC>
 __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
     decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap xmap) {
   // independent accumulator chains per tile (k16 step kk goes to chain kk % NC)
-  constexpr int NC = (MT == 4 ? 2 : 4) / T > 0 ? (MT == 4 ? 2 : 4) / T : 1;
+  // Independent accumulator chains per tile (k16 step kk goes to chain
+  // kk % NC). Grouped scales fold the chains into acc once per 128-channel
+  // group; per-channel scales never fold until the end.
+  constexpr int NC = PC ? (MT == 4 ? 2 : 4) : (T == 1 && MT < 4 ? 2 : 1);
   constexpr int Mp = 8 * MT;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -172,10 +189,12 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
   const DecodeLayout L{K, p.nt16, p.P, PC};
   const size_t run_full = (size_t)Pc * L.stage_tile_bytes(kDecodeRun);
 
+  // consumer warps with at least one tile: KW warps per row group of T tiles
+  const int busy_warps = p.KW * ((Pc + T - 1) / T);
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], NW);
+      mbar_init(&empty[s], busy_warps);
     }
     mbar_init(szbar, 1);
     mbar_init(ubar, kEcWarps);
@@ -312,11 +331,13 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
   // ------------------------------------------------------------ consumer warps
   const int pw_i = warp / p.KW, kw_i = warp % p.KW;
   const int g = lane >> 2, tq = lane & 3;
-  // x box addressing: token row g, byte 4 t, and the swizzled chunk offsets
-  const uint32_t lane_off = g * 128 + 4 * tq;
+  // x box addressing for ldmatrix: this lane supplies row (lane % 8) of matrix
+  // lane / 8, i.e. token 8 * (lane / 16) + lane % 8 and k half (lane / 8) % 2
+  const int mrow = lane & 7, mkh = (lane >> 3) & 1, mtok = 8 * (lane >> 4) + mrow;
+  const uint32_t lane_off = mtok * 128;
   uint32_t swz[8];
 #pragma unroll
-  for (int c = 0; c < 8; ++c) swz[c] = (uint32_t)((c ^ g) << 4);
+  for (int c = 0; c < 8; ++c) swz[c] = (uint32_t)((((c + mkh) & 7) ^ mrow) << 4);
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   float acc[T][MT][4];
@@ -348,7 +369,9 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
     }
   }
 
-  for (int i = 0; i < p.n_stages && ok; ++i) {
+  // warps without a tile skip the stages (they are not counted on `empty`)
+  const bool busy = pw_i * T < Pc;
+  for (int i = 0; i < p.n_stages && ok && busy; ++i) {
     const int slot = i % p.NS;
     if (!mbar_wait_bounded(&full[slot], (i / p.NS) & 1, p.wait_ns)) {
       ok = false;
@@ -373,7 +396,7 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
 #pragma unroll
       for (int t = 0; t < T; ++t) {
         const int tl = pw_i * T + t;
-        if (tl < Pc) {
+        if (t == 0 || tl < Pc) {
           wv[t][0] = lds128(wsm + ((tl * (kcw_r / 64) + 2 * uin) * 32 + lane) * 16);
           wv[t][1] = lds128(wsm + ((tl * (kcw_r / 64) + 2 * uin + 1) * 32 + lane) * 16);
           if constexpr (!PC) {
@@ -401,7 +424,7 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
 #pragma unroll
         for (int t = 0; t < T; ++t) {
           const int tl = pw_i * T + t;
-          if (tl < Pc) {
+          if (t == 0 || tl < Pc) {
             const uint32_t w = word_of(wv[t][kk >> 2], kk & 3);
             const uint32_t a[4] = {bf16x2_sub(int4_pair_to_bf16x2_biased(w), zz[t][0]),
                                    bf16x2_sub(int4_pair_to_bf16x2_biased(w >> 4), zz[t][1]),
@@ -412,23 +435,22 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
           }
         }
       }
-      // fold the chains; grouped scales apply once per group here
+      // grouped scales: fold the chains into acc once per group
+      if constexpr (!PC) {
 #pragma unroll
-      for (int t = 0; t < T; ++t)
+        for (int t = 0; t < T; ++t)
 #pragma unroll
-        for (int n = 0; n < MT; ++n)
+          for (int n = 0; n < MT; ++n)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float v = accg[t][0][n][e];
+            for (int e = 0; e < 4; ++e) {
+              float v = accg[t][0][n][e];
 #pragma unroll
-            for (int c = 1; c < NC; ++c) v += accg[t][c][n][e];
+              for (int c = 1; c < NC; ++c) v += accg[t][c][n][e];
 #pragma unroll
-            for (int c = 0; c < NC; ++c) accg[t][c][n][e] = 0.f;
-            if constexpr (PC)
-              acc[t][n][e] += v;
-            else
+              for (int c = 0; c < NC; ++c) accg[t][c][n][e] = 0.f;
               acc[t][n][e] = fmaf(sc[t][e >> 1], v, acc[t][n][e]);
-          }
+            }
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
@@ -441,7 +463,12 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
 #pragma unroll
       for (int n = 0; n < MT; ++n)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[t][n][e] *= spc[t][e >> 1];
+        for (int e = 0; e < 4; ++e) {
+          float v = accg[t][0][n][e];
+#pragma unroll
+          for (int c = 1; c < NC; ++c) v += accg[t][c][n][e];
+          acc[t][n][e] = v * spc[t][e >> 1];
+        }
   }
 
   // ------------------------------------------------------------ reduction over K warps
