@@ -52,8 +52,11 @@ struct DecodeParams {
   int skip_arrive;
 };
 
+// Named barrier of the consumer warps. bar.sync counts whole warps, so each
+// warp reconverges first (lane-0 branches precede both uses).
 template <int NW>
 SPEAR_DEVINL void consumer_bar() {
+  __syncwarp();
   asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory");
 }
 
@@ -203,6 +206,7 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
   // Token rows M..Mp-1 of the staged x boxes are zero-filled by the copy
   // engine; in any case they only feed MMA output columns M..Mp-1, which are
   // never stored.
+  __syncwarp();
   __syncthreads();
   // Let the next kernel in the stream launch now; it only touches its own
   // weights until its griddepcontrol.wait, which waits for this grid.

@@ -71,6 +71,8 @@ struct spear_linear_s {
   float* z_dec = nullptr;
   float* z_pre = nullptr;            // [max_tokens][rank] fp32 (prefill projection)
   __nv_bfloat16* u_pre = nullptr;    // [max_tokens][rank] bf16 (prefill gated, alpha-scaled)
+  unsigned* pre_done = nullptr;      // [ceil(max_tokens / 128)] split counters of the pre-kernel
+  size_t ws_bytes = 0;               // workspace size (zeroed at create and by a TIMEOUT check)
   __nv_bfloat16* x_stage = nullptr;  // host-path staging [max_tokens][K]
   __nv_bfloat16* y_stage = nullptr;  // host-path staging [max_tokens][N]
 

@@ -38,7 +38,8 @@ constexpr int kBarrierBytes = 1024;
 constexpr int kMaxStages = 6;
 
 struct GemmParams {
-  int kblocks;      // K blocks of 64 from the main operands
+  int kblocks;      // K blocks of 64 from the main operands (per split for the pre-kernel)
+  int kb_total;     // all K blocks (the last split may be shorter)
   int tail_blocks;  // compensator K blocks (A from mapAt, B from mapBt)
   int TN;           // B rows per tile = MMA N (multiple of 16, <= 256)
   int a_rows;       // rows of the A operand (W rows, or tokens for the pre-kernel)
@@ -56,6 +57,9 @@ struct GemmParams {
   int NS;
   uint32_t a_bytes, b_bytes, raw_bytes, stage_bytes;
   uint32_t tmem_cols;
+  float* zacc;          // pre-kernel: fp32 [M][rank] partial sums of z (zero between calls)
+  unsigned* tile_done;  // pre-kernel: per 128-token tile, splits finished
+  int splits;
 };
 
 SPEAR_DEVINL void fail(const GemmParams& p) { atomicOr(p.status, kStatusTimeoutPipe); }
@@ -72,6 +76,18 @@ SPEAR_DEVINL uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
 
 SPEAR_DEVINL float gate_apply(float z, int gate) {
   return gate == SPEAR_GATE_ONE ? z : z * (1.0f / (1.0f + expf(-z)));
+}
+
+SPEAR_DEVINL void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// Named barrier of the 4 epilogue warps; bar.sync counts whole warps, so a
+// warp split by a single-thread branch reconverges first.
+SPEAR_DEVINL void epilogue_bar() {
+  __syncwarp();
+  asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
 template <bool DEQ, int EPI>
@@ -91,8 +107,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a0 = blockIdx.x * 128;
-  const int b0 = blockIdx.y * p.TN;
-  const int total = p.kblocks + p.tail_blocks;
+  // main kernel: blockIdx.y is the token tile; pre-kernel: the K split
+  const int b0 = EPI == 2 ? 0 : blockIdx.y * p.TN;
+  const int kb0 = EPI == 2 ? blockIdx.y * p.kblocks : 0;
+  const int kmain = EPI == 2 ? min(p.kblocks, p.kb_total - kb0) : p.kblocks;
+  const int total = kmain + p.tail_blocks;
+  volatile int& last_split = *reinterpret_cast<volatile int*>(smem + 512);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
@@ -107,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, p.tmem_cols);
     tmem_relinquish();
   }
+  __syncwarp();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -126,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* A = st;
         uint8_t* B = st + p.a_bytes;
         uint8_t* raw = B + p.b_bytes;
-        if (it < p.kblocks) {
+        if (it < kmain) {
           if constexpr (DEQ) {
             mbar_arrive_expect_tx(&full_tma[s], kRawBytes + p.b_bytes);
             bulk_g2s(raw, p.wq + ((size_t)blockIdx.x * p.kblocks + it) * 1024, kRawWBytes, &full_tma[s]);
@@ -134,11 +155,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                      &full_tma[s]);
           } else {
             mbar_arrive_expect_tx(&full_tma[s], kATileBytes + p.b_bytes);
-            tma_load_2d(A, &mapA, it * 64, a0, &full_tma[s]);
+            tma_load_2d(A, &mapA, (kb0 + it) * 64, a0, &full_tma[s]);
           }
-          tma_load_2d(B, &mapB, it * 64, b0, &full_tma[s]);
+          tma_load_2d(B, &mapB, (kb0 + it) * 64, b0, &full_tma[s]);
         } else {
-          const int t = it - p.kblocks;
+          const int t = it - kmain;
           mbar_arrive_expect_tx(&full_tma[s], kATileBytes + p.b_bytes);
           tma_load_2d(A, &mapAt, t * 64, a0, &full_tma[s]);
           tma_load_2d(B, &mapBt, t * 64, b0, &full_tma[s]);
@@ -156,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           fail(p);
           break;
         }
-        if (DEQ && it < p.kblocks && !mbar_wait_bounded(&full_a[s], par, p.wait_ns)) {
+        if (DEQ && it < kmain && !mbar_wait_bounded(&full_a[s], par, p.wait_ns)) {
           fail(p);
           break;
         }
@@ -173,7 +194,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------- dequantisers
-    const int r = threadIdx.x - 64;  // A row of this thread (0..127)
+    // Two threads per row: thread d takes words 4 (d % 2) .. + 3 (channels
+    // 32 (d % 2) .. + 31) of row d / 2 and of row d / 2 + 64, so each warp's
+    // 16-byte loads of the packed tile are contiguous and its 16-byte stores
+    // hit 8 distinct swizzled chunks per 8 lanes (no bank conflicts).
+    const int d = threadIdx.x - 64;  // 0..127
+    const int half = d & 1;
     if constexpr (DEQ) {
       for (int it = 0; it < p.kblocks; ++it) {
         const int s = it % p.NS;
@@ -183,18 +209,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t a_s = stages_s + s * p.stage_bytes;
         const uint32_t raw_sa = a_s + p.a_bytes + p.b_bytes;
-        const uint4 w0 = lds128(raw_sa + r * 32), w1 = lds128(raw_sa + r * 32 + 16);
-        const uint32_t szw = lds32(raw_sa + kRawWBytes + r * 4);
-        const uint32_t zz = biased_zero_x2(szw >> 16);
-        const uint32_t sc = (szw & 0xFFFFu) | (szw << 16);
-        const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t w = words[c];
-          uint32_t v[4];
+        for (int pass = 0; pass < 2; ++pass) {
+          const int r = (d >> 1) + 64 * pass;
+          const uint4 wv = lds128(raw_sa + (uint32_t)(r * 32 + half * 16));
+          const uint32_t szw = lds32(raw_sa + kRawWBytes + r * 4);
+          const uint32_t zz = biased_zero_x2(szw >> 16);
+          const uint32_t sc = (szw & 0xFFFFu) | (szw << 16);
+          const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) v[j] = bf16x2_mul(bf16x2_sub(int4_pair_to_bf16x2_biased(w >> (4 * j)), zz), sc);
-          st_shared_v4(a_s + r * 128 + ((c ^ (r & 7)) << 4), v[0], v[1], v[2], v[3]);
+          for (int j4 = 0; j4 < 4; ++j4) {
+            const int c = 4 * half + j4;
+            const uint32_t w = words[j4];
+            uint32_t v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              v[j] = bf16x2_mul(bf16x2_sub(int4_pair_to_bf16x2_biased(w >> (4 * j)), zz), sc);
+            st_shared_v4(a_s + r * 128 + ((c ^ (r & 7)) << 4), v[0], v[1], v[2], v[3]);
+          }
         }
         fence_proxy_async_smem();  // make the generic-proxy tile visible to the tensor cores
         __syncwarp();
@@ -222,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (m < p.b_rows) p.out[(size_t)m * p.ld_out + row] = __float2bfloat16_rn(__uint_as_float(v[j]));
             }
           }
-        } else {
+        } else if constexpr (EPI == 1) {
           // u'[m][j] = bf16(alpha * gamma(z) * z): lane = token m, columns = rank index
           if (row < p.a_rows) {
             uint32_t pk[8];
@@ -234,11 +266,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
+        } else {
+          // split-K partial of z: add into the fp32 accumulator
+          if (row < p.a_rows) {
+            float* dst = p.zacc + (size_t)row * p.ld_out + c0;
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+              red_add_v4(dst + j, __uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                         __uint_as_float(v[j + 3]));
+          }
         }
       }
     }
+    if constexpr (EPI == 2) {
+      // The last split of this 128-token tile applies the gate to the complete z,
+      // writes u' and clears z and the counter for the next call.
+      __threadfence();
+      epilogue_bar();
+      if (threadIdx.x == 64) {
+        last_split = ok && atomicAdd(&p.tile_done[blockIdx.x], 1u) == (unsigned)(p.splits - 1);
+        __threadfence();
+      }
+      epilogue_bar();
+      if (last_split && row < p.a_rows) {
+        float* zr = p.zacc + (size_t)row * p.ld_out;
+        __nv_bfloat16* ur = p.out + (size_t)row * p.ld_out;
+        for (int c0 = 0; c0 < p.TN; c0 += 8) {
+          const float4 z0 = __ldcg(reinterpret_cast<const float4*>(zr + c0));
+          const float4 z1 = __ldcg(reinterpret_cast<const float4*>(zr + c0 + 4));
+          const float zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+          uint32_t pk[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            pk[j] = pack_bf16x2(p.alpha * gate_apply(zz[2 * j], p.gate), p.alpha * gate_apply(zz[2 * j + 1], p.gate));
+          *reinterpret_cast<uint4*>(ur + c0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<float4*>(zr + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4*>(zr + c0 + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      if (last_split && threadIdx.x == 64) p.tile_done[blockIdx.x] = 0;
+    }
   }
 
+  // single-thread roles leave warps split: reconverge before the CTA barrier
+  __syncwarp();
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem_d, p.tmem_cols);
@@ -308,7 +379,17 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
         !encode_2d_bf16(&ma, h->a_pre, K, r, (uint64_t)K * 2, 64, r))
       return SPEAR_ERR_CUDA;
     GemmParams p{};
-    p.kblocks = K / 64;
+    const int kbt = K / 64, mt = (M + 127) / 128;
+    // K splits so that the pre-kernel spans about one wave, at least 4 K blocks each
+    int splits = (h->sm_count + mt - 1) / mt;
+    if (splits > kbt / 4) splits = kbt / 4;
+    if (splits < 1) splits = 1;
+    p.kblocks = (kbt + splits - 1) / splits;
+    splits = (kbt + p.kblocks - 1) / p.kblocks;
+    p.kb_total = kbt;
+    p.splits = splits;
+    p.zacc = h->z_pre;
+    p.tile_done = h->pre_done;
     p.tail_blocks = 0;
     p.TN = r;
     p.a_rows = M;
@@ -327,7 +408,7 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
     p.NS = stages_for(p.stage_bytes);
     p.tmem_cols = tmem_cols_for(r);
     const size_t smem = kBarrierBytes + 1024 + (size_t)p.NS * p.stage_bytes;
-    e = launch<false, 1>(p, dim3((M + 127) / 128, 1), smem, stream, mx, ma, none, none);
+    e = launch<false, 2>(p, dim3(mt, splits), smem, stream, mx, ma, none, none);
     if (e != cudaSuccess) return SPEAR_ERR_CUDA;
   }
 
@@ -345,6 +426,8 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
   }
   GemmParams p{};
   p.kblocks = K / 64;
+  p.kb_total = K / 64;
+  p.splits = 1;
   p.tail_blocks = (r + 63) / 64;
   p.TN = TN;
   p.a_rows = N;

@@ -125,7 +125,9 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
   h->dec_tile_bytes = DecodeLayout{h->K, h->nt16, h->dec_P, h->per_channel}.tile_bytes();
 
   const size_t K = h->K, r = h->rank, mt = h->max_tokens;
-  const size_t ws_bytes = sizeof(spear::SyncWords) + kZDecFloats * 4 + mt * r * 4 + mt * r * 2 + 256;
+  const size_t pre_tiles = (mt + 127) / 128;
+  const size_t ws_bytes = sizeof(spear::SyncWords) + kZDecFloats * 4 + mt * r * 4 + mt * r * 2 + pre_tiles * 4 + 256;
+  h->ws_bytes = ws_bytes;
   cudaError_t e = cudaSuccess;
   auto A = [&](cudaError_t x) {
     if (e == cudaSuccess) e = x;
@@ -154,6 +156,7 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
   h->z_dec = reinterpret_cast<float*>(w + sizeof(spear::SyncWords));
   h->z_pre = h->z_dec + kZDecFloats;
   h->u_pre = reinterpret_cast<__nv_bfloat16*>(h->z_pre + mt * r);
+  h->pre_done = reinterpret_cast<unsigned*>(h->u_pre + mt * r);
 
   spear_status_t st = SPEAR_OK;
   if (cudaMemsetAsync(h->ws, 0, ws_bytes, stream) != cudaSuccess) st = SPEAR_ERR_CUDA;
@@ -225,8 +228,8 @@ spear_status_t spear_linear_check(spear_linear_t h, cudaStream_t stream) {
   if (cudaMemcpy(&status, &h->sync->status, sizeof status, cudaMemcpyDeviceToHost) != cudaSuccess)
     return SPEAR_ERR_CUDA;
   if (status == 0) return SPEAR_OK;
-  // Reset the workspace (counters, status, z accumulators) so the handle is usable again.
-  if (cudaMemset(h->sync, 0, sizeof(spear::SyncWords) + kZDecFloats * 4) != cudaSuccess) return SPEAR_ERR_CUDA;
+  // Reset the workspace (counters, status, accumulators) so the handle is usable again.
+  if (cudaMemset(h->ws, 0, h->ws_bytes) != cudaSuccess) return SPEAR_ERR_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return SPEAR_ERR_CUDA;
   return SPEAR_ERR_TIMEOUT;
 }
