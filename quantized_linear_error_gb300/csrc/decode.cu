@@ -117,12 +117,40 @@ SPEAR_DEVINL void load_unit_x_frags(const uint32_t (&lane_base)[8], uint32_t (&b
   }
 }
 
+// D = A B (no accumulator input: the first k16 step of a chain).
+SPEAR_DEVINL void mma_bf16_16816_zero(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// Named barrier of the compensator warps (reconverged first: bar.sync counts warps).
+SPEAR_DEVINL void ec_bar() {
+  __syncwarp();
+  asm volatile("bar.sync 2, %0;" ::"n"(kEcWarps * 32) : "memory");
+}
+
 SPEAR_DEVINL uint32_t word_of(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
 SPEAR_DEVINL float gate_apply(float z, int gate) {
   return gate == SPEAR_GATE_ONE ? z : z * (1.0f / (1.0f + expf(-z)));
+}
+
+// A does not depend on the previous kernel: pull this warp's units of it
+// (4 KB each, contiguous in fragment order) into L2 before waiting for x.
+SPEAR_DEVINL void ec_prefetch(const DecodeParams& p, int ew, int lane) {
+  const int kb128 = p.K / 128;
+  const int units = (p.rank / 16) * kb128;
+  const int u0 = (int)((long)blockIdx.x * units / gridDim.x);
+  const int u1 = (int)((long)(blockIdx.x + 1) * units / gridDim.x);
+  if (lane == 0)
+    for (int ua = u0 + ew; ua < u1; ua += kEcWarps) {
+      const int at = ua / kb128, kb = ua % kb128;
+      prefetch_l2(p.a_frag + ((size_t)at * (p.K / 16) + kb * 8) * 32, 8 * 32 * 16);
+    }
 }
 
 // z += A[:, this CTA's share] x, via warp MMA with A rows as the M side.
@@ -259,25 +287,31 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
   if (warp > NW) {
     if constexpr (EC) {
       const int ew = warp - NW - 1;
+      volatile int* ec_flag = reinterpret_cast<volatile int*>(smem + 512);
+      ec_prefetch(p, ew, lane);
       asm volatile("griddepcontrol.wait;" ::: "memory");
       ec_project<MT>(p, ew, lane);
-      __syncwarp();
-      if (lane == 0 && !p.skip_arrive) {
-        __threadfence();
-        atomicAdd(&p.sync->arrive, 1u);
-      }
-      bool arrived = false;
-      if (lane == 0) {
-        const unsigned target = gridDim.x * kEcWarps;
-        arrived = ld_acquire_gpu(&p.sync->arrive) >= target;
+      // Every lane's additions into z are visible device-wide before the
+      // CTA's single arrival (release) on the grid-wide counter.
+      __threadfence();
+      ec_bar();
+      if (ew == 0 && lane == 0) {
+        if (!p.skip_arrive) atomicAdd(&p.sync->arrive, 1u);
+        const unsigned target = gridDim.x;
+        bool arrived = ld_acquire_gpu(&p.sync->arrive) >= target;
         if (!arrived) {
           const uint64_t t0 = globaltimer();
-          while (!(arrived = ld_acquire_gpu(&p.sync->arrive) >= target))
+          while (!(arrived = ld_acquire_gpu(&p.sync->arrive) >= target)) {
             if (globaltimer() - t0 > p.wait_ns) break;
+            __nanosleep(64);  // one poller per CTA, spaced out on the counter's L2 line
+          }
         }
         if (!arrived) atomicOr(&p.sync->status, kStatusTimeoutZ);
+        *ec_flag = arrived ? 1 : 0;
+        __threadfence_block();
       }
-      arrived = __shfl_sync(0xffffffffu, arrived ? 1 : 0, 0) != 0;
+      ec_bar();
+      const bool arrived = *ec_flag != 0;
       // u = alpha * gamma(z) * z for 4 tokens per float4 of z ([rank][32] fp32),
       // eight independent loads in flight per lane
       const int nv = p.rank * (Mp / 4);
@@ -309,23 +343,27 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(ubar);  // release: this warp's share of u is visible to the consumers
-      // The last compensator warp (over all CTAs) to have read z clears it and
-      // the counters for the next call.
-      int last = 0;
-      if (lane == 0 && arrived) {
-        __threadfence();
-        last = atomicAdd(&p.sync->depart, 1u) == gridDim.x * kEcWarps - 1;
-        __threadfence();
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        for (int idx = lane; idx < p.rank * 32; idx += 32) p.z[idx] = 0.f;
-        __syncwarp();
-        if (lane == 0) {
+      // The last CTA (over the grid) to have read z clears it and the counters
+      // for the next call.
+      ec_bar();
+      if (ew == 0) {
+        int last = 0;
+        if (lane == 0 && arrived) {
           __threadfence();
-          p.sync->arrive = 0;
-          p.sync->depart = 0;
+          last = atomicAdd(&p.sync->depart, 1u) == gridDim.x - 1;
           __threadfence();
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          for (int idx = lane; idx < p.rank * 8; idx += 32)
+            reinterpret_cast<float4*>(p.z)[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
+          __syncwarp();
+          if (lane == 0) {
+            __threadfence();
+            p.sync->arrive = 0;
+            p.sync->depart = 0;
+            __threadfence();
+          }
         }
       }
     }
@@ -435,12 +473,18 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
                                    bf16x2_sub(int4_pair_to_bf16x2_biased(w >> 8), zz[t][0]),
                                    bf16x2_sub(int4_pair_to_bf16x2_biased(w >> 12), zz[t][1])};
 #pragma unroll
-            for (int n = 0; n < MT; ++n) mma_bf16_16816(accg[t][kk % NC][n], a, b[n][0], b[n][1]);
+            for (int n = 0; n < MT; ++n) {
+              // grouped scales restart the chains every group (folded below)
+              if (!PC && kk < NC)
+                mma_bf16_16816_zero(accg[t][kk % NC][n], a, b[n][0], b[n][1]);
+              else
+                mma_bf16_16816(accg[t][kk % NC][n], a, b[n][0], b[n][1]);
+            }
           }
         }
       }
-      // grouped scales: fold the chains into acc once per group
       if constexpr (!PC) {
+        // grouped scales: fold the chains into acc once per group
 #pragma unroll
         for (int t = 0; t < T; ++t)
 #pragma unroll
@@ -450,8 +494,6 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
               float v = accg[t][0][n][e];
 #pragma unroll
               for (int c = 1; c < NC; ++c) v += accg[t][c][n][e];
-#pragma unroll
-              for (int c = 0; c < NC; ++c) accg[t][c][n][e] = 0.f;
               acc[t][n][e] = fmaf(sc[t][e >> 1], v, acc[t][n][e]);
             }
       }
@@ -491,6 +533,16 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
   }
 
   // ------------------------------------------------------------ compensator term
+  // B fragments of this warp's first tile: loads in flight while u is awaited
+  constexpr int kBPre = MT == 1 ? 4 : 2;
+  uint4 bpre[kBPre];
+  if constexpr (EC) {
+#pragma unroll
+    for (int j = 0; j < kBPre; ++j)
+      bpre[j] = (warp < Pc && j < p.rank / 16)
+                    ? __ldg(p.b_frag + ((size_t)(tile0 + warp) * (p.rank / 16) + j) * 32 + lane)
+                    : make_uint4(0u, 0u, 0u, 0u);
+  }
   bool ec_ok = false;
   if constexpr (EC) ec_ok = mbar_wait_bounded(ubar, 0, 2 * p.wait_ns);
   consumer_bar<NW>();  // partial sums of all K warps are in shared memory
@@ -512,16 +564,28 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
     const int tile = tile0 + tl;
     if constexpr (EC) {
       if (ec_ok) {
-        for (int j16 = 0; j16 < p.rank / 16; ++j16) {
-          const uint4 bf = __ldg(p.b_frag + ((size_t)tile * (p.rank / 16) + j16) * 32 + lane);
-          const uint32_t a[4] = {bf.x, bf.y, bf.z, bf.w};
-          uint32_t bh[MT][2], bl[MT][2];
-          load_token_frags<MT>(uh, us, j16 * 16, lane, bh);
-          load_token_frags<MT>(ul, us, j16 * 16, lane, bl);
+        const int nj = p.rank / 16;
+        for (int j0 = 0; j0 < nj; j0 += kBPre) {
+          uint4 bf[kBPre];
 #pragma unroll
-          for (int n = 0; n < MT; ++n) {
-            mma_bf16_16816(c[n], a, bh[n][0], bh[n][1]);
-            mma_bf16_16816(c[n], a, bl[n][0], bl[n][1]);
+          for (int jj = 0; jj < kBPre; ++jj)
+            bf[jj] = (tl == warp && j0 == 0)
+                         ? bpre[jj]
+                         : (j0 + jj < nj ? __ldg(p.b_frag + ((size_t)tile * nj + j0 + jj) * 32 + lane)
+                                         : make_uint4(0u, 0u, 0u, 0u));
+#pragma unroll
+          for (int jj = 0; jj < kBPre; ++jj) {
+            if (j0 + jj < nj) {
+              const uint32_t a[4] = {bf[jj].x, bf[jj].y, bf[jj].z, bf[jj].w};
+              uint32_t bh[MT][2], bl[MT][2];
+              load_token_frags<MT>(uh, us, (j0 + jj) * 16, lane, bh);
+              load_token_frags<MT>(ul, us, (j0 + jj) * 16, lane, bl);
+#pragma unroll
+              for (int n = 0; n < MT; ++n) {
+                mma_bf16_16816(c[n], a, bh[n][0], bh[n][1]);
+                mma_bf16_16816(c[n], a, bl[n][0], bl[n][1]);
+              }
+            }
           }
         }
       }
