@@ -371,14 +371,44 @@ def run_ours(args, world, rank, local):
         h.close()
 
 
-def run_case(case: str, reps: int = 5):
-    """Run one named linear `reps` times and exit (a target for profilers):
-    <decode|prefill>:<linear>:<M>[:noec], <linear> a workload linear name such
-    as c2/q, c2/gate, c3/gate, c4/up."""
+def run_step_case():
+    """One warm-up pass, then one pass of the decode step's 21 launches (the
+    seven config-2 linears with the compensator at M = 1, 8, 32), without
+    graphs: a profiler skips the first 21 decode launches and captures the
+    next 21, i.e. exactly one step."""
     import torch
 
     from quantized_linear_error_gb300 import build, spear
     from quantized_linear_error_gb300 import workload as wl
+    build.build()
+    specs = wl.config_linears(2)
+    hs = [spear.from_weights(wl.make_weights(sp, 0), max_tokens=32) for sp in specs]
+    gen = torch.Generator().manual_seed(0)
+    xs = {(M, K): torch.randn((M, K), generator=gen).to(torch.bfloat16).cuda()
+          for M in DECODE_TOKENS for K in (4096, 11008)}
+    ys = {(M, N): torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+          for M in DECODE_TOKENS for N in (4096, 11008)}
+    for _ in range(2):
+        for M in DECODE_TOKENS:
+            for h, sp in zip(hs, specs):
+                h.forward_decode(xs[(M, sp.K)], ys[(M, sp.N)])
+    torch.cuda.synchronize()
+    for h in hs:
+        if h.check() != spear.SPEAR_OK:
+            raise SystemExit("device status error")
+    print("case decode-step: ok")
+
+
+def run_case(case: str, reps: int = 5):
+    """Run one named linear `reps` times and exit (a target for profilers):
+    <decode|prefill>:<linear>:<M>[:noec], <linear> a workload linear name such
+    as c2/q, c2/gate, c3/gate, c4/up; or decode-step (see run_step_case)."""
+    import torch
+
+    from quantized_linear_error_gb300 import build, spear
+    from quantized_linear_error_gb300 import workload as wl
+    if case == "decode-step":
+        return run_step_case()
     parts = case.split(":")
     path, name, M = parts[0], parts[1], int(parts[2])
     ec = not (len(parts) > 3 and parts[3] == "noec")
@@ -402,7 +432,7 @@ def run_case(case: str, reps: int = 5):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-prefill", action="store_true")
