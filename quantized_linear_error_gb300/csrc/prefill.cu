@@ -11,10 +11,13 @@
 //     the gate and writes u' = bf16(alpha * gamma(z) * z), z = A x, [M][rank].
 //  2. Main kernel: A = W rows, dequantised in the CTA: the TMA warp brings
 //     the packed INT4 tile and its scale/zero words, four warps turn them into
-//     bf16 (q - z) * s (one rounding, the exported dequantised value) and
-//     write the swizzled A tile; B = x tokens by TMA. After the K blocks of W
+//     bf16 (q - z) * s (one rounding, the exported dequantised value), one
+//     row per thread, and write them straight into a 4-deep ring of A
+//     operands in tensor memory (tcgen05.st), so the dequantised tile never
+//     passes through shared memory; B = x tokens by TMA. After the K blocks of W
 //     come ceil(rank / 64) more K blocks with A = rows of the compensator's B
-//     matrix and B = u', both by TMA: since W x + B u' = [W | B] [x ; u'],
+//     matrix (read by the same four warps into the same ring) and B = u' by
+//     TMA: since W x + B u' = [W | B] [x ; u'],
 //     the same accumulator absorbs the compensator term. The epilogue reads
 //     TMEM (lane = output row n, column = token) and stores y in bf16.
 //
@@ -36,11 +39,13 @@ constexpr int kRawWBytes = 128 * 8 * 4;        // 128 rows x 64 codes, packed
 constexpr int kRawBytes = kRawWBytes + 128 * 4;  // plus one scale/zero word per row
 constexpr int kBarrierBytes = 1024;
 constexpr int kMaxStages = 6;
+constexpr int kNA = 4;                 // A operands in tensor memory (main kernel)
+constexpr uint32_t kTmemA = 256;       // first column of the A ring (after the accumulator)
 
 struct GemmParams {
   int kblocks;      // K blocks of 64 from the main operands (per split for the pre-kernel)
   int kb_total;     // all K blocks (the last split may be shorter)
-  int tail_blocks;  // compensator K blocks (A from mapAt, B from mapBt)
+  int tail_blocks;  // compensator K blocks (main kernel: A rows of B through tensor memory, B = u' from mapBt)
   int TN;           // B rows per tile = MMA N (multiple of 16, <= 256)
   int a_rows;       // rows of the A operand (W rows, or tokens for the pre-kernel)
   int b_rows;       // rows of the B operand (tokens, or rank for the pre-kernel)
@@ -57,6 +62,8 @@ struct GemmParams {
   int NS;
   uint32_t a_bytes, b_bytes, raw_bytes, stage_bytes;
   uint32_t tmem_cols;
+  const __nv_bfloat16* bt;  // main kernel: compensator B rows [nt128 * 128][rank] (the K-tail's A operand)
+  int rank;
   float* zacc;          // pre-kernel: fp32 [M][rank] partial sums of z (zero between calls)
   unsigned* tile_done;  // pre-kernel: per 128-token tile, splits finished
   int splits;
@@ -64,9 +71,6 @@ struct GemmParams {
 
 SPEAR_DEVINL void fail(const GemmParams& p) { atomicOr(p.status, kStatusTimeoutPipe); }
 
-SPEAR_DEVINL void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
 
 SPEAR_DEVINL uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   uint32_t r;
@@ -101,7 +105,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full_a = full_tma + 8;
   uint64_t* empty = full_tma + 16;
   uint64_t* acc_full = full_tma + 24;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 256);
+  uint64_t* a_empty = full_tma + 25;  // main kernel: A ring in tensor memory free again
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 384);
   uint8_t* stages = smem + kBarrierBytes;
   const uint32_t stages_s = smem_u32(stages);
 
@@ -117,8 +122,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
       mbar_init(&full_tma[s], 1);
-      mbar_init(&full_a[s], 4);
       mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < kNA; ++s) {
+      mbar_init(&full_a[s], 4);
+      mbar_init(&a_empty[s], 1);
     }
     mbar_init(acc_full, 1);
     fence_mbar_init();
@@ -132,11 +140,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_d = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Grid dependencies. The pre-kernel reads x, written by the previous kernel:
+  // it waits for that grid, then lets the main kernel launch. The main kernel
+  // can then read x at once (x's producer has completed) and waits for the
+  // pre-kernel only before it loads u' for its compensator K-tail; without a
+  // compensator it waits for its predecessor here. Either kernel lets the
+  // next one launch early; the next one waits for it before reading anything
+  // it writes.
+  const bool late_wait = DEQ && p.tail_blocks > 0;
+  if (!late_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
+      if (DEQ && p.tail_blocks > 0) prefetch_l2(p.bt + (size_t)a0 * p.rank, 128u * p.rank * 2u);
       for (int it = 0; it < total; ++it) {
         const int s = it % p.NS;
         if (it >= p.NS && !mbar_wait_bounded(&empty[s], ((it / p.NS) - 1) & 1, p.wait_ns)) {
@@ -159,9 +177,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tma_load_2d(B, &mapB, (kb0 + it) * 64, b0, &full_tma[s]);
         } else {
+          // compensator K-tail: A rows come through the tensor-memory ring,
+          // B = u' from the pre-kernel
           const int t = it - kmain;
-          mbar_arrive_expect_tx(&full_tma[s], kATileBytes + p.b_bytes);
-          tma_load_2d(A, &mapAt, t * 64, a0, &full_tma[s]);
+          if (t == 0 && late_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
+          mbar_arrive_expect_tx(&full_tma[s], p.b_bytes);
           tma_load_2d(B, &mapBt, t * 64, b0, &full_tma[s]);
         }
       }
@@ -177,60 +197,96 @@ __global__ void __launch_bounds__(kThreads, 1)
           fail(p);
           break;
         }
-        if (DEQ && it < kmain && !mbar_wait_bounded(&full_a[s], par, p.wait_ns)) {
+        const int ab = it % kNA;
+        if (DEQ && !mbar_wait_bounded(&full_a[ab], (it / kNA) & 1, p.wait_ns)) {
           fail(p);
           break;
         }
         tc_fence_after_sync();
         const uint32_t a_s = stages_s + s * p.stage_bytes;
         const uint32_t b_s = a_s + p.a_bytes;
+        if (DEQ) {
+          // A from the tensor-memory ring: 8 columns (16 channels) per k16 step
 #pragma unroll
-        for (int k16 = 0; k16 < 4; ++k16)
-          umma_bf16(tmem_d, sw128_kmajor_desc(a_s + 32 * k16), sw128_kmajor_desc(b_s + 32 * k16), idesc,
-                    (it | k16) != 0);
+          for (int k16 = 0; k16 < 4; ++k16)
+            umma_ts_bf16(tmem_d, tmem_d + kTmemA + 32 * ab + 8 * k16, sw128_kmajor_desc(b_s + 32 * k16), idesc,
+                         (it | k16) != 0);
+          umma_commit(&a_empty[ab]);
+        } else {
+#pragma unroll
+          for (int k16 = 0; k16 < 4; ++k16)
+            umma_bf16(tmem_d, sw128_kmajor_desc(a_s + 32 * k16), sw128_kmajor_desc(b_s + 32 * k16), idesc,
+                      (it | k16) != 0);
+        }
         umma_commit(&empty[s]);
       }
       umma_commit(acc_full);  // the accumulator is complete once every MMA above has finished
     }
   } else {
     // ---------------------------------------------------------- dequantisers
-    // Two threads per row: thread d takes words 4 (d % 2) .. + 3 (channels
-    // 32 (d % 2) .. + 31) of row d / 2 and of row d / 2 + 64, so each warp's
-    // 16-byte loads of the packed tile are contiguous and its 16-byte stores
-    // hit 8 distinct swizzled chunks per 8 lanes (no bank conflicts).
-    const int d = threadIdx.x - 64;  // 0..127
-    const int half = d & 1;
+    // One thread per row: warp w owns tensor-memory lanes 32 (w % 4) .. + 31,
+    // i.e. rows r = 32 (w % 4) + lane of the tile. Per K block a thread reads
+    // its row's 8 packed words and scale/zero word, makes 32 bf16 pairs (pair
+    // c = channels 2c, 2c + 1) and stores them as 32 columns of the A ring.
+    // The store of block it is still in flight while block it + 1 is
+    // converted; block it is published (full_a) once its store has completed.
     if constexpr (DEQ) {
-      for (int it = 0; it < p.kblocks; ++it) {
-        const int s = it % p.NS;
-        if (!mbar_wait_bounded(&full_tma[s], (it / p.NS) & 1, p.wait_ns)) {
-          fail(p);
-          break;
-        }
-        const uint32_t a_s = stages_s + s * p.stage_bytes;
-        const uint32_t raw_sa = a_s + p.a_bytes + p.b_bytes;
-#pragma unroll
-        for (int pass = 0; pass < 2; ++pass) {
-          const int r = (d >> 1) + 64 * pass;
-          const uint4 wv = lds128(raw_sa + (uint32_t)(r * 32 + half * 16));
+      const int q = warp & 3;
+      const int r = 32 * q + lane;
+      const uint32_t lane_base = tmem_d + ((uint32_t)(32 * q) << 16) + kTmemA;
+      int pending = -1;  // block whose store is in flight
+      for (int it = 0; it < total; ++it) {
+        const int s = it % p.NS, ab = it % kNA;
+        uint32_t v[32];
+        if (it < kmain) {
+          if (!mbar_wait_bounded(&full_tma[s], (it / p.NS) & 1, p.wait_ns)) {
+            fail(p);
+            break;
+          }
+          const uint32_t raw_sa = stages_s + s * p.stage_bytes + p.a_bytes + p.b_bytes;
+          const uint4 w0 = lds128(raw_sa + (uint32_t)(r * 32));
+          const uint4 w1 = lds128(raw_sa + (uint32_t)(r * 32 + 16));
           const uint32_t szw = lds32(raw_sa + kRawWBytes + r * 4);
           const uint32_t zz = biased_zero_x2(szw >> 16);
           const uint32_t sc = (szw & 0xFFFFu) | (szw << 16);
-          const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+          const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-          for (int j4 = 0; j4 < 4; ++j4) {
-            const int c = 4 * half + j4;
-            const uint32_t w = words[j4];
-            uint32_t v[4];
+          for (int c = 0; c < 8; ++c)
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              v[j] = bf16x2_mul(bf16x2_sub(int4_pair_to_bf16x2_biased(w >> (4 * j)), zz), sc);
-            st_shared_v4(a_s + r * 128 + ((c ^ (r & 7)) << 4), v[0], v[1], v[2], v[3]);
+              v[4 * c + j] = bf16x2_mul(bf16x2_sub(int4_pair_to_bf16x2_biased(words[c] >> (4 * j)), zz), sc);
+        } else {
+          // row a0 + r of the compensator's B, columns 64 t .. + 63 (zero past rank)
+          const int t = it - kmain;
+          const uint4* src = reinterpret_cast<const uint4*>(p.bt + (size_t)(a0 + r) * p.rank + t * 64);
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) {
+            const uint4 w = t * 64 + c8 * 8 < p.rank ? __ldg(src + c8) : make_uint4(0u, 0u, 0u, 0u);
+            v[4 * c8] = w.x;
+            v[4 * c8 + 1] = w.y;
+            v[4 * c8 + 2] = w.z;
+            v[4 * c8 + 3] = w.w;
           }
         }
-        fence_proxy_async_smem();  // make the generic-proxy tile visible to the tensor cores
+        if (pending >= 0) {
+          tmem_st_wait();
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full_a[pending % kNA]);
+        }
+        if (it >= kNA && !mbar_wait_bounded(&a_empty[ab], ((it / kNA) - 1) & 1, p.wait_ns)) {
+          fail(p);
+          pending = -1;
+          break;
+        }
+        tmem_st_x32(lane_base + 32 * ab, v);
+        pending = it;
+      }
+      if (pending >= 0) {
+        tmem_st_wait();
+        tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&full_a[s]);
+        if (lane == 0) mbar_arrive(&full_a[pending % kNA]);
       }
     }
 
@@ -288,20 +344,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence();
       }
       epilogue_bar();
-      if (last_split && row < p.a_rows) {
-        float* zr = p.zacc + (size_t)row * p.ld_out;
-        __nv_bfloat16* ur = p.out + (size_t)row * p.ld_out;
-        for (int c0 = 0; c0 < p.TN; c0 += 8) {
-          const float4 z0 = __ldcg(reinterpret_cast<const float4*>(zr + c0));
-          const float4 z1 = __ldcg(reinterpret_cast<const float4*>(zr + c0 + 4));
-          const float zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
-          uint32_t pk[4];
+      if (last_split) {
+        // Warp q finishes rows a0 + 32 q .. + 31, eight rows per round with all
+        // loads in flight; lanes run along the row (coalesced), 4 columns each.
+        for (int r0 = 0; r0 < 32; r0 += 8) {
+          for (int c = lane * 4; c < p.TN; c += 128) {
+            float4 zv[8];
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            pk[j] = pack_bf16x2(p.alpha * gate_apply(zz[2 * j], p.gate), p.alpha * gate_apply(zz[2 * j + 1], p.gate));
-          *reinterpret_cast<uint4*>(ur + c0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<float4*>(zr + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
-          *reinterpret_cast<float4*>(zr + c0 + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < 8; ++j) {
+              const int m = a0 + 32 * q + r0 + j;
+              zv[j] = m < p.a_rows ? __ldcg(reinterpret_cast<const float4*>(p.zacc + (size_t)m * p.ld_out + c))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int m = a0 + 32 * q + r0 + j;
+              if (m < p.a_rows) {
+                const uint2 pk = make_uint2(pack_bf16x2(p.alpha * gate_apply(zv[j].x, p.gate),
+                                                        p.alpha * gate_apply(zv[j].y, p.gate)),
+                                            pack_bf16x2(p.alpha * gate_apply(zv[j].z, p.gate),
+                                                        p.alpha * gate_apply(zv[j].w, p.gate)));
+                *reinterpret_cast<uint2*>(p.out + (size_t)m * p.ld_out + c) = pk;
+                *reinterpret_cast<float4*>(p.zacc + (size_t)m * p.ld_out + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+            }
+          }
         }
       }
       if (last_split && threadIdx.x == 64) p.tile_done[blockIdx.x] = 0;
@@ -380,9 +447,10 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
       return SPEAR_ERR_CUDA;
     GemmParams p{};
     const int kbt = K / 64, mt = (M + 127) / 128;
-    // K splits so that the pre-kernel spans about one wave, at least 4 K blocks each
-    int splits = (h->sm_count + mt - 1) / mt;
-    if (splits > kbt / 4) splits = kbt / 4;
+    // About 32 CTAs (at least 8 K blocks each): the pre-kernel runs on a few
+    // SMs next to the main kernel, which needs u' only for its last K blocks.
+    int splits = (32 + mt - 1) / mt;
+    if (splits > kbt / 8) splits = kbt / 8;
     if (splits < 1) splits = 1;
     p.kblocks = (kbt + splits - 1) / splits;
     splits = (kbt + p.kblocks - 1) / p.kblocks;
@@ -414,14 +482,11 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
 
   // ---- main contraction with the compensator K-tail
   const int TN = prefill_tn(M);
-  CUtensorMap mx, mbt, mut;
+  CUtensorMap mx, mut;
   if (!encode_2d_bf16(&mx, x, K, M, (uint64_t)K * 2, 64, TN)) return SPEAR_ERR_CUDA;
   if (r > 0) {
-    if (!encode_2d_bf16(&mbt, h->b_pre, r, (uint64_t)h->nt128 * 128, (uint64_t)r * 2, 64, 128) ||
-        !encode_2d_bf16(&mut, h->u_pre, r, M, (uint64_t)r * 2, 64, TN))
-      return SPEAR_ERR_CUDA;
+    if (!encode_2d_bf16(&mut, h->u_pre, r, M, (uint64_t)r * 2, 64, TN)) return SPEAR_ERR_CUDA;
   } else {
-    mbt = none;
     mut = none;
   }
   GemmParams p{};
@@ -443,13 +508,15 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
   p.gate = h->gate;
   p.status = &h->sync->status;
   p.wait_ns = h->wait_ns;
-  p.a_bytes = kATileBytes;
+  p.a_bytes = 0;  // every A operand of the main kernel lives in tensor memory
+  p.bt = h->b_pre;
+  p.rank = r;
   p.b_bytes = (uint32_t)(TN * 128 + 1023) / 1024 * 1024;
   p.raw_bytes = kRawBytes;
   p.stage_bytes = (p.a_bytes + p.b_bytes + kRawBytes + 1023) / 1024 * 1024;
   p.NS = stages_for(p.stage_bytes);
-  p.tmem_cols = tmem_cols_for(TN);
+  p.tmem_cols = 512;  // accumulator (TN <= 256 columns) + the A ring from column 256
   const size_t smem = kBarrierBytes + 1024 + (size_t)p.NS * p.stage_bytes;
-  e = launch<true, 0>(p, dim3(h->nt128, (M + TN - 1) / TN), smem, stream, none, mx, mbt, mut);
+  e = launch<true, 0>(p, dim3(h->nt128, (M + TN - 1) / TN), smem, stream, none, mx, none, mut);
   return e == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
 }
