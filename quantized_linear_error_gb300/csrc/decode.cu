@@ -3,7 +3,7 @@
 // Recovery", section 2.2A: in the memory-bound decode phase the compensator is
 // fused into the low-bit GEMM so the correction path is a single kernel).
 //
-// Design (one CTA per SM; 8 or 16 consumer warps + 1 producer warp):
+// Design (one CTA per SM; 16 consumer warps, 8 for M > 16 with <= 2 tiles per CTA, + 1 producer warp):
 //  * The CTA owns P consecutive 16-row tiles of W. A producer warp streams K
 //    in stages: per stage one bulk copy brings the tiles' packed codes and
 //    scale/zero words (laid out at create as one contiguous run per CTA and
@@ -129,6 +129,17 @@ SPEAR_DEVINL void mma_bf16_16816_zero(float (&d)[4], const uint32_t (&a)[4], uin
 SPEAR_DEVINL void ec_bar() {
   __syncwarp();
   asm volatile("bar.sync 2, %0;" ::"n"(kEcWarps * 32) : "memory");
+}
+
+// The x fragments of k16 step kk of a unit only (MT >= 2: fewer live registers).
+template <int MT>
+SPEAR_DEVINL void load_kk_x_frags(const uint32_t (&lane_base)[8], int kk, uint32_t (&b)[MT][2]) {
+  constexpr int Mp = 8 * MT;
+  const int c = (2 * kk) & 7;
+  const uint32_t blk = (kk >> 2) * Mp * 128;
+#pragma unroll
+  for (int pr = 0; pr < MT / 2; ++pr)
+    ldsm_x4(b[2 * pr][0], b[2 * pr][1], b[2 * pr + 1][0], b[2 * pr + 1][1], lane_base[c] + blk + pr * 16 * 128);
 }
 
 SPEAR_DEVINL uint32_t word_of(const uint4& v, int i) {
@@ -458,11 +469,15 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
       const uint32_t ub = st + (uint32_t)(2 * u) * (Mp * 128) + lane_off;
 #pragma unroll
       for (int c = 0; c < 8; ++c) lane_base[c] = ub + swz[c];
-      uint32_t bb[8][MT][2];
-      load_unit_x_frags<MT>(lane_base, bb);
+      // M <= 8: all eight k16 steps' x fragments at once (16 registers);
+      // wider M: per k16 step
+      uint32_t bb[MT == 1 ? 8 : 1][MT][2];
+      if constexpr (MT == 1) load_unit_x_frags<MT>(lane_base, reinterpret_cast<uint32_t(&)[8][MT][2]>(bb));
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t(&b)[MT][2] = bb[kk];
+        uint32_t bk[MT][2];
+        if constexpr (MT > 1) load_kk_x_frags<MT>(lane_base, kk, bk);
+        const uint32_t(&b)[MT][2] = MT == 1 ? bb[MT == 1 ? kk : 0] : bk;
 #pragma unroll
         for (int t = 0; t < T; ++t) {
           const int tl = pw_i * T + t;
@@ -700,13 +715,13 @@ spear_status_t spear_launch_decode(spear_linear_s* h, const __nv_bfloat16* x, __
 
   const bool pc = h->per_channel;
   cudaError_t e;
-  // 16 consumer warps hold at most 16 tiles with T = 1 (create limits P to 16)
+  // one tile per consumer warp at most (create limits P to 16)
   if (MT == 1)
     e = launch_t<16, 1, 1>(p, xmap, pc, ec, grid, smem, stream);
   else if (MT == 2)
     e = launch_t<16, 2, 1>(p, xmap, pc, ec, grid, smem, stream);
   else
-    e = T == 1 ? launch_t<8, 4, 1>(p, xmap, pc, ec, grid, smem, stream)
-               : launch_t<8, 4, 2>(p, xmap, pc, ec, grid, smem, stream);
+    e = NW == 8 ? launch_t<8, 4, 1>(p, xmap, pc, ec, grid, smem, stream)
+                : launch_t<16, 4, 1>(p, xmap, pc, ec, grid, smem, stream);
   return e == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
 }

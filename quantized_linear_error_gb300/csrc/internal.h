@@ -118,7 +118,9 @@ inline int decode_tiles_per_cta(int nt16, int sm_count) { return (nt16 + sm_coun
 // tiles per warp, KW warps splitting K, KC channels per pipeline stage (a
 // whole number of layout runs).
 inline void decode_plan(int P, int K, int M, int* NW, int* T, int* KW, int* KC) {
-  *NW = M <= 16 ? 16 : 8;
+  // M > 16: with one or two tiles per CTA, 8 warps already split K four ways
+  // (measured faster than 16); with more tiles 16 warps keep every warp busy.
+  *NW = (M > 16 && P <= 2) ? 8 : 16;
   *T = P > *NW ? 2 : 1;
   const int pw = (P + *T - 1) / *T;  // warps along rows
   *KW = *NW / pw;                    // warps along K; 128-channel units go round-robin
@@ -127,9 +129,13 @@ inline void decode_plan(int P, int K, int M, int* NW, int* T, int* KW, int* KC) 
   int kc = kDecodeRun * *KW;
   const int kr = (K + kDecodeRun - 1) / kDecodeRun * kDecodeRun;
   if (kc > kr) kc = kr;
+  // x box of a stage (KC channels x Mp tokens, bf16) at most 64 KB
+  const int mp = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
+  const int kx = 32768 / mp / kDecodeRun * kDecodeRun;
+  if (kc > kx) kc = kx;
   *KC = kc;
 }
-constexpr int kDecodeMaxTilesPerCta = 16;  // 8 warps x T = 2 tiles (M > 16)
+constexpr int kDecodeMaxTilesPerCta = 16;  // 16 consumer warps x one tile each
 constexpr size_t kZDecFloats = 256 * 32;
 
 // Tensor map over x [M][K] bf16 viewed as {64, M, K/64} (strides K*2 and 128
