@@ -202,6 +202,113 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ other workloads
+def measure_other_configs(args, stream, time_graphs, dev, hbm_peak, bf16_peak, with_config5):
+    """Configs 1 and 4 through the decode kernel (with their EC-off twins) and,
+    if asked, config 5 (the mixed serving step) through the prefill path. Every
+    timed pass streams more than the 129 MB L2 from HBM: config 1 rotates 64
+    handle copies (158 MB), config 4 is 275 MB per pass, config 5 3.4 GB."""
+    import torch
+
+    from quantized_linear_error_gb300 import spear
+    from quantized_linear_error_gb300 import workload as wl
+
+    def graph_of(calls):
+        with torch.cuda.stream(stream):
+            for f in calls:  # warm-up outside capture (configures the kernels)
+                f()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for f in calls:
+                f()
+        return g
+
+    def no_ec(w):
+        return wl.LinearWeights(wl.LinearSpec(w.spec.name, w.spec.K, w.spec.N, w.spec.group_size, 0),
+                                w.q, w.s, w.z, None, None, w.outliers)
+
+    out = {}
+    steps = max(20, args.steps // 20)
+
+    # config 1: one 2048 x 2048 linear (g128, EC r32) at M = 4
+    sp = wl.config_linears(1)[0]
+    M = wl.CONFIG_TOKENS[1][0]
+    w = wl.make_weights(sp, 0)
+    x = dev(wl.make_x(sp.K, M, w.outliers, 0, sp.name))
+    y = torch.empty((M, sp.N), dtype=torch.bfloat16, device="cuda")
+    res = {}
+    for ec in (True, False):
+        hs = [spear.from_weights(w if ec else no_ec(w), max_tokens=M, stream=stream) for _ in range(64)]
+        g = graph_of([lambda h=h: h.forward_decode(x, y, stream=stream) for h in hs])
+        t = time_graphs([g], steps, 3) / len(hs)  # ms per call
+        b = (sp if ec else no_ec(w).spec).algorithmic_bytes(M)
+        res[ec] = {"us_per_call": t * 1e3, "tokens_per_s": M / (t / 1e3), "hbm_gbs": b / (t / 1e3) / 1e9,
+                   "frac_hbm": b / (t / 1e3) / 1e9 / hbm_peak}
+        for h in hs:
+            if h.check() != spear.SPEAR_OK:
+                raise SystemExit("config 1 device status error")
+            h.close()
+        del g
+    out["1"] = {"workload": "2048x2048, INT4 g128, EC r32, M=4 (64 rotating copies)", **res[True],
+                "ec_off": res[False]}
+
+    # config 4: Llama-70B-shaped MLP pair, per-channel scales, EC r256, M = 16
+    specs = wl.config_linears(4)
+    M = wl.CONFIG_TOKENS[4][0]
+    ws = [wl.make_weights(s4, 0) for s4 in specs]
+    xs = [dev(wl.make_x(s4.K, M, w4.outliers, 0, s4.name)) for s4, w4 in zip(specs, ws)]
+    ys = [torch.empty((M, s4.N), dtype=torch.bfloat16, device="cuda") for s4 in specs]
+    res = {}
+    for ec in (True, False):
+        hs = [spear.from_weights(w4 if ec else no_ec(w4), max_tokens=M, stream=stream) for w4 in ws]
+        g = graph_of([lambda h=h, xx=xx, yy=yy: h.forward_decode(xx, yy, stream=stream)
+                      for h, xx, yy in zip(hs, xs, ys)])
+        t = time_graphs([g], steps, 3)
+        b = sum((s4 if ec else no_ec(w4).spec).algorithmic_bytes(M) for s4, w4 in zip(specs, ws))
+        res[ec] = {"us_per_step": t * 1e3, "tokens_per_s": M / (t / 1e3), "hbm_gbs": b / (t / 1e3) / 1e9,
+                   "frac_hbm": b / (t / 1e3) / 1e9 / hbm_peak}
+        for h in hs:
+            if h.check() != spear.SPEAR_OK:
+                raise SystemExit("config 4 device status error")
+            h.close()
+        del g
+    out["4"] = {"workload": "8192->28672 and 28672->8192, INT4 per-channel, EC r256, M=16", **res[True],
+                "ec_off": res[False]}
+    del ws, xs, ys
+
+    if with_config5:
+        # config 5: 32 Llama-7B-shaped layers (7 projections each), EC r64 on four
+        # seeded layers, one batch of 64 decode tokens + a prefill chunk C per linear
+        specs = wl.config_linears(5)
+        base = {s5.name.split("/")[-1]: wl.make_weights(s5, 0) for s5 in wl.llama7b_layer("c5/", rank=64)}
+        mmax = max(wl.CONFIG_TOKENS[5])
+        hs = []
+        for s5 in specs:
+            w = base[s5.name.split("/")[-1]]
+            hs.append(spear.from_weights(w if s5.rank else no_ec(w), max_tokens=mmax, stream=stream))
+        res = {}
+        for M in wl.CONFIG_TOKENS[5]:
+            xs = {K: dev(wl.make_x(K, M, base["q" if K == 4096 else "down"].outliers, 0, f"c5/x{K}"))
+                  for K in (4096, 11008)}
+            ys = {N: torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for N in (4096, 11008)}
+            g = graph_of([lambda h=h, s5=s5: h.forward_prefill(xs[s5.K], ys[s5.N], stream=stream)
+                          for h, s5 in zip(hs, specs)])
+            t = time_graphs([g], max(3, args.steps // 200), 2)
+            fl = sum(s5.flops(M) for s5 in specs)
+            res[str(M - 64)] = {"tokens": M, "ms_per_step": t, "tokens_per_s": M / (t / 1e3),
+                                "tflops": fl / (t / 1e3) / 1e12, "frac_bf16_peak": fl / (t / 1e3) / 1e12 / bf16_peak}
+            del g
+        for h in hs:
+            if h.check() != spear.SPEAR_OK:
+                raise SystemExit("config 5 device status error")
+            h.close()
+        out["5"] = {"workload": "32-layer Llama-7B-shaped stack (224 linears), INT4 g128, EC r64 on layers "
+                                f"{wl.ec_layer_indices(0)}, 64 decode tokens + prefill chunk C, one CUDA graph "
+                                "per step", "by_chunk": res}
+    return out
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_ours(args, world, rank, local):
     import numpy as np
@@ -339,6 +446,11 @@ def run_ours(args, world, rank, local):
             if h.check() != spear.SPEAR_OK:
                 raise SystemExit("prefill device status error")
 
+    # --- the other workloads: config 1 and 4 (decode), config 5 (mixed serving step, on request)
+    configs = None
+    if not args.skip_configs:
+        configs = measure_other_configs(args, stream, time_graphs, dev, hbm_peak, bf16_peak, args.config5)
+
     # --- roofline of the decode kernel (the only kernel in the step)
     launches = len(DECODE_TOKENS) * len(specs)
     achieved = bytes_step / (ms_step / 1e3) / 1e9
@@ -363,7 +475,7 @@ def run_ours(args, world, rank, local):
             "ec_off": {"ms_per_step": ms_noec, "tokens_per_s": tokens * world / (ms_noec / 1e3),
                        "hbm_gbs": decode_bytes(specs, False) / (ms_noec / 1e3) / 1e9,
                        "ec_overhead": ms_step / ms_noec - 1.0},
-            "prefill": prefill, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "prefill": prefill, "configs": configs, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches * args.steps, "clocks": clocks}
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -437,6 +549,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-configs", action="store_true", help="skip the config 1 and 4 measurements")
+    ap.add_argument("--config5", action="store_true", help="also measure config 5 (32-layer mixed serving step)")
     ap.add_argument("--case", help="run one small named case 5 times and exit (profiling target), "
                                    "e.g. decode:c2/q:1, decode:c4/up:16:noec, prefill:c3/gate:2048")
     args = ap.parse_args()
