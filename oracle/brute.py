@@ -48,7 +48,15 @@ def sigmoid(v: float) -> float:
     return 1.0 / (1.0 + math.exp(-v))
 
 
-def forward(q, s, z, K, G, A, B, alpha, gate, x) -> np.ndarray:
+def mlp_gamma(zvec, W1, W2) -> list:
+    """Bottleneck-MLP gate values gamma(z) = sigmoid(W2 relu(W1 z)) by plain
+    loops (W1 bf16 bits [h][r], W2 bf16 bits [r][h])."""
+    h, r = len(W1), len(zvec)
+    t = [max(0.0, sum(bf16_value(W1[i][j]) * zvec[j] for j in range(r))) for i in range(h)]
+    return [sigmoid(sum(bf16_value(W2[j][i]) * t[i] for i in range(h))) for j in range(r)]
+
+
+def forward(q, s, z, K, G, A, B, alpha, gate, x, W1=None, W2=None) -> np.ndarray:
     """y [M][N] from the explicitly materialised effective weight per token."""
     N = len(q)
     M = len(x)
@@ -60,7 +68,10 @@ def forward(q, s, z, K, G, A, B, alpha, gate, x) -> np.ndarray:
     for m in range(M):
         xm = [bf16_value(v) for v in x[m]]
         zvec = [sum(Af[j][k] * xm[k] for k in range(K)) for j in range(r)]
-        gam = [1.0 if gate == 1 else sigmoid(v) for v in zvec]
+        if gate == 2:
+            gam = mlp_gamma(zvec, W1, W2)
+        else:
+            gam = [1.0 if gate == 1 else sigmoid(v) for v in zvec]
         weff = [[W[n][k] + alpha * sum(Bf[n][j] * gam[j] * Af[j][k] for j in range(r))
                  for k in range(K)] for n in range(N)]
         for n in range(N):

@@ -43,7 +43,8 @@ def lib():
         L.oracle_dequant_f64.argtypes = [P, P, P, I, I, I, P]
         L.oracle_ec.argtypes = [P, P, I, I, I, I, P, P]
         L.oracle_gate.argtypes = [P, I, I, P]
-        L.oracle_forward.argtypes = [P, P, P, I, I, I, P, P, I, ctypes.c_double, I, P, I, P, I, P, I]
+        L.oracle_forward.argtypes = [P, P, P, I, I, I, P, P, I, ctypes.c_double, I, P, I, P, I, P, I, I, P, P]
+        L.oracle_gate_mlp.argtypes = [P, I, I, I, P, P, P]
         L.oracle_max_threads.restype = I
         _libs[plant] = L
     return _libs[plant]
@@ -107,10 +108,24 @@ def gate(z, gate=0):
     return u
 
 
-def forward(q, s, z, K, G, A, B, alpha, gate, x, rows=None, nthreads=0):
-    """y double [M][len(rows)] (all N rows when rows is None)."""
+def gate_mlp(z, W1, W2):
+    """u double [M][r] = sigmoid(W2 relu(W1 z)) * z per token; W1 bf16 [h][r], W2 bf16 [r][h]."""
+    z = _c(np.atleast_2d(z), np.float64)
+    W1, W2 = _c(W1, np.uint16), _c(W2, np.uint16)
+    M, r = z.shape
+    h = W1.shape[0]
+    u = np.empty_like(z)
+    lib().oracle_gate_mlp(_p(z), M, r, h, _p(W1), _p(W2), _p(u))
+    return u
+
+
+def forward(q, s, z, K, G, A, B, alpha, gate, x, rows=None, nthreads=0, W1=None, W2=None):
+    """y double [M][len(rows)] (all N rows when rows is None). gate 2 (MLP)
+    takes W1 bf16 [h][r] and W2 bf16 [r][h]."""
     q, s, z = _c(q, np.uint8), _c(s, np.uint16), _c(z, np.uint8)
     A, B, x = _c(A, np.uint16), _c(B, np.uint16), _c(x, np.uint16)
+    W1, W2 = _c(W1, np.uint16), _c(W2, np.uint16)
+    h = 0 if W1 is None else W1.shape[0]
     N = q.shape[0]
     r = 0 if A is None else A.shape[0]
     M = x.shape[0]
@@ -118,14 +133,15 @@ def forward(q, s, z, K, G, A, B, alpha, gate, x, rows=None, nthreads=0):
     nrows = N if rows_a is None else rows_a.size
     y = np.empty((M, nrows), np.float64)
     lib().oracle_forward(_p(q), _p(s), _p(z), N, K, G, _p(A), _p(B), r, float(alpha), gate,
-                         _p(x), M, _p(rows_a), nrows, _p(y), int(nthreads))
+                         _p(x), M, _p(rows_a), nrows, _p(y), int(nthreads), h, _p(W1), _p(W2))
     return y
 
 
 def forward_w(w, x, rows=None, nthreads=0):
     """Convenience: forward for a ``workload.LinearWeights``."""
     sp = w.spec
-    return forward(w.q, w.s, w.z, sp.K, sp.G, w.A, w.B, sp.alpha, sp.gate, x, rows, nthreads)
+    return forward(w.q, w.s, w.z, sp.K, sp.G, w.A, w.B, sp.alpha, sp.gate, x, rows, nthreads,
+                   getattr(w, "W1", None), getattr(w, "W2", None))
 
 
 def max_threads() -> int:

@@ -15,8 +15,13 @@
  * space, gamma is the input-dependent gate and B (N x r) projects back. Applied
  * to x this is y = W x + alpha * B (gamma(z) (.) z) with z = A x, which is the
  * form evaluated here (section 2.1A, "Mechanism"). The gate is the elementwise
- * sigmoid, or the constant 1 (the static low-rank correction W + alpha B A that
- * the paper contrasts with in section 1).
+ * sigmoid, the constant 1 (the static low-rank correction W + alpha B A that
+ * the paper contrasts with in section 1), or the bottleneck MLP the paper names
+ * for gamma (section 2.1A, "Mechanism"): per token,
+ *
+ *     gamma(z) = sigmoid(W2 relu(W1 z)),  W1 (h x r), W2 (r x h),
+ *
+ * with relu as the hidden activation (the paper does not name it).
  *
  * Everything is fp64. Inputs are bf16 bit patterns widened exactly.
  * Dequantisation is w = (q - zp) * s with q the 4-bit code, zp the integer zero
@@ -102,6 +107,30 @@ static double gated(double z, int gate) {
 
 /* ---------------------------------------------------------------- exports */
 
+/* Bottleneck-MLP gate for M tokens: t = relu(W1 z) (h values), gamma(z) =
+ * sigmoid(W2 t) (r values), u = gamma(z) (.) z.
+ * W1 bf16 [h][r]; W2 bf16 [r][h]; z, u double [M][r]. */
+void oracle_gate_mlp(const double *z, int M, int r, int h, const uint16_t *W1, const uint16_t *W2,
+                     double *u) {
+    double *t = (double *)malloc(sizeof(double) * (size_t)(h > 0 ? h : 1));
+    for (int m = 0; m < M; ++m) {
+        const double *zm = z + (size_t)m * r;
+        for (int i = 0; i < h; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < r; ++j)
+                acc += bf16_to_double(W1[SPEAR_PLANT == 11 ? (size_t)j * h + i : (size_t)i * r + j]) * zm[j];
+            t[i] = (SPEAR_PLANT == 10 || acc > 0.0) ? acc : 0.0;
+        }
+        for (int j = 0; j < r; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < h; ++i) acc += bf16_to_double(W2[(size_t)j * h + i]) * t[i];
+            double g = SPEAR_PLANT == 12 ? acc : 1.0 / (1.0 + exp(-acc));
+            u[(size_t)m * r + j] = g * zm[j];
+        }
+    }
+    free(t);
+}
+
 /* bf16 dequantised weights, one RNE rounding of the exact (q - z) * s.
  * q uint8 [N][K/2]; s bf16 [N][K/G]; zp uint8 [N][K/G] or NULL; out bf16 [N][K]. */
 void oracle_dequant_bf16(const uint8_t *q, const uint16_t *s, const uint8_t *zp,
@@ -145,13 +174,15 @@ void oracle_gate(const double *z, int count, int gate, double *u) {
 /* Full forward for a set of output rows.
  *   y[m][i] = sum_k W[rows[i]][k] x[m][k] + alpha * sum_j B[rows[i]][j] u[m][j]
  * with u = gamma(A x) (.) (A x). rows == NULL means all N rows (nrows = N).
+ * gate 2 (bottleneck MLP) reads gate_hidden, W1 and W2; the others ignore them.
  * rank == 0 (or A/B NULL) means no compensator. y is double [M][nrows].
  * nthreads <= 0 keeps the OpenMP default. */
 void oracle_forward(const uint8_t *q, const uint16_t *s, const uint8_t *zp,
                     int N, int K, int G,
                     const uint16_t *A, const uint16_t *B, int rank, double alpha, int gate,
                     const uint16_t *x, int M,
-                    const int64_t *rows, int nrows, double *y, int nthreads) {
+                    const int64_t *rows, int nrows, double *y, int nthreads,
+                    int gate_hidden, const uint16_t *W1, const uint16_t *W2) {
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
 #endif
@@ -159,7 +190,14 @@ void oracle_forward(const uint8_t *q, const uint16_t *s, const uint8_t *zp,
     double *u = NULL;
     if (use_ec) {
         u = (double *)malloc(sizeof(double) * (size_t)M * rank);
-        oracle_ec(A, x, rank, K, M, gate, NULL, u);
+        if (gate == 2) {
+            double *zz = (double *)malloc(sizeof(double) * (size_t)M * rank);
+            oracle_ec(A, x, rank, K, M, 1, zz, NULL);
+            oracle_gate_mlp(zz, M, rank, gate_hidden, W1, W2, u);
+            free(zz);
+        } else {
+            oracle_ec(A, x, rank, K, M, gate, NULL, u);
+        }
     }
     double *xd = (double *)malloc(sizeof(double) * (size_t)M * K);
     for (size_t i = 0; i < (size_t)M * K; ++i) xd[i] = bf16_to_double(x[i]);

@@ -35,6 +35,7 @@ import torch
 
 GATE_SIGMOID = 0
 GATE_ONE = 1
+GATE_MLP = 2
 
 
 def stream(base_seed: int, name: str) -> np.random.Generator:
@@ -69,6 +70,7 @@ class LinearSpec:
     rank: int = 0              # 0 means no error compensator
     alpha: float = 1.0
     gate: int = GATE_SIGMOID
+    gate_hidden: int = 16      # hidden width h of the bottleneck-MLP gate (GATE_MLP only)
 
     @property
     def G(self) -> int:
@@ -83,11 +85,15 @@ class LinearSpec:
         4-bit zeros, the EC's A and B, x read once and y written once."""
         w = self.N * self.K // 2 + self.N * self.n_groups * 2 + (self.N * self.n_groups + 1) // 2
         ec = self.rank * (self.K + self.N) * 2
+        if self.rank and self.gate == GATE_MLP:
+            ec += 2 * self.rank * self.gate_hidden * 2
         return w + ec + M * self.K * 2 + M * self.N * 2
 
     def flops(self, M: int) -> int:
-        """Multiply-adds x2 of the main contraction plus both EC projections."""
-        return 2 * M * self.K * self.N + 2 * M * self.rank * (self.K + self.N)
+        """Multiply-adds x2 of the main contraction plus both EC projections
+        (and the two layers of an MLP gate)."""
+        mlp = 4 * M * self.rank * self.gate_hidden if self.rank and self.gate == GATE_MLP else 0
+        return 2 * M * self.K * self.N + 2 * M * self.rank * (self.K + self.N) + mlp
 
 
 @dataclass
@@ -99,6 +105,8 @@ class LinearWeights:
     A: np.ndarray | None   # uint16 (bf16) [r][K]
     B: np.ndarray | None   # uint16 (bf16) [N][r]
     outliers: np.ndarray = field(default_factory=lambda: np.zeros(0, np.int64))
+    W1: np.ndarray | None = None   # uint16 (bf16) [h][r], MLP gate only
+    W2: np.ndarray | None = None   # uint16 (bf16) [r][h], MLP gate only
 
 
 def outlier_channels(K: int, base_seed: int, name: str) -> np.ndarray:
@@ -117,7 +125,13 @@ def make_weights(spec: LinearSpec, base_seed: int = 0, prefix: str = "") -> Line
     if r > 0:
         A = to_bf16_bits(stream(base_seed, f"{name}/A").normal(0.0, 0.02, size=(r, K)).astype(np.float32))
         B = to_bf16_bits(stream(base_seed, f"{name}/B").normal(0.0, 0.02, size=(N, r)).astype(np.float32))
-    return LinearWeights(spec, q, s, z, A, B, outlier_channels(K, base_seed, name))
+    W1 = W2 = None
+    if r > 0 and spec.gate == GATE_MLP:
+        # weights of unit gain per layer: hidden pre-activations and gate logits O(1)
+        h = spec.gate_hidden
+        W1 = to_bf16_bits(stream(base_seed, f"{name}/W1").normal(0.0, r ** -0.5, size=(h, r)).astype(np.float32))
+        W2 = to_bf16_bits(stream(base_seed, f"{name}/W2").normal(0.0, h ** -0.5, size=(r, h)).astype(np.float32))
+    return LinearWeights(spec, q, s, z, A, B, outlier_channels(K, base_seed, name), W1, W2)
 
 
 def make_x(K: int, M: int, outliers: np.ndarray, base_seed: int = 0, name: str = "x") -> np.ndarray:

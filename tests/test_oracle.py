@@ -12,6 +12,8 @@ mathematics rather than against itself:
   W + alpha B A, both evaluated with numpy's matmul on independently unpacked
   weights;
 * the gate against torch's SiLU and closed-form sigmoid values;
+* the bottleneck-MLP gate against sigma(0) = 1/2, hand-derived sparse cases
+  and its reduction to the elementwise sigmoid gate for W1 = W2 = I, z >= 0;
 * special inputs: A = 0, B = 0, q = z (compensator alone), x = e_k.
 """
 import math
@@ -130,6 +132,52 @@ def test_gate_is_silu():
     np.testing.assert_allclose(ref.gate(z, 0), _silu(z), rtol=1e-14, atol=1e-300)
 
 
+def _bits(a):
+    return wl.to_bf16_bits(np.asarray(a, np.float32))
+
+
+def test_mlp_gate_with_zero_output_layer_is_one_half():
+    """W2 = 0: every gate logit is 0 and sigma(0) = 1/2 exactly, whatever W1."""
+    rng = np.random.default_rng(11)
+    z = rng.normal(0, 3, size=(5, 16))
+    W1 = _bits(rng.normal(0, 1, size=(4, 16)))
+    u = ref.gate_mlp(z, W1, np.zeros((16, 4), np.uint16))
+    np.testing.assert_array_equal(u, z / 2)
+
+
+def test_mlp_gate_sparse_hand_cases():
+    """r = h = 2, W1 = [[0, 1], [0, 0]] (t0 = relu(z1)), W2 = [[1, 0], [0, 0]]:
+    gamma = (sigma(relu(z1)), 1/2). z = (2, 3) gives u = (2 sigma(3), 3/2);
+    z = (2, -3) cuts the hidden unit: u = (1, -3/2)."""
+    W1 = _bits([[0, 1], [0, 0]])
+    W2 = _bits([[1, 0], [0, 0]])
+    sig3 = 1.0 / (1.0 + math.exp(-3.0))
+    np.testing.assert_allclose(ref.gate_mlp(np.array([[2.0, 3.0]]), W1, W2), [[2 * sig3, 1.5]], rtol=1e-15)
+    np.testing.assert_array_equal(ref.gate_mlp(np.array([[2.0, -3.0]]), W1, W2), [[1.0, -1.5]])
+
+
+def test_mlp_gate_relu_and_shapes():
+    """r = 2, h = 1, W1 = [[1, -1]], W2 = [[2], [-1]]: t = relu(z0 - z1).
+    z = (1, 3): t = 0, u = z / 2; z = (3, 1): t = 2, u = (3 sigma(4), sigma(-2))."""
+    W1 = _bits([[1, -1]])
+    W2 = _bits([[2], [-1]])
+    np.testing.assert_array_equal(ref.gate_mlp(np.array([[1.0, 3.0]]), W1, W2), [[0.5, 1.5]])
+    s4, sm2 = 1 / (1 + math.exp(-4.0)), 1 / (1 + math.exp(2.0))
+    np.testing.assert_allclose(ref.gate_mlp(np.array([[3.0, 1.0]]), W1, W2), [[3 * s4, sm2]], rtol=1e-15)
+
+
+def test_mlp_gate_identity_reduces_to_sigmoid_gate():
+    """W1 = W2 = I (h = r): gamma_j = sigma(relu(z_j)), which for z >= 0 is the
+    elementwise sigmoid gate, i.e. u = SiLU(z) (compared with the separate
+    elementwise path of the oracle and with torch)."""
+    rng = np.random.default_rng(12)
+    z = np.abs(rng.normal(0, 2, size=(3, 16)))
+    eye = _bits(np.eye(16))
+    u = ref.gate_mlp(z, eye, eye)
+    np.testing.assert_allclose(u, ref.gate(z, 0), rtol=1e-15)
+    np.testing.assert_allclose(u, _silu(z), rtol=1e-14)
+
+
 def test_ec_projection_matches_numpy():
     _, q, s, z, A, B, x = _tiny(3, 16, 256, 128, 8, 3)
     zz, uu = ref.ec(A, x, 0)
@@ -145,6 +193,19 @@ def test_forward_matches_materialised_effective_weight(N, K, G, r, M, gate):
     alpha = 1.7
     yb = brute.forward(q, s, z, K, G, A, B, alpha, gate, x)
     yc = ref.forward(q, s, z, K, G, A, B, alpha, gate, x)
+    assert _rel(yc, yb) <= 1e-12
+
+
+@pytest.mark.parametrize("N,K,G,r,h,M", [(16, 64, 32, 8, 3, 3), (8, 48, 48, 4, 5, 2)])
+def test_forward_mlp_gate_matches_materialised_effective_weight(N, K, G, r, h, M):
+    _, q, s, z, A, B, x = _tiny(N + K + r + h, N, K, G, r, M)
+    rng = np.random.default_rng(N * h)
+    # A x is small (std 0.02 sqrt(K)); scale the gate weights so the gate varies
+    W1 = _bits(rng.normal(0, 4, size=(h, r)))
+    W2 = _bits(rng.normal(0, 4, size=(r, h)))
+    alpha = 1.3
+    yb = brute.forward(q, s, z, K, G, A, B, alpha, 2, x, W1, W2)
+    yc = ref.forward(q, s, z, K, G, A, B, alpha, 2, x, W1=W1, W2=W2)
     assert _rel(yc, yb) <= 1e-12
 
 
@@ -226,6 +287,14 @@ def test_workload_generator_properties():
     assert np.array_equal(w.q, w2.q) and np.array_equal(w.A, w2.A)
 
 
+def test_mlp_gate_generator():
+    sp = wl.LinearSpec("t/mlp", 1024, 64, 128, 32, gate=wl.GATE_MLP, gate_hidden=8)
+    w = wl.make_weights(sp, 0)
+    assert w.W1.shape == (8, 32) and w.W2.shape == (32, 8)
+    assert wl.make_weights(wl.LinearSpec("t/mlp", 1024, 64, 128, 32), 0).W1 is None
+    assert sp.algorithmic_bytes(1) == wl.LinearSpec("t/mlp", 1024, 64, 128, 32).algorithmic_bytes(1) + 2 * 32 * 8 * 2
+
+
 def test_config_shapes():
     assert [(l.K, l.N) for l in wl.config_linears(2)] == [
         (4096, 4096)] * 4 + [(4096, 11008)] * 2 + [(11008, 4096)]
@@ -238,7 +307,8 @@ def test_config_shapes():
 # ------------------------------------------------------------------ planted mistakes
 PLANTS = {1: "nibble order swapped", 2: "zero point added, not subtracted", 3: "gate drops the z factor",
           4: "B indexed transposed", 5: "alpha ignored", 6: "rounding ties away from zero",
-          7: "group index ignores the group size", 8: "sigmoid sign flipped", 9: "x reversed in A x"}
+          7: "group index ignores the group size", 8: "sigmoid sign flipped", 9: "x reversed in A x",
+          10: "MLP gate without the relu", 11: "MLP gate reads W1 transposed", 12: "MLP gate without the sigmoid"}
 
 _PIN_TESTS = [
     lambda: [test_golden_rounding(*c) for c in _golden_cases()],
@@ -254,6 +324,10 @@ _PIN_TESTS = [
     test_zero_projections_drop_compensator,
     test_codes_equal_zeros_leave_compensator_alone,
     test_unit_vector_input_picks_a_column,
+    test_mlp_gate_with_zero_output_layer_is_one_half,
+    test_mlp_gate_sparse_hand_cases,
+    test_mlp_gate_relu_and_shapes,
+    test_mlp_gate_identity_reduces_to_sigmoid_gate,
 ]
 
 
