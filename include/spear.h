@@ -12,8 +12,9 @@
  * weight with bf16 scales and integer zero points per group of 128 input
  * channels or per output channel (section 1 and section 3.1 use 4-bit weights,
  * per-channel being the hard case); A is rank x K, B is N x rank, gamma is the
- * elementwise sigmoid (or the constant one, which gives the static low-rank
- * correction W_q + alpha B A that section 1 contrasts with). Phase-aware
+ * elementwise sigmoid, the constant one (which gives the static low-rank
+ * correction W_q + alpha B A that section 1 contrasts with), or the
+ * bottleneck MLP that section 2.1A names for gamma. Phase-aware
  * dispatch (section 2.2A) is exposed as two entry points: a fused single-kernel
  * decode path for M <= 32 tokens and a tensor-core prefill path for larger M.
  *
@@ -53,7 +54,10 @@ typedef enum {
 
 typedef enum {
   SPEAR_GATE_SIGMOID = 0,      /* gamma(z) = 1 / (1 + exp(-z)), so gamma(z) * z = SiLU(z) */
-  SPEAR_GATE_ONE = 1           /* gamma = 1: static correction W_q + alpha B A */
+  SPEAR_GATE_ONE = 1,          /* gamma = 1: static correction W_q + alpha B A */
+  SPEAR_GATE_MLP = 2           /* bottleneck MLP ("SPEAR", section 2.1A, "Mechanism"), per token:
+                                  gamma(z) = sigmoid(W2 relu(W1 z)), W1 (h x rank), W2 (rank x h);
+                                  relu as the hidden activation is this library's reading */
 } spear_gate_t;
 
 typedef struct {
@@ -70,6 +74,10 @@ typedef struct {
   float alpha;                 /* compensator strength */
   spear_gate_t gate;
   int32_t max_tokens;          /* largest M any forward on this handle will use (>= 1) */
+  /* SPEAR_GATE_MLP only (ignored otherwise; zero them for the other gates): */
+  int32_t gate_hidden;         /* h, 1 <= h <= 64 */
+  const void* gate_w1;         /* device, bf16 [h][rank], 16-byte aligned */
+  const void* gate_w2;         /* device, bf16 [rank][h], 16-byte aligned */
 } spear_linear_desc_t;
 
 /* Build a handle from user-layout weights ("SPEAR", section 2.1A: the W_q of the
@@ -78,9 +86,11 @@ typedef struct {
  * `stream`, then synchronises `stream`, so the caller may free or reuse its
  * buffers as soon as this returns. On success *out holds the handle.
  * Errors: INVALID_ARG (null desc/out/pointers, K % 128, N % 8, bad group size,
- * rank not a multiple of 16 or > 256, max_tokens < 1), UNSUPPORTED (shape
- * outside the kernels' limits: N > 16 * 16 * SM count for the decode path),
- * OOM, CUDA. On error *out is left NULL and nothing is leaked. */
+ * rank not a multiple of 16 or > 256, max_tokens < 1; for SPEAR_GATE_MLP:
+ * rank == 0, gate_hidden outside 1..64, null or unaligned gate weights),
+ * UNSUPPORTED (shape outside the kernels' limits: N > 16 * 16 * SM count for
+ * the decode path), OOM, CUDA. On error *out is left NULL and nothing is
+ * leaked. */
 spear_status_t spear_linear_create(const spear_linear_desc_t* desc, cudaStream_t stream,
                                    spear_linear_t* out);
 
@@ -146,6 +156,7 @@ spear_status_t spear_linear_debug_set(spear_linear_t h, int64_t wait_ns, int32_t
  *   x: device bf16 [M][K]; y: device bf16 [M][N]; 1 <= M <= 32 (0 is a no-op).
  * Result: y = bf16_RNE(W_q x + alpha B (gamma(Ax) (.) Ax)), fp32 accumulation,
  * as spear_linear_forward_decode computes (summation order differs).
+ * SPEAR_GATE_MLP is not supported here (SPEAR_ERR_UNSUPPORTED).
  * Scratch: the compensator projection z and an arrival counter live in one
  * static device array of the library (33,024 bytes, held on every GPU that
  * loads the library until the process exits); it bounds rank <= 256 and

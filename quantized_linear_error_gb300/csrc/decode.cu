@@ -50,6 +50,9 @@ struct DecodeParams {
   uint32_t bytes_x, stage_bytes;  // x box bytes (KC * Mp * 2), bytes per stage buffer
   uint64_t wait_ns;
   int skip_arrive;
+  const __nv_bfloat16* gw1;  // SPEAR_GATE_MLP: W1 [gh][rank]
+  const __nv_bfloat16* gw2;  // SPEAR_GATE_MLP: W2 [rank][gh]
+  int gh;
 };
 
 // Named barrier of the consumer warps. bar.sync counts whole warps, so each
@@ -164,6 +167,47 @@ SPEAR_DEVINL void ec_prefetch(const DecodeParams& p, int ew, int lane) {
     }
 }
 
+// Bottleneck-MLP gate ("SPEAR", section 2.1A: gamma is a bottleneck MLP):
+// u = alpha * sigmoid(W2 relu(W1 z)) (.) z per token, by the four compensator
+// warps on z staged in shared memory (zs [M][rank], hidden ts [M][gh]); u is
+// written split into bf16 hi + lo like the elementwise gates (zero for tokens
+// M..Mp-1, and everywhere if z never arrived).
+template <int Mp>
+SPEAR_DEVINL void ec_u_mlp(const DecodeParams& p, bool arrived, int tid, float* zs, float* ts, __nv_bfloat16* uh,
+                           __nv_bfloat16* ul, int us) {
+  constexpr int kThr = kEcWarps * 32;
+  const int r = p.rank, hh = p.gh, M = p.M;
+  for (int i = tid; i < M * r; i += kThr) {
+    const int m = i / r, j = i - m * r;
+    zs[i] = arrived ? __ldcg(p.z + j * 32 + m) : 0.f;
+  }
+  ec_bar();
+  for (int i = tid; i < M * hh; i += kThr) {
+    const int m = i / hh, c = i - m * hh;
+    const __nv_bfloat16* w = p.gw1 + (size_t)c * r;
+    const float* zm = zs + m * r;
+    float acc = 0.f;
+    for (int j = 0; j < r; ++j) acc = fmaf(__bfloat162float(w[j]), zm[j], acc);
+    ts[i] = fmaxf(acc, 0.f);
+  }
+  ec_bar();
+  for (int i = tid; i < Mp * r; i += kThr) {
+    const int m = i / r, j = i - m * r;
+    float uval = 0.f;
+    if (arrived && m < M) {
+      const __nv_bfloat16* w = p.gw2 + (size_t)j * hh;
+      const float* tm = ts + m * hh;
+      float acc = 0.f;
+      for (int c = 0; c < hh; ++c) acc = fmaf(__bfloat162float(w[c]), tm[c], acc);
+      uval = p.alpha * zs[m * r + j] * (1.0f / (1.0f + expf(-acc)));
+    }
+    __nv_bfloat16 hi, lo;
+    split_bf16(uval, hi, lo);
+    uh[m * us + j] = hi;
+    ul[m * us + j] = lo;
+  }
+}
+
 // z += A[:, this CTA's share] x, via warp MMA with A rows as the M side.
 template <int MT>
 SPEAR_DEVINL void ec_project(const DecodeParams& p, int ew, int lane) {
@@ -222,6 +266,7 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
   const int us = p.rank + 8;  // bf16 elements per token row of u
   __nv_bfloat16* uh = reinterpret_cast<__nv_bfloat16*>(szpc + (PC ? p.P * 16 : 0));
   __nv_bfloat16* ul = uh + Mp * us;
+  float* zs_mlp = reinterpret_cast<float*>(ul + Mp * us);  // MLP gate: z [M][rank], then hidden [M][gh]
 
   const uint32_t stages_s = smem_u32(stages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -323,31 +368,35 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
       }
       ec_bar();
       const bool arrived = *ec_flag != 0;
-      // u = alpha * gamma(z) * z for 4 tokens per float4 of z ([rank][32] fp32),
-      // eight independent loads in flight per lane
-      const int nv = p.rank * (Mp / 4);
-      for (int base = ew * 32 + lane; base < nv; base += kEcWarps * 32 * 8) {
-        float4 v[8];
+      if (p.gate == SPEAR_GATE_MLP) {
+        ec_u_mlp<Mp>(p, arrived, ew * 32 + lane, zs_mlp, zs_mlp + p.M * p.rank, uh, ul, us);
+      } else {
+        // u = alpha * gamma(z) * z for 4 tokens per float4 of z ([rank][32] fp32),
+        // eight independent loads in flight per lane
+        const int nv = p.rank * (Mp / 4);
+        for (int base = ew * 32 + lane; base < nv; base += kEcWarps * 32 * 8) {
+          float4 v[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int idx = base + q * kEcWarps * 32;
-          v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (arrived && idx < nv)
-            v[q] = __ldcg(reinterpret_cast<const float4*>(p.z + (idx / (Mp / 4)) * 32 + (idx % (Mp / 4)) * 4));
-        }
+          for (int q = 0; q < 8; ++q) {
+            const int idx = base + q * kEcWarps * 32;
+            v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (arrived && idx < nv)
+              v[q] = __ldcg(reinterpret_cast<const float4*>(p.z + (idx / (Mp / 4)) * 32 + (idx % (Mp / 4)) * 4));
+          }
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int idx = base + q * kEcWarps * 32;
-          if (idx < nv) {
-            const int j = idx / (Mp / 4), m0 = (idx % (Mp / 4)) * 4;
-            const float zz[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+          for (int q = 0; q < 8; ++q) {
+            const int idx = base + q * kEcWarps * 32;
+            if (idx < nv) {
+              const int j = idx / (Mp / 4), m0 = (idx % (Mp / 4)) * 4;
+              const float zz[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float uval = (m0 + e < p.M) ? p.alpha * gate_apply(zz[e], p.gate) : 0.f;
-              __nv_bfloat16 hi, lo;
-              split_bf16(uval, hi, lo);
-              uh[(m0 + e) * us + j] = hi;
-              ul[(m0 + e) * us + j] = lo;
+              for (int e = 0; e < 4; ++e) {
+                const float uval = (m0 + e < p.M) ? p.alpha * gate_apply(zz[e], p.gate) : 0.f;
+                __nv_bfloat16 hi, lo;
+                split_bf16(uval, hi, lo);
+                uh[(m0 + e) * us + j] = hi;
+                ul[(m0 + e) * us + j] = lo;
+              }
             }
           }
         }
@@ -695,12 +744,16 @@ spear_status_t spear_launch_decode(spear_linear_s* h, const __nv_bfloat16* x, __
   p.n_stages = (h->K + KC - 1) / KC;
   p.wait_ns = h->wait_ns;
   p.skip_arrive = h->skip_arrive;
+  p.gw1 = h->gate_w1;
+  p.gw2 = h->gate_w2;
+  p.gh = h->gate_hidden;
 
   const size_t red_bytes = (size_t)P * KW * 32 * 4 * MT * 4;
   const size_t u_bytes = ec ? (size_t)2 * Mp * (h->rank + 8) * 2 : 0;
+  const size_t mlp_bytes = h->gate_hidden > 0 ? (size_t)M * (h->rank + h->gate_hidden) * 4 : 0;
   const size_t pc_bytes = h->per_channel ? (size_t)P * 64 : 0;
   // barriers, alignment slack, per-channel words, u (hi and lo)
-  const size_t fixed = kBarrierBytes + 1024 + pc_bytes + u_bytes;
+  const size_t fixed = kBarrierBytes + 1024 + pc_bytes + u_bytes + mlp_bytes;
   const size_t budget = kSmemCap > fixed ? kSmemCap - fixed : 0;
   int NS = (int)(budget / p.stage_bytes);
   if (NS > kMaxStages) NS = kMaxStages;

@@ -177,6 +177,7 @@ extern "C" spear_status_t spear_linear_forward_decode_noalloc(const spear_linear
   if (d->K <= 0 || d->N <= 0 || d->K % 128 != 0 || d->N % 8 != 0) return SPEAR_ERR_INVALID_ARG;
   if (d->group_size != 0 && d->group_size != 128) return SPEAR_ERR_INVALID_ARG;
   if (d->rank < 0 || d->rank % 16 != 0 || (d->rank > 0 && (!d->A || !d->B))) return SPEAR_ERR_INVALID_ARG;
+  if (d->gate == SPEAR_GATE_MLP) return SPEAR_ERR_UNSUPPORTED;
   if (d->gate != SPEAR_GATE_SIGMOID && d->gate != SPEAR_GATE_ONE) return SPEAR_ERR_INVALID_ARG;
   // beyond the scratch array's capacity
   if (M > kNoallocMaxTokens || d->rank > kNoallocMaxRank) return SPEAR_ERR_INVALID_ARG;

@@ -63,6 +63,9 @@ struct GemmParams {
   uint32_t a_bytes, b_bytes, raw_bytes, stage_bytes;
   uint32_t tmem_cols;
   const __nv_bfloat16* bt;  // main kernel: compensator B rows [nt128 * 128][rank] (the K-tail's A operand)
+  const __nv_bfloat16* gw1;  // pre-kernel, SPEAR_GATE_MLP: W1 [gh][rank]
+  const __nv_bfloat16* gw2;  // pre-kernel, SPEAR_GATE_MLP: W2 [rank][gh]
+  int gh;
   int rank;
   float* zacc;          // pre-kernel: fp32 [M][rank] partial sums of z (zero between calls)
   unsigned* tile_done;  // pre-kernel: per 128-token tile, splits finished
@@ -344,7 +347,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence();
       }
       epilogue_bar();
-      if (last_split) {
+      if (last_split && p.gate == SPEAR_GATE_MLP) {
+        // Bottleneck-MLP gate: warp q stages z rows a0 + 32 q .. + 31 in the
+        // (now idle) stage memory, odd row strides keep the per-row reads on
+        // distinct banks; then lane l evaluates token row 32 q + l:
+        // t = relu(W1 z), u' = bf16(alpha sigmoid(W2 t) (.) z).
+        const int zst = p.TN + 1, tst = p.gh + 1;
+        float* zt = reinterpret_cast<float*>(stages);
+        float* tt = zt + 128 * zst;
+        for (int rr = 0; rr < 32; ++rr) {
+          const int m = a0 + 32 * q + rr;
+          for (int c = lane; c < p.TN; c += 32)
+            zt[(32 * q + rr) * zst + c] = m < p.a_rows ? __ldcg(p.zacc + (size_t)m * p.ld_out + c) : 0.f;
+        }
+        __syncwarp();
+        const int lr = 32 * q + lane, m = a0 + lr;
+        const float* zr = zt + lr * zst;
+        float* tr = tt + lr * tst;
+        for (int i = 0; i < p.gh; ++i) {
+          const __nv_bfloat16* w = p.gw1 + (size_t)i * p.TN;
+          float acc = 0.f;
+          for (int j = 0; j < p.TN; ++j) acc = fmaf(__bfloat162float(w[j]), zr[j], acc);
+          tr[i] = fmaxf(acc, 0.f);
+        }
+        if (m < p.a_rows) {
+          for (int j = 0; j < p.TN; ++j) {
+            const __nv_bfloat16* w = p.gw2 + (size_t)j * p.gh;
+            float acc = 0.f;
+            for (int i = 0; i < p.gh; ++i) acc = fmaf(__bfloat162float(w[i]), tr[i], acc);
+            p.out[(size_t)m * p.ld_out + j] = __float2bfloat16_rn(p.alpha * zr[j] * (1.0f / (1.0f + expf(-acc))));
+          }
+        }
+        __syncwarp();
+        for (int rr = 0; rr < 32; ++rr) {
+          const int mm = a0 + 32 * q + rr;
+          if (mm < p.a_rows)
+            for (int c = lane * 4; c < p.TN; c += 128)
+              *reinterpret_cast<float4*>(p.zacc + (size_t)mm * p.ld_out + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      } else if (last_split) {
         // Warp q finishes rows a0 + 32 q .. + 31, eight rows per round with all
         // loads in flight; lanes run along the row (coalesced), 4 columns each.
         for (int r0 = 0; r0 < 32; r0 += 8) {
@@ -474,6 +515,15 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
     p.raw_bytes = 0;
     p.stage_bytes = p.a_bytes + p.b_bytes;
     p.NS = stages_for(p.stage_bytes);
+    p.gw1 = h->gate_w1;
+    p.gw2 = h->gate_w2;
+    p.gh = h->gate_hidden;
+    if (h->gate_hidden > 0) {
+      // the MLP gate stages 128 z rows and 128 hidden rows in the stage area
+      const size_t need = (size_t)128 * (r + 1) * 4 + (size_t)128 * (h->gate_hidden + 1) * 4;
+      while ((size_t)p.NS * p.stage_bytes < need) ++p.NS;
+      if (p.NS > 8 || kBarrierBytes + 1024 + (size_t)p.NS * p.stage_bytes > 227 * 1024) return SPEAR_ERR_UNSUPPORTED;
+    }
     p.tmem_cols = tmem_cols_for(r);
     const size_t smem = kBarrierBytes + 1024 + (size_t)p.NS * p.stage_bytes;
     e = launch<false, 2>(p, dim3(mt, splits), smem, stream, mx, ma, none, none);

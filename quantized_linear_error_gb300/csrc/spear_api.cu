@@ -59,8 +59,8 @@ cudaError_t alloc(T** p, size_t bytes) {
 }
 
 void free_all(spear_linear_s* h) {
-  void* ptrs[] = {h->wq_dec, h->sz_dec, h->a_dec, h->b_dec, h->wq_pre, h->sz_pre,
-                  h->a_pre,  h->b_pre,  h->ws,    h->x_stage, h->y_stage};
+  void* ptrs[] = {h->wq_dec, h->sz_dec, h->a_dec,   h->b_dec,   h->wq_pre,  h->sz_pre, h->a_pre,
+                  h->b_pre,  h->ws,     h->x_stage, h->y_stage, h->gate_w1, h->gate_w2};
   for (void* p : ptrs)
     if (p) cudaFree(p);
 }
@@ -72,7 +72,13 @@ spear_status_t validate(const spear_linear_desc_t* d) {
   if (!d->qweight || !d->scales) return SPEAR_ERR_INVALID_ARG;
   if (d->rank < 0 || d->rank > 256 || d->rank % 16 != 0) return SPEAR_ERR_INVALID_ARG;
   if (d->rank > 0 && (!d->A || !d->B)) return SPEAR_ERR_INVALID_ARG;
-  if (d->gate != SPEAR_GATE_SIGMOID && d->gate != SPEAR_GATE_ONE) return SPEAR_ERR_INVALID_ARG;
+  if (d->gate != SPEAR_GATE_SIGMOID && d->gate != SPEAR_GATE_ONE && d->gate != SPEAR_GATE_MLP)
+    return SPEAR_ERR_INVALID_ARG;
+  if (d->gate == SPEAR_GATE_MLP) {
+    if (d->rank == 0 || d->gate_hidden < 1 || d->gate_hidden > kMaxGateHidden || !d->gate_w1 || !d->gate_w2 ||
+        !aligned16(d->gate_w1) || !aligned16(d->gate_w2))
+      return SPEAR_ERR_INVALID_ARG;
+  }
   if (d->max_tokens < 1) return SPEAR_ERR_INVALID_ARG;
   return SPEAR_OK;
 }
@@ -114,6 +120,7 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
   h->rank = d->rank;
   h->alpha = d->alpha;
   h->gate = d->gate;
+  h->gate_hidden = d->gate == SPEAR_GATE_MLP ? d->gate_hidden : 0;
   h->max_tokens = d->max_tokens;
   h->nt16 = (h->N + 15) / 16;
   h->nt128 = (h->N + 127) / 128;
@@ -142,6 +149,10 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
     A(alloc(&h->a_pre, r * K * 2));
     A(alloc(&h->b_pre, (size_t)h->nt128 * 128 * r * 2));
   }
+  if (h->gate_hidden > 0) {
+    A(alloc(&h->gate_w1, (size_t)h->gate_hidden * r * 2));
+    A(alloc(&h->gate_w2, (size_t)h->gate_hidden * r * 2));
+  }
   A(alloc(&h->ws, ws_bytes));
   A(alloc(&h->x_stage, mt * K * 2));
   A(alloc(&h->y_stage, mt * (size_t)h->N * 2));
@@ -161,6 +172,12 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
   spear_status_t st = SPEAR_OK;
   if (cudaMemsetAsync(h->ws, 0, ws_bytes, stream) != cudaSuccess) st = SPEAR_ERR_CUDA;
   if (st == SPEAR_OK) st = spear_build_layouts(h, d, stream);
+  if (st == SPEAR_OK && h->gate_hidden > 0) {
+    const size_t gb = (size_t)h->gate_hidden * r * 2;
+    if (cudaMemcpyAsync(h->gate_w1, d->gate_w1, gb, cudaMemcpyDeviceToDevice, stream) != cudaSuccess ||
+        cudaMemcpyAsync(h->gate_w2, d->gate_w2, gb, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+      st = SPEAR_ERR_CUDA;
+  }
   if (st == SPEAR_OK && cudaStreamSynchronize(stream) != cudaSuccess) st = SPEAR_ERR_CUDA;
   if (st != SPEAR_OK) {
     cudaGetLastError();

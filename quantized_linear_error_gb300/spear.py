@@ -18,7 +18,7 @@ LIB_PATH = PKG / "libspear_gb300.so"
 HEADER = PKG.parent / "include" / "spear.h"
 
 SPEAR_OK, SPEAR_ERR_INVALID_ARG, SPEAR_ERR_UNSUPPORTED, SPEAR_ERR_OOM, SPEAR_ERR_CUDA, SPEAR_ERR_TIMEOUT = range(6)
-SPEAR_GATE_SIGMOID, SPEAR_GATE_ONE = 0, 1
+SPEAR_GATE_SIGMOID, SPEAR_GATE_ONE, SPEAR_GATE_MLP = 0, 1, 2
 DECODE_MAX_TOKENS = 32
 
 
@@ -26,7 +26,8 @@ class spear_linear_desc_t(ctypes.Structure):
     _fields_ = [("K", c_int32), ("N", c_int32), ("group_size", c_int32),
                 ("qweight", c_void_p), ("scales", c_void_p), ("zeros", c_void_p),
                 ("rank", c_int32), ("A", c_void_p), ("B", c_void_p),
-                ("alpha", c_float), ("gate", c_int), ("max_tokens", c_int32)]
+                ("alpha", c_float), ("gate", c_int), ("max_tokens", c_int32),
+                ("gate_hidden", c_int32), ("gate_w1", c_void_p), ("gate_w2", c_void_p)]
 
 
 class SpearError(RuntimeError):
@@ -99,17 +100,20 @@ class SpearLinear:
     """Owner of one ``spear_linear_t``.
 
     ``qweight`` uint8 [N][K/2], ``scales`` bf16 [N][K/G], ``zeros`` uint8
-    [N][K/G] or None, ``A`` bf16 [r][K], ``B`` bf16 [N][r] (None when r = 0):
-    CUDA tensors in the layout ``spear_linear_desc_t`` documents. The library
-    copies them; the tensors may be freed after construction.
+    [N][K/G] or None, ``A`` bf16 [r][K], ``B`` bf16 [N][r] (None when r = 0),
+    and for the MLP gate ``W1`` bf16 [h][r], ``W2`` bf16 [r][h]: CUDA tensors
+    in the layout ``spear_linear_desc_t`` documents. The library copies them;
+    the tensors may be freed after construction.
     """
 
     def __init__(self, K, N, group_size, qweight, scales, zeros=None, A=None, B=None,
-                 alpha=1.0, gate=SPEAR_GATE_SIGMOID, max_tokens=32, stream=None):
+                 alpha=1.0, gate=SPEAR_GATE_SIGMOID, max_tokens=32, stream=None, W1=None, W2=None):
         L = load()
         rank = 0 if A is None else int(A.shape[0])
+        hidden = 0 if W1 is None else int(W1.shape[0])
         d = spear_linear_desc_t(int(K), int(N), int(group_size), _ptr(qweight), _ptr(scales), _ptr(zeros),
-                                rank, _ptr(A), _ptr(B), float(alpha), int(gate), int(max_tokens))
+                                rank, _ptr(A), _ptr(B), float(alpha), int(gate), int(max_tokens),
+                                hidden, _ptr(W1), _ptr(W2))
         h = c_void_p()
         _check(L.spear_linear_create(byref(d), _stream(stream), byref(h)), "spear_linear_create")
         self.h = h
@@ -172,7 +176,9 @@ def from_weights(w, device="cuda", max_tokens=32, alpha=None, gate=None, stream=
     z = dev(w.z, torch.uint8)
     A = dev(w.A.view(np.int16), torch.bfloat16) if sp.rank else None
     B = dev(w.B.view(np.int16), torch.bfloat16) if sp.rank else None
+    W1 = dev(w.W1.view(np.int16), torch.bfloat16) if getattr(w, "W1", None) is not None else None
+    W2 = dev(w.W2.view(np.int16), torch.bfloat16) if getattr(w, "W2", None) is not None else None
     lin = SpearLinear(sp.K, sp.N, sp.group_size, q, s, z, A, B,
                       sp.alpha if alpha is None else alpha, sp.gate if gate is None else gate,
-                      max_tokens, stream)
+                      max_tokens, stream, W1, W2)
     return lin

@@ -39,12 +39,12 @@ def codes_equal_zeros(w: wl.LinearWeights) -> wl.LinearWeights:
     sp = w.spec
     zfull = np.repeat(w.z, sp.G, axis=1).astype(np.uint8)           # [N][K]
     q = (zfull[:, 0::2] | (zfull[:, 1::2] << 4)).astype(np.uint8)
-    return wl.LinearWeights(sp, q, w.s, w.z, w.A, w.B, w.outliers)
+    return wl.LinearWeights(sp, q, w.s, w.z, w.A, w.B, w.outliers, w.W1, w.W2)
 
 
 def with_spec(w: wl.LinearWeights, **kw) -> wl.LinearWeights:
     import dataclasses
-    return wl.LinearWeights(dataclasses.replace(w.spec, **kw), w.q, w.s, w.z, w.A, w.B, w.outliers)
+    return wl.LinearWeights(dataclasses.replace(w.spec, **kw), w.q, w.s, w.z, w.A, w.B, w.outliers, w.W1, w.W2)
 
 
 def run(lin: spear.SpearLinear, x_bits: np.ndarray, path: str) -> np.ndarray:

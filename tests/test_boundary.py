@@ -30,7 +30,7 @@ def test_status_strings(L):
 
 def _desc(**kw):
     d = dict(K=256, N=64, group_size=128, qweight=16, scales=16, zeros=None, rank=0, A=None, B=None,
-             alpha=1.0, gate=0, max_tokens=4)
+             alpha=1.0, gate=0, max_tokens=4, gate_hidden=0, gate_w1=None, gate_w2=None)
     d.update(kw)
     return spear.spear_linear_desc_t(*[d[f] for f, _ in spear.spear_linear_desc_t._fields_])
 
@@ -55,3 +55,21 @@ def test_null_arguments(L):
     assert L.spear_linear_check(None, None) == spear.SPEAR_ERR_INVALID_ARG
     assert L.spear_linear_debug_set(None, 0, 0) == spear.SPEAR_ERR_INVALID_ARG
     assert L.spear_linear_destroy(None) == spear.SPEAR_OK
+
+
+_MLP = dict(gate=spear.SPEAR_GATE_MLP, rank=16, A=16, B=16, gate_hidden=8, gate_w1=16, gate_w2=32)
+
+
+@pytest.mark.parametrize("bad", [dict(gate_hidden=0), dict(gate_hidden=65), dict(gate_w1=None), dict(gate_w2=None),
+                                 dict(gate_w1=24), dict(rank=0, A=None, B=None)])
+def test_create_rejects_bad_mlp_gate(L, bad):
+    h = ctypes.c_void_p(1234)
+    d = _desc(**{**_MLP, **bad})
+    assert L.spear_linear_create(ctypes.byref(d), None, ctypes.byref(h)) == spear.SPEAR_ERR_INVALID_ARG
+    assert h.value is None
+
+
+def test_noalloc_entry_point_rejects_mlp_gate(L):
+    """The allocation-free decode has no MLP gate: refused before any device work."""
+    d = _desc(**_MLP)
+    assert L.spear_linear_forward_decode_noalloc(ctypes.byref(d), 16, 32, 1, None) == spear.SPEAR_ERR_UNSUPPORTED
