@@ -277,6 +277,43 @@ def measure_other_configs(args, stream, time_graphs, dev, hbm_peak, bf16_peak, w
                 "ec_off": res[False]}
     del ws, xs, ys
 
+    # the bottleneck-MLP gate (h = 16) on the config-2 decode layer set and the
+    # config-3 prefill MLP, next to the elementwise sigmoid gate
+    import dataclasses
+    res = {}
+    for gate in (wl.GATE_MLP, wl.GATE_SIGMOID):
+        specs = [dataclasses.replace(s2, gate=gate, gate_hidden=16) for s2 in wl.config_linears(2)]
+        hs = [spear.from_weights(wl.make_weights(s2, 10 + c), max_tokens=32, stream=stream)
+              for c in range(4) for s2 in specs]
+        xs = {(M, K): dev(wl.make_x(K, M, wl.outlier_channels(K, 0, "mlp"), 0, f"mlp/x{K}"))
+              for M in (1, 8, 32) for K in (4096, 11008)}
+        ys = {(M, N): torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for M in (1, 8, 32) for N in (4096, 11008)}
+        per = {}
+        for M in (1, 8, 32):
+            gs = [graph_of([lambda h=h, s2=s2: h.forward_decode(xs[(M, s2.K)], ys[(M, s2.N)], stream=stream)
+                            for h, s2 in zip(hs[c * 7:(c + 1) * 7], specs)]) for c in range(4)]
+            t = time_graphs(gs, steps, 3)
+            b = sum(s2.algorithmic_bytes(M) for s2 in specs)
+            per[str(M)] = {"us_per_layer_set": t * 1e3, "tokens_per_s": M / (t / 1e3), "hbm_gbs": b / (t / 1e3) / 1e9,
+                           "frac_hbm": b / (t / 1e3) / 1e9 / hbm_peak}
+            del gs
+        pspecs = [dataclasses.replace(s3, gate=gate, gate_hidden=16) for s3 in wl.config_linears(3)]
+        pl = [spear.from_weights(wl.make_weights(s3, 0), max_tokens=2048, stream=stream) for s3 in pspecs]
+        px = {K: dev(wl.make_x(K, 2048, wl.outlier_channels(K, 0, "mlp"), 0, f"mlp/p{K}")) for K in (4096, 14336)}
+        py = {N: torch.empty((2048, N), dtype=torch.bfloat16, device="cuda") for N in (4096, 14336)}
+        g = graph_of([lambda h=h, s3=s3: h.forward_prefill(px[s3.K], py[s3.N], stream=stream) for h, s3 in zip(pl, pspecs)])
+        t = time_graphs([g], max(10, steps // 4), 2)
+        fl = sum(s3.flops(2048) for s3 in pspecs)
+        per["prefill_2048"] = {"ms": t, "tflops": fl / (t / 1e3) / 1e12, "frac_bf16_peak": fl / (t / 1e3) / 1e12 / bf16_peak}
+        for h in hs + pl:
+            if h.check() != spear.SPEAR_OK:
+                raise SystemExit("gate comparison: device status error")
+            h.close()
+        del g
+        res["mlp_h16" if gate == wl.GATE_MLP else "sigmoid"] = per
+    out["gate_mlp"] = {"workload": "config-2 decode layer set (4 rotating copies) and config-3 prefill MLP at "
+                                   "M=2048, bottleneck-MLP gate h=16 vs elementwise sigmoid", **res}
+
     if with_config5:
         # config 5: 32 Llama-7B-shaped layers (7 projections each), EC r64 on four
         # seeded layers, one batch of 64 decode tokens + a prefill chunk C per linear

@@ -169,9 +169,31 @@ SPEAR_DEVINL void ec_prefetch(const DecodeParams& p, int ew, int lane) {
 
 // Bottleneck-MLP gate ("SPEAR", section 2.1A: gamma is a bottleneck MLP):
 // u = alpha * sigmoid(W2 relu(W1 z)) (.) z per token, by the four compensator
-// warps on z staged in shared memory (zs [M][rank], hidden ts [M][gh]); u is
-// written split into bf16 hi + lo like the elementwise gates (zero for tokens
-// M..Mp-1, and everywhere if z never arrived).
+// warps on z staged in shared memory (zs [M][rank], hidden ts [M][gh], gh a
+// multiple of 8); u is written split into bf16 hi + lo like the elementwise
+// gates (zero for tokens M..Mp-1, and everywhere if z never arrived).
+SPEAR_DEVINL float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+SPEAR_DEVINL float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// sum_k w[k] v[k] over n = 8 * n8 bf16 weights (16-byte rows) and fp32 values.
+SPEAR_DEVINL float dot_bf16_f32(const uint4* w, const float4* v, int n8) {
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 4
+  for (int k = 0; k < n8; ++k) {
+    const uint4 wv = __ldg(w + k);
+    const float4 v0 = v[2 * k], v1 = v[2 * k + 1];
+    a0 = fmaf(bf_lo(wv.x), v0.x, a0);
+    a1 = fmaf(bf_hi(wv.x), v0.y, a1);
+    a2 = fmaf(bf_lo(wv.y), v0.z, a2);
+    a3 = fmaf(bf_hi(wv.y), v0.w, a3);
+    a0 = fmaf(bf_lo(wv.z), v1.x, a0);
+    a1 = fmaf(bf_hi(wv.z), v1.y, a1);
+    a2 = fmaf(bf_lo(wv.w), v1.z, a2);
+    a3 = fmaf(bf_hi(wv.w), v1.w, a3);
+  }
+  return (a0 + a1) + (a2 + a3);
+}
+
 template <int Mp>
 SPEAR_DEVINL void ec_u_mlp(const DecodeParams& p, bool arrived, int tid, float* zs, float* ts, __nv_bfloat16* uh,
                            __nv_bfloat16* ul, int us) {
@@ -184,22 +206,17 @@ SPEAR_DEVINL void ec_u_mlp(const DecodeParams& p, bool arrived, int tid, float* 
   ec_bar();
   for (int i = tid; i < M * hh; i += kThr) {
     const int m = i / hh, c = i - m * hh;
-    const __nv_bfloat16* w = p.gw1 + (size_t)c * r;
-    const float* zm = zs + m * r;
-    float acc = 0.f;
-    for (int j = 0; j < r; ++j) acc = fmaf(__bfloat162float(w[j]), zm[j], acc);
-    ts[i] = fmaxf(acc, 0.f);
+    ts[i] = fmaxf(dot_bf16_f32(reinterpret_cast<const uint4*>(p.gw1 + (size_t)c * r),
+                               reinterpret_cast<const float4*>(zs + m * r), r / 8), 0.f);
   }
   ec_bar();
   for (int i = tid; i < Mp * r; i += kThr) {
     const int m = i / r, j = i - m * r;
     float uval = 0.f;
     if (arrived && m < M) {
-      const __nv_bfloat16* w = p.gw2 + (size_t)j * hh;
-      const float* tm = ts + m * hh;
-      float acc = 0.f;
-      for (int c = 0; c < hh; ++c) acc = fmaf(__bfloat162float(w[c]), tm[c], acc);
-      uval = p.alpha * zs[m * r + j] * (1.0f / (1.0f + expf(-acc)));
+      const float g = dot_bf16_f32(reinterpret_cast<const uint4*>(p.gw2 + (size_t)j * hh),
+                                   reinterpret_cast<const float4*>(ts + m * hh), hh / 8);
+      uval = p.alpha * zs[m * r + j] * (1.0f / (1.0f + expf(-g)));
     }
     __nv_bfloat16 hi, lo;
     split_bf16(uval, hi, lo);

@@ -72,9 +72,9 @@ struct spear_linear_s {
   float* z_pre = nullptr;            // [max_tokens][rank] fp32 (prefill projection)
   __nv_bfloat16* u_pre = nullptr;    // [max_tokens][rank] bf16 (prefill gated, alpha-scaled)
   unsigned* pre_done = nullptr;      // [ceil(max_tokens / 128)] split counters of the pre-kernel
-  int gate_hidden = 0;               // SPEAR_GATE_MLP: hidden width h
-  __nv_bfloat16* gate_w1 = nullptr;  // SPEAR_GATE_MLP: W1 [h][rank]
-  __nv_bfloat16* gate_w2 = nullptr;  // SPEAR_GATE_MLP: W2 [rank][h]
+  int gate_hidden = 0;               // SPEAR_GATE_MLP: hidden width h8 = h rounded up to 8
+  __nv_bfloat16* gate_w1 = nullptr;  // SPEAR_GATE_MLP: W1 [h8][rank], rows h.. zero
+  __nv_bfloat16* gate_w2 = nullptr;  // SPEAR_GATE_MLP: W2 [rank][h8], columns h.. zero
   size_t ws_bytes = 0;               // workspace size (zeroed at create and by a TIMEOUT check)
   __nv_bfloat16* x_stage = nullptr;  // host-path staging [max_tokens][K]
   __nv_bfloat16* y_stage = nullptr;  // host-path staging [max_tokens][N]

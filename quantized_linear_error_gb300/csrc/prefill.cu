@@ -81,6 +81,28 @@ SPEAR_DEVINL uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   return r;
 }
 
+SPEAR_DEVINL float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+SPEAR_DEVINL float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// sum_k w[k] v[k] over n = 8 * n8 bf16 weights (16-byte rows) and fp32 values.
+SPEAR_DEVINL float dot_bf16_f32(const uint4* w, const float4* v, int n8) {
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 4
+  for (int k = 0; k < n8; ++k) {
+    const uint4 wv = __ldg(w + k);
+    const float4 v0 = v[2 * k], v1 = v[2 * k + 1];
+    a0 = fmaf(bf_lo(wv.x), v0.x, a0);
+    a1 = fmaf(bf_hi(wv.x), v0.y, a1);
+    a2 = fmaf(bf_lo(wv.y), v0.z, a2);
+    a3 = fmaf(bf_hi(wv.y), v0.w, a3);
+    a0 = fmaf(bf_lo(wv.z), v1.x, a0);
+    a1 = fmaf(bf_hi(wv.z), v1.y, a1);
+    a2 = fmaf(bf_lo(wv.w), v1.z, a2);
+    a3 = fmaf(bf_hi(wv.w), v1.w, a3);
+  }
+  return (a0 + a1) + (a2 + a3);
+}
+
 SPEAR_DEVINL float gate_apply(float z, int gate) {
   return gate == SPEAR_GATE_ONE ? z : z * (1.0f / (1.0f + expf(-z)));
 }
@@ -349,10 +371,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       epilogue_bar();
       if (last_split && p.gate == SPEAR_GATE_MLP) {
         // Bottleneck-MLP gate: warp q stages z rows a0 + 32 q .. + 31 in the
-        // (now idle) stage memory, odd row strides keep the per-row reads on
-        // distinct banks; then lane l evaluates token row 32 q + l:
+        // (now idle) stage memory, rows padded by 4 floats so that 8 lanes'
+        // float4 reads of one column hit 8 distinct 16-byte bank groups; then
+        // lane l evaluates token row 32 q + l:
         // t = relu(W1 z), u' = bf16(alpha sigmoid(W2 t) (.) z).
-        const int zst = p.TN + 1, tst = p.gh + 1;
+        const int zst = p.TN + 4, tst = p.gh + 4;
         float* zt = reinterpret_cast<float*>(stages);
         float* tt = zt + 128 * zst;
         for (int rr = 0; rr < 32; ++rr) {
@@ -362,20 +385,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         const int lr = 32 * q + lane, m = a0 + lr;
-        const float* zr = zt + lr * zst;
+        const float4* zr = reinterpret_cast<const float4*>(zt + lr * zst);
         float* tr = tt + lr * tst;
-        for (int i = 0; i < p.gh; ++i) {
-          const __nv_bfloat16* w = p.gw1 + (size_t)i * p.TN;
-          float acc = 0.f;
-          for (int j = 0; j < p.TN; ++j) acc = fmaf(__bfloat162float(w[j]), zr[j], acc);
-          tr[i] = fmaxf(acc, 0.f);
-        }
+        for (int i = 0; i < p.gh; ++i)
+          tr[i] = fmaxf(dot_bf16_f32(reinterpret_cast<const uint4*>(p.gw1 + (size_t)i * p.TN), zr, p.TN / 8), 0.f);
         if (m < p.a_rows) {
-          for (int j = 0; j < p.TN; ++j) {
-            const __nv_bfloat16* w = p.gw2 + (size_t)j * p.gh;
-            float acc = 0.f;
-            for (int i = 0; i < p.gh; ++i) acc = fmaf(__bfloat162float(w[i]), tr[i], acc);
-            p.out[(size_t)m * p.ld_out + j] = __float2bfloat16_rn(p.alpha * zr[j] * (1.0f / (1.0f + expf(-acc))));
+          const float* zs = zt + lr * zst;
+          for (int j = 0; j < p.TN; j += 2) {
+            float g[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+              g[e] = dot_bf16_f32(reinterpret_cast<const uint4*>(p.gw2 + (size_t)(j + e) * p.gh),
+                                  reinterpret_cast<const float4*>(tr), p.gh / 8);
+            *reinterpret_cast<uint32_t*>(p.out + (size_t)m * p.ld_out + j) =
+                pack_bf16x2(p.alpha * zs[j] * (1.0f / (1.0f + expf(-g[0]))),
+                            p.alpha * zs[j + 1] * (1.0f / (1.0f + expf(-g[1]))));
           }
         }
         __syncwarp();
@@ -520,7 +544,7 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
     p.gh = h->gate_hidden;
     if (h->gate_hidden > 0) {
       // the MLP gate stages 128 z rows and 128 hidden rows in the stage area
-      const size_t need = (size_t)128 * (r + 1) * 4 + (size_t)128 * (h->gate_hidden + 1) * 4;
+      const size_t need = (size_t)128 * (r + 4) * 4 + (size_t)128 * (h->gate_hidden + 4) * 4;
       while ((size_t)p.NS * p.stage_bytes < need) ++p.NS;
       if (p.NS > 8 || kBarrierBytes + 1024 + (size_t)p.NS * p.stage_bytes > 227 * 1024) return SPEAR_ERR_UNSUPPORTED;
     }

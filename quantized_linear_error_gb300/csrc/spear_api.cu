@@ -120,7 +120,9 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
   h->rank = d->rank;
   h->alpha = d->alpha;
   h->gate = d->gate;
-  h->gate_hidden = d->gate == SPEAR_GATE_MLP ? d->gate_hidden : 0;
+  // zero-padded to a multiple of 8 hidden units (16-byte rows of W2): the
+  // extra units are relu(0) = 0 and meet zero columns of W2
+  h->gate_hidden = d->gate == SPEAR_GATE_MLP ? (d->gate_hidden + 7) / 8 * 8 : 0;
   h->max_tokens = d->max_tokens;
   h->nt16 = (h->N + 15) / 16;
   h->nt128 = (h->N + 127) / 128;
@@ -173,9 +175,12 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
   if (cudaMemsetAsync(h->ws, 0, ws_bytes, stream) != cudaSuccess) st = SPEAR_ERR_CUDA;
   if (st == SPEAR_OK) st = spear_build_layouts(h, d, stream);
   if (st == SPEAR_OK && h->gate_hidden > 0) {
-    const size_t gb = (size_t)h->gate_hidden * r * 2;
-    if (cudaMemcpyAsync(h->gate_w1, d->gate_w1, gb, cudaMemcpyDeviceToDevice, stream) != cudaSuccess ||
-        cudaMemcpyAsync(h->gate_w2, d->gate_w2, gb, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+    const size_t h8 = h->gate_hidden, hu = d->gate_hidden;
+    if (cudaMemsetAsync(h->gate_w1, 0, h8 * r * 2, stream) != cudaSuccess ||
+        cudaMemsetAsync(h->gate_w2, 0, h8 * r * 2, stream) != cudaSuccess ||
+        cudaMemcpyAsync(h->gate_w1, d->gate_w1, hu * r * 2, cudaMemcpyDeviceToDevice, stream) != cudaSuccess ||
+        cudaMemcpy2DAsync(h->gate_w2, h8 * 2, d->gate_w2, hu * 2, hu * 2, r, cudaMemcpyDeviceToDevice, stream) !=
+            cudaSuccess)
       st = SPEAR_ERR_CUDA;
   }
   if (st == SPEAR_OK && cudaStreamSynchronize(stream) != cudaSuccess) st = SPEAR_ERR_CUDA;
