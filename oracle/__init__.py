@@ -8,4 +8,6 @@ this package imports nothing from the library.
   through ctypes by :mod:`oracle.ref`.
 * ``brute.py`` -- pure-Python version for tiny shapes that materialises the
   per-token effective weight explicitly.
+* ``rtn.py`` -- numpy RTN 4-bit quantiser (fp32 decisions, as the GPU kernel
+  takes them) and the truncated-SVD initialisation of the compensator.
 """
