@@ -314,6 +314,8 @@ def measure_other_configs(args, stream, time_graphs, dev, hbm_peak, bf16_peak, w
     out["gate_mlp"] = {"workload": "config-2 decode layer set (4 rotating copies) and config-3 prefill MLP at "
                                    "M=2048, bottleneck-MLP gate h=16 vs elementwise sigmoid", **res}
 
+    out["rtn_svd"] = measure_rtn_svd(stream)
+
     if with_config5:
         # config 5: 32 Llama-7B-shaped layers (7 projections each), EC r64 on four
         # seeded layers, one batch of 64 decode tokens + a prefill chunk C per linear
@@ -344,6 +346,66 @@ def measure_other_configs(args, stream, time_graphs, dev, hbm_peak, bf16_peak, w
                                 f"{wl.ec_layer_indices(0)}, 64 decode tokens + prefill chunk C, one CUDA graph "
                                 "per step", "by_chunk": res}
     return out
+
+
+def measure_rtn_svd(stream):
+    """Quality stand-in for the compensator: synthetic fp32 weights (4096 x
+    4096, N(0, 0.02)) quantised by the library's RTN kernel (g128), the
+    compensator initialised by truncated SVD of the quantisation error (rank
+    64; plain, and weighted by the RMS of each input channel over 64
+    calibration tokens), relative output error ||y - W x|| / ||W x|| of the
+    decode kernel on 8 fresh tokens with the 1% x20 outlier channels, and the
+    share of the W4 error the compensator removes. Also the time of the RTN
+    kernel on this matrix."""
+    import numpy as np
+    import torch
+
+    from quantized_linear_error_gb300 import calibrate, spear
+    from quantized_linear_error_gb300 import workload as wl
+    K = N = 4096
+    M, rank = 8, 64
+    W = torch.from_numpy(wl.stream(0, "rtn/W").normal(0.0, 0.02, size=(N, K)).astype(np.float32)).cuda()
+    outl = wl.outlier_channels(K, 0, "rtn")
+    xcal = wl.bf16_bits_to_f32(wl.make_x(K, 64, outl, 1, "rtn/cal")).astype(np.float64)
+    act = torch.from_numpy(np.sqrt((xcal ** 2).mean(axis=0))).float().cuda()
+    xb = wl.make_x(K, M, outl, 2, "rtn/x")
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    y_fp = x.double() @ W.double().T
+
+    def err(q, s, z, A, B, gate):
+        lin = spear.SpearLinear(K, N, 128, q, s, z, A, B, alpha=1.0, gate=gate, max_tokens=M, stream=stream)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        lin.forward_decode(x, y, stream=stream)
+        stream.synchronize()
+        if lin.check() != spear.SPEAR_OK:
+            raise SystemExit("rtn/svd: device status error")
+        lin.close()
+        return float(torch.linalg.norm(y.double() - y_fp) / torch.linalg.norm(y_fp))
+
+    q, s, z, A0, B0, _ = calibrate.quantize_and_init(W, 128, rank, None, stream)
+    _, _, _, Aa, Ba, _ = calibrate.quantize_and_init(W, 128, rank, act, stream)
+    e_w4 = err(q, s, z, None, None, spear.SPEAR_GATE_ONE)
+    res = {"w4": e_w4}
+    for name, (A, B, gate) in {"ec_svd_static": (A0, B0, spear.SPEAR_GATE_ONE),
+                               "ec_act_svd_static": (Aa, Ba, spear.SPEAR_GATE_ONE),
+                               "ec_act_svd_sigmoid_gate_uncalibrated": (Aa, Ba, spear.SPEAR_GATE_SIGMOID)}.items():
+        e = err(q, s, z, A, B, gate)
+        res[name] = e
+        res[name + "_gap_recovered"] = 1.0 - e / e_w4
+    # RTN kernel time on the 4096 x 4096 matrix
+    for _ in range(3):
+        spear.quantize_rtn(W, 128, stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(20):
+        spear.quantize_rtn(W, 128, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 20
+    res["rtn_kernel_us"] = t * 1e3
+    res["rtn_kernel_gbs"] = (N * K * 4 + N * K // 2 + N * (K // 128) * 3) / (t / 1e3) / 1e9
+    return {"workload": "W ~ N(0, 0.02) 4096x4096 fp32 -> RTN g128 + rank-64 SVD init; relative output error "
+                        "of the decode kernel on 8 tokens with 1% x20 outlier channels", **res}
 
 
 # ------------------------------------------------------------------ GPU arm

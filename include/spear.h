@@ -171,6 +171,23 @@ spear_status_t spear_linear_debug_set(spear_linear_t h, int64_t wait_ns, int32_t
 spear_status_t spear_linear_forward_decode_noalloc(const spear_linear_desc_t* desc, const void* x, void* y,
                                                    int32_t M, cudaStream_t stream);
 
+/* Round-to-nearest 4-bit quantiser (offline; the "RTN" backend of "SPEAR",
+ * section 3.1, which the paper does not spell out: the usual asymmetric
+ * min/max form). Per group of G input channels (G = 128, or K for
+ * group_size 0) of each output row:
+ *   lo = min(0, min w), hi = max(0, max w), range = max(hi - lo, 1e-8),
+ *   s = bf16_RNE(range / 15), z = clamp(rint(-lo / s), 0, 15),
+ *   q = clamp(rint(w / s) + z, 0, 15),
+ * all in fp32 with IEEE division and round half to even.
+ *   w: device fp32 [N][K], 16-byte aligned; outputs in the layout
+ *   spear_linear_desc_t takes: qweight device uint8 [N][K/2] (2-byte
+ *   aligned), scales device bf16 [N][K/G], zeros device uint8 [N][K/G].
+ * K must be a multiple of 128. Enqueues one kernel on `stream`.
+ * Errors: INVALID_ARG (null or misaligned pointers, bad shape or group size),
+ * UNSUPPORTED (grid too large), CUDA. */
+spear_status_t spear_quantize_rtn(const float* w, int32_t N, int32_t K, int32_t group_size, uint8_t* qweight,
+                                  void* scales, uint8_t* zeros, cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* spear_status_string(spear_status_t s);
 

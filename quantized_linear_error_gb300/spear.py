@@ -66,6 +66,8 @@ def load(path: Path | None = None):
     L.spear_linear_debug_set.argtypes = [H, c_int64, c_int32]
     L.spear_linear_forward_decode_noalloc.argtypes = [POINTER(spear_linear_desc_t), c_void_p, c_void_p, c_int32, H]
     L.spear_linear_forward_decode_noalloc.restype = c_int
+    L.spear_quantize_rtn.argtypes = [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, H]
+    L.spear_quantize_rtn.restype = c_int
     L.spear_status_string.argtypes = [c_int]
     L.spear_status_string.restype = c_char_p
     for name in ("spear_linear_create", "spear_linear_forward_decode", "spear_linear_forward_prefill",
@@ -182,3 +184,19 @@ def from_weights(w, device="cuda", max_tokens=32, alpha=None, gate=None, stream=
                       sp.alpha if alpha is None else alpha, sp.gate if gate is None else gate,
                       max_tokens, stream, W1, W2)
     return lin
+
+
+def quantize_rtn(w, group_size=128, stream=None):
+    """RTN 4-bit quantisation of a CUDA fp32 tensor w [N][K] by the library's
+    kernel: returns (qweight uint8 [N][K/2], scales bf16 [N][K/G], zeros uint8
+    [N][K/G]) in the layout :class:`SpearLinear` takes."""
+    import torch
+    N, K = w.shape
+    G = K if group_size == 0 else group_size
+    w = w.contiguous()
+    q = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    s = torch.empty((N, K // G), dtype=torch.bfloat16, device=w.device)
+    z = torch.empty((N, K // G), dtype=torch.uint8, device=w.device)
+    _check(load().spear_quantize_rtn(_ptr(w), int(N), int(K), int(group_size), _ptr(q), _ptr(s), _ptr(z),
+                                     _stream(stream)), "spear_quantize_rtn")
+    return q, s, z
