@@ -345,7 +345,84 @@ def measure_other_configs(args, stream, time_graphs, dev, hbm_peak, bf16_peak, w
         out["5"] = {"workload": "32-layer Llama-7B-shaped stack (224 linears), INT4 g128, EC r64 on layers "
                                 f"{wl.ec_layer_indices(0)}, 64 decode tokens + prefill chunk C, one CUDA graph "
                                 "per step", "by_chunk": res}
+        del hs
+        out["scheduler"] = measure_scheduler(args, stream, time_graphs, dev, base)
     return out
+
+
+def measure_scheduler(args, stream, time_graphs, dev, base):
+    """The SLO-constrained chunk scheduler on the 32-layer stack: a latency
+    table measured on our kernels at EC densities {0, 1/8, 1/2, 1} (the first
+    round(32 d) layers of a seeded order carry a rank-64 compensator) and
+    64 decode tokens + chunks {256, 512, 1024, 2048}; then, at held-out
+    densities 1/4 and 3/4 and ITL targets 16 and 22 ms, the chunk it picks
+    (multiples of 64) and the measured time of that step, next to static
+    chunks of 512 and 1024."""
+    import dataclasses
+
+    import torch
+
+    from quantized_linear_error_gb300 import spear
+    from quantized_linear_error_gb300 import workload as wl
+
+    n_dec, mmax = 64, 64 + 2048
+    order = [int(i) for i in wl.stream(0, "sched/ec_order").permutation(32)]
+    layer_specs = wl.llama7b_layer("c5/", rank=64)
+    names = [sp.name.split("/")[-1] for sp in layer_specs]
+    ec_h = [[spear.from_weights(base[n], max_tokens=mmax, stream=stream) for n in names] for _ in range(32)]
+    plain_h = [[spear.from_weights(wl.LinearWeights(dataclasses.replace(base[n].spec, rank=0), base[n].q,
+                                                    base[n].s, base[n].z, None, None, base[n].outliers),
+                                   max_tokens=mmax, stream=stream) for n in names] for _ in range(32)]
+    xs = {K: dev(wl.make_x(K, mmax, base["q" if K == 4096 else "down"].outliers, 0, f"sched/x{K}"))
+          for K in (4096, 11008)}
+    ys = {N: torch.empty((mmax, N), dtype=torch.bfloat16, device="cuda") for N in (4096, 11008)}
+
+    def step_ms(density, M):
+        ec_layers = set(order[:round(32 * density)])
+        calls = []
+        for layer in range(32):
+            hs = ec_h[layer] if layer in ec_layers else plain_h[layer]
+            for h, sp in zip(hs, layer_specs):
+                calls.append(lambda h=h, sp=sp: h.forward_prefill(xs[sp.K][:M], ys[sp.N][:M], stream=stream))
+        with torch.cuda.stream(stream):
+            for f in calls:
+                f()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for f in calls:
+                f()
+        t = time_graphs([g], max(3, args.steps // 400), 1)
+        del g
+        return t
+
+    dens = [0.0, 0.125, 0.5, 1.0]
+    toks = [n_dec + c for c in (256, 512, 1024, 2048)]
+    table = [[step_ms(d, m) for m in toks] for d in dens]
+    sched = spear.ChunkScheduler(dens, toks, table)
+    cands = list(range(64, 2049, 64))
+    checks = []
+    for d in (0.25, 0.75):
+        for itl in (16.0, 22.0):
+            c = sched.pick_chunk(n_dec, d, itl, cands)
+            row = {"density": d, "itl_ms": itl, "picked_chunk": c,
+                   "predicted_ms": sched.predict(n_dec + c, d) if c else None,
+                   "measured_ms": step_ms(d, n_dec + c) if c else None}
+            row["meets_slo"] = row["measured_ms"] is not None and row["measured_ms"] <= itl
+            for sc in (512, 1024):
+                t = step_ms(d, n_dec + sc)
+                row[f"static_{sc}_ms"] = t
+                row[f"static_{sc}_meets_slo"] = t <= itl
+            checks.append(row)
+    for hs in ec_h + plain_h:
+        for h in hs:
+            if h.check() != spear.SPEAR_OK:
+                raise SystemExit("scheduler: device status error")
+            h.close()
+    sched.close()
+    return {"workload": "32-layer Llama-7B-shaped stack through the prefill path, 64 decode tokens + chunk; "
+                        "latency table measured on these kernels", "table_densities": dens, "table_tokens": toks,
+            "table_ms": table, "checks": checks}
 
 
 def measure_rtn_svd(stream):

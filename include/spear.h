@@ -188,6 +188,35 @@ spear_status_t spear_linear_forward_decode_noalloc(const spear_linear_desc_t* de
 spear_status_t spear_quantize_rtn(const float* w, int32_t N, int32_t K, int32_t group_size, uint8_t* qweight,
                                   void* scales, uint8_t* zeros, cudaStream_t stream);
 
+/* SLO-constrained, compensator-aware chunk scheduler ("SPEAR", section 2.2C:
+ * a latency-aware scheduler driven by precomputed kernel-latency lookup tables
+ * picks the largest prefill chunk that meets an inter-token-latency target,
+ * adapting to the compensator density). Host only; no device work.
+ * The table holds measured times of one whole serving step: ms[i * n_m + j]
+ * for density densities[i] (share of layers with a compensator, strictly
+ * ascending in [0, 1]) and tokens[j] tokens in the step (strictly ascending,
+ * >= 1). Prediction is piecewise linear in the token count (extrapolated
+ * linearly past the table's ends) and linear in the density between rows
+ * (clamped to the first and last rows). */
+typedef struct spear_sched_s* spear_sched_t;
+
+/* Copies the table. Errors: INVALID_ARG (null pointers, empty or unsorted
+ * axes, densities outside [0, 1], negative or NaN times), OOM. */
+spear_status_t spear_sched_create(const double* densities, int32_t n_d, const int32_t* tokens, int32_t n_m,
+                                  const double* ms, spear_sched_t* out);
+
+/* Predicted step time (ms) for M tokens at the given density; -1 for a null
+ * handle or M < 0. */
+double spear_sched_predict(spear_sched_t s, int32_t M, double density);
+
+/* *chunk_out = the largest candidate chunk c (candidates in any order, >= 0)
+ * with predict(n_decode + c, density) <= itl_ms, or 0 if none fits. */
+spear_status_t spear_sched_pick_chunk(spear_sched_t s, int32_t n_decode, double density, double itl_ms,
+                                      const int32_t* candidates, int32_t n_c, int32_t* chunk_out);
+
+/* Frees the scheduler; NULL is accepted. */
+spear_status_t spear_sched_destroy(spear_sched_t s);
+
 /* Human-readable name of a status code (static storage). */
 const char* spear_status_string(spear_status_t s);
 

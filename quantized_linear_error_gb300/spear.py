@@ -10,7 +10,7 @@ from __future__ import annotations
 
 import ctypes
 import re
-from ctypes import POINTER, byref, c_char_p, c_float, c_int, c_int32, c_int64, c_void_p
+from ctypes import POINTER, byref, c_char_p, c_double, c_float, c_int, c_int32, c_int64, c_void_p
 from pathlib import Path
 
 PKG = Path(__file__).resolve().parent
@@ -66,6 +66,14 @@ def load(path: Path | None = None):
     L.spear_linear_debug_set.argtypes = [H, c_int64, c_int32]
     L.spear_linear_forward_decode_noalloc.argtypes = [POINTER(spear_linear_desc_t), c_void_p, c_void_p, c_int32, H]
     L.spear_linear_forward_decode_noalloc.restype = c_int
+    L.spear_sched_create.argtypes = [c_void_p, c_int32, c_void_p, c_int32, c_void_p, POINTER(c_void_p)]
+    L.spear_sched_create.restype = c_int
+    L.spear_sched_predict.argtypes = [H, c_int32, c_double]
+    L.spear_sched_predict.restype = c_double
+    L.spear_sched_pick_chunk.argtypes = [H, c_int32, c_double, c_double, c_void_p, c_int32, POINTER(c_int32)]
+    L.spear_sched_pick_chunk.restype = c_int
+    L.spear_sched_destroy.argtypes = [H]
+    L.spear_sched_destroy.restype = c_int
     L.spear_quantize_rtn.argtypes = [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, H]
     L.spear_quantize_rtn.restype = c_int
     L.spear_status_string.argtypes = [c_int]
@@ -200,3 +208,42 @@ def quantize_rtn(w, group_size=128, stream=None):
     _check(load().spear_quantize_rtn(_ptr(w), int(N), int(K), int(group_size), _ptr(q), _ptr(s), _ptr(z),
                                      _stream(stream)), "spear_quantize_rtn")
     return q, s, z
+
+
+class ChunkScheduler:
+    """Owner of one ``spear_sched_t`` (host only): a latency table of measured
+    step times over (compensator density, tokens per step)."""
+
+    def __init__(self, densities, tokens, ms):
+        import numpy as np
+        self._d = np.ascontiguousarray(densities, dtype=np.float64)
+        self._t = np.ascontiguousarray(tokens, dtype=np.int32)
+        self._ms = np.ascontiguousarray(ms, dtype=np.float64)
+        if self._ms.shape != (self._d.size, self._t.size):
+            raise ValueError("ms must be [len(densities)][len(tokens)]")
+        h = c_void_p()
+        _check(load().spear_sched_create(self._d.ctypes.data, self._d.size, self._t.ctypes.data, self._t.size,
+                                         self._ms.ctypes.data, byref(h)), "spear_sched_create")
+        self.h = h
+
+    def predict(self, M: int, density: float) -> float:
+        return load().spear_sched_predict(self.h, int(M), float(density))
+
+    def pick_chunk(self, n_decode: int, density: float, itl_ms: float, candidates) -> int:
+        import numpy as np
+        c = np.ascontiguousarray(candidates, dtype=np.int32)
+        out = c_int32()
+        _check(load().spear_sched_pick_chunk(self.h, int(n_decode), float(density), float(itl_ms), c.ctypes.data,
+                                             c.size, byref(out)), "spear_sched_pick_chunk")
+        return int(out.value)
+
+    def close(self):
+        if getattr(self, "h", None) and self.h.value:
+            load().spear_sched_destroy(self.h)
+            self.h = c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
