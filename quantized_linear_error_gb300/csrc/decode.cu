@@ -388,33 +388,25 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
       if (p.gate == SPEAR_GATE_MLP) {
         ec_u_mlp<Mp>(p, arrived, ew * 32 + lane, zs_mlp, zs_mlp + p.M * p.rank, uh, ul, us);
       } else {
-        // u = alpha * gamma(z) * z for 4 tokens per float4 of z ([rank][32] fp32),
-        // eight independent loads in flight per lane
+        // u = alpha * gamma(z) * z for 4 tokens per float4 of z ([rank][32] fp32).
+        // Kept compact (two loads in flight, fast exp and division for the
+        // sigmoid, ~1e-6 relative): this code runs once per launch, and a
+        // large unrolled body here costs the consumer warps instruction fetch.
         const int nv = p.rank * (Mp / 4);
-        for (int base = ew * 32 + lane; base < nv; base += kEcWarps * 32 * 8) {
-          float4 v[8];
+#pragma unroll 2
+        for (int idx = ew * 32 + lane; idx < nv; idx += kEcWarps * 32) {
+          const int j = idx / (Mp / 4), m0 = (idx % (Mp / 4)) * 4;
+          const float4 v = arrived ? __ldcg(reinterpret_cast<const float4*>(p.z + j * 32 + m0))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float zz[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int idx = base + q * kEcWarps * 32;
-            v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (arrived && idx < nv)
-              v[q] = __ldcg(reinterpret_cast<const float4*>(p.z + (idx / (Mp / 4)) * 32 + (idx % (Mp / 4)) * 4));
-          }
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int idx = base + q * kEcWarps * 32;
-            if (idx < nv) {
-              const int j = idx / (Mp / 4), m0 = (idx % (Mp / 4)) * 4;
-              const float zz[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float uval = (m0 + e < p.M) ? p.alpha * gate_apply(zz[e], p.gate) : 0.f;
-                __nv_bfloat16 hi, lo;
-                split_bf16(uval, hi, lo);
-                uh[(m0 + e) * us + j] = hi;
-                ul[(m0 + e) * us + j] = lo;
-              }
-            }
+          for (int e = 0; e < 4; ++e) {
+            const float g = p.gate == SPEAR_GATE_ONE ? 1.0f : __fdividef(1.0f, 1.0f + __expf(-zz[e]));
+            const float uval = (m0 + e < p.M) ? p.alpha * zz[e] * g : 0.f;
+            __nv_bfloat16 hi, lo;
+            split_bf16(uval, hi, lo);
+            uh[(m0 + e) * us + j] = hi;
+            ul[(m0 + e) * us + j] = lo;
           }
         }
       }
