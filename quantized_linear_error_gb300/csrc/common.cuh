@@ -197,6 +197,13 @@ SPEAR_DEVINL uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
 // bf16 bits of (128 + z) in both halves.
 SPEAR_DEVINL uint32_t biased_zero_x2(uint32_t zbits16) { return zbits16 | (zbits16 << 16); }
 
+// The same pair from a scale/zero word (bits 16..31 = bf16(128 + z)): one byte permute.
+SPEAR_DEVINL uint32_t biased_zero_x2_of_word(uint32_t w) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %1, 0x3232;" : "=r"(r) : "r"(w));
+  return r;
+}
+
 SPEAR_DEVINL float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
 
 SPEAR_DEVINL uint32_t pack_bf16x2(float lo, float hi) {

@@ -449,6 +449,11 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
   uint32_t swz[8];
 #pragma unroll
   for (int c = 0; c < 8; ++c) swz[c] = (uint32_t)((((c + mkh) & 7) ^ mrow) << 4);
+  // M <= 8: one ldmatrix.x4 brings two k16 steps; lane l addresses token l % 8,
+  // chunk c0 + l / 8 of the k64 block (c0 = 0 for steps 0-1, 4 for steps 2-3)
+  const uint32_t lane_off1 = mrow * 128;
+  const uint32_t swz1[2] = {(uint32_t)((((lane >> 3) & 7) ^ mrow) << 4),
+                            (uint32_t)((((4 + (lane >> 3)) & 7) ^ mrow) << 4)};
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   float acc[T][MT][4];
@@ -513,8 +518,8 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
           if constexpr (!PC) {
             const uint32_t w0 = lds32(szs + ((tl * (kcw_r / 128) + uin) * 16 + g) * 4);
             const uint32_t w1 = lds32(szs + ((tl * (kcw_r / 128) + uin) * 16 + g + 8) * 4);
-            zz[t][0] = biased_zero_x2(w0 >> 16);
-            zz[t][1] = biased_zero_x2(w1 >> 16);
+            zz[t][0] = biased_zero_x2_of_word(w0);
+            zz[t][1] = biased_zero_x2_of_word(w1);
             sc[t][0] = bf16_bits_to_float(w0 & 0xFFFF);
             sc[t][1] = bf16_bits_to_float(w1 & 0xFFFF);
           } else {
@@ -524,13 +529,21 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
         }
       }
       uint32_t lane_base[8];
-      const uint32_t ub = st + (uint32_t)(2 * u) * (Mp * 128) + lane_off;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) lane_base[c] = ub + swz[c];
-      // M <= 8: all eight k16 steps' x fragments at once (16 registers);
-      // wider M: per k16 step
+      // M <= 8: all eight k16 steps' x fragments at once (16 registers, four
+      // ldmatrix.x4); wider M: per k16 step
       uint32_t bb[MT == 1 ? 8 : 1][MT][2];
-      if constexpr (MT == 1) load_unit_x_frags<MT>(lane_base, reinterpret_cast<uint32_t(&)[8][MT][2]>(bb));
+      if constexpr (MT == 1) {
+        const uint32_t ub1 = st + (uint32_t)(2 * u) * (Mp * 128) + lane_off1;
+        const uint32_t a0 = ub1 + swz1[0], a1 = ub1 + swz1[1];
+        ldsm_x4(bb[0][0][0], bb[0][0][1], bb[1][0][0], bb[1][0][1], a0);
+        ldsm_x4(bb[2][0][0], bb[2][0][1], bb[3][0][0], bb[3][0][1], a1);
+        ldsm_x4(bb[4][0][0], bb[4][0][1], bb[5][0][0], bb[5][0][1], a0 + Mp * 128);
+        ldsm_x4(bb[6][0][0], bb[6][0][1], bb[7][0][0], bb[7][0][1], a1 + Mp * 128);
+      } else {
+        const uint32_t ub = st + (uint32_t)(2 * u) * (Mp * 128) + lane_off;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) lane_base[c] = ub + swz[c];
+      }
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         uint32_t bk[MT][2];
