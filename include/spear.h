@@ -145,6 +145,13 @@ spear_status_t spear_linear_check(spear_linear_t h, cudaStream_t stream);
  * latches TIMEOUT). */
 spear_status_t spear_linear_debug_set(spear_linear_t h, int64_t wait_ns, int32_t skip_arrive);
 
+/* Choose the decode kernel of the handle: 0 automatic (the default), 1 the
+ * warp-MMA kernel (mma.sync, dequantised fragments in registers), 2 the
+ * tensor-core kernel (tcgen05: weights streamed by bulk copies, dequantised
+ * into tensor memory, compensator up-projection as an extra K block). Both
+ * compute the same y up to summation order. Errors: INVALID_ARG. */
+spear_status_t spear_linear_select_decode(spear_linear_t h, int32_t kernel);
+
 /* Decode forward that allocates nothing (the paper has no counterpart; this is
  * a deployment convenience). For callers that cannot call cudaMalloc at all,
  * for instance a process whose device memory is entirely reserved up front by

@@ -68,29 +68,13 @@ SPEAR_DEVINL bool mbar_try_wait(uint64_t* bar, unsigned parity) {
   return ok != 0;
 }
 
-// try_wait with a suspend-time hint: the thread sleeps until the phase
-// completes or about `hint_ns` have passed, instead of polling.
-SPEAR_DEVINL bool mbar_try_wait_sleep(uint64_t* bar, unsigned parity, uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-
 // Wait for phase `parity` of `bar` to complete; gives up after `limit_ns`
-// (returns false) so that a broken pipeline can never hang the GPU. Waiting
-// threads sleep in the barrier (a few polls per millisecond at most) rather
-// than spinning, so they take no issue slots from the working warps.
+// (returns false) so that a broken pipeline can never hang the GPU.
 SPEAR_DEVINL bool mbar_wait_bounded(uint64_t* bar, unsigned parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
-    if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (globaltimer() - t0 > limit_ns) return false;
   }
 }

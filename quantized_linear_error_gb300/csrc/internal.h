@@ -76,6 +76,9 @@ struct spear_linear_s {
   __nv_bfloat16* gate_w1 = nullptr;  // SPEAR_GATE_MLP: W1 [h8][rank], rows h.. zero
   __nv_bfloat16* gate_w2 = nullptr;  // SPEAR_GATE_MLP: W2 [rank][h8], columns h.. zero
   size_t ws_bytes = 0;               // workspace size (zeroed at create and by a TIMEOUT check)
+  float* y32_tc = nullptr;           // tensor-core decode: [sm_count + 2 nt128][128][32] fp32 partials
+  unsigned* tile_cnt_tc = nullptr;   // tensor-core decode: [nt128] contributors done per tile
+  int decode_kernel = 0;             // 0 automatic, 1 warp MMA, 2 tensor cores (tcgen05)
   __nv_bfloat16* x_stage = nullptr;  // host-path staging [max_tokens][K]
   __nv_bfloat16* y_stage = nullptr;  // host-path staging [max_tokens][N]
 
@@ -157,5 +160,7 @@ spear_status_t spear_launch_decode(spear_linear_s* h, const __nv_bfloat16* x, __
                                    cudaStream_t stream);
 spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,
                                     cudaStream_t stream);
+spear_status_t spear_launch_decode_tc(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,
+                                      cudaStream_t stream);
 spear_status_t spear_build_layouts(spear_linear_s* h, const spear_linear_desc_t* d, cudaStream_t stream);
 spear_status_t spear_launch_dequant(spear_linear_s* h, int path, __nv_bfloat16* out, cudaStream_t stream);

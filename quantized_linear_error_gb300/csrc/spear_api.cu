@@ -135,7 +135,9 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
 
   const size_t K = h->K, r = h->rank, mt = h->max_tokens;
   const size_t pre_tiles = (mt + 127) / 128;
-  const size_t ws_bytes = sizeof(spear::SyncWords) + kZDecFloats * 4 + mt * r * 4 + mt * r * 2 + pre_tiles * 4 + 256;
+  const size_t y32_tc_floats = ((size_t)h->sm_count + 2 * (size_t)h->nt128) * 128 * 32;
+  const size_t ws_bytes = sizeof(spear::SyncWords) + kZDecFloats * 4 + mt * r * 4 + mt * r * 2 + pre_tiles * 4 +
+                          256 + y32_tc_floats * 4 + (size_t)h->nt128 * 4 + 256;
   h->ws_bytes = ws_bytes;
   cudaError_t e = cudaSuccess;
   auto A = [&](cudaError_t x) {
@@ -170,6 +172,11 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
   h->z_pre = h->z_dec + kZDecFloats;
   h->u_pre = reinterpret_cast<__nv_bfloat16*>(h->z_pre + mt * r);
   h->pre_done = reinterpret_cast<unsigned*>(h->u_pre + mt * r);
+  {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(h->pre_done + pre_tiles);
+    h->y32_tc = reinterpret_cast<float*>((a + 255) & ~uintptr_t(255));
+    h->tile_cnt_tc = reinterpret_cast<unsigned*>(h->y32_tc + y32_tc_floats);
+  }
 
   spear_status_t st = SPEAR_OK;
   if (cudaMemsetAsync(h->ws, 0, ws_bytes, stream) != cudaSuccess) st = SPEAR_ERR_CUDA;
@@ -199,7 +206,10 @@ spear_status_t spear_linear_forward_decode(spear_linear_t h, const void* x, void
   spear_status_t v = check_io(h, x, y, M);
   if (v != SPEAR_OK || M == 0) return v;
   if (M > kDecodeMaxTokens) return SPEAR_ERR_INVALID_ARG;
-  return spear_launch_decode(h, static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), M, stream);
+  const auto* xb = static_cast<const __nv_bfloat16*>(x);
+  auto* yb = static_cast<__nv_bfloat16*>(y);
+  if (h->decode_kernel == 2) return spear_launch_decode_tc(h, xb, yb, M, stream);
+  return spear_launch_decode(h, xb, yb, M, stream);
 }
 
 spear_status_t spear_linear_forward_prefill(spear_linear_t h, const void* x, void* y, int32_t M,
@@ -260,6 +270,12 @@ spear_status_t spear_linear_debug_set(spear_linear_t h, int64_t wait_ns, int32_t
   if (!h || wait_ns < 0) return SPEAR_ERR_INVALID_ARG;
   h->wait_ns = wait_ns == 0 ? 100000000ull : (uint64_t)wait_ns;
   h->skip_arrive = skip_arrive != 0;
+  return SPEAR_OK;
+}
+
+spear_status_t spear_linear_select_decode(spear_linear_t h, int32_t kernel) {
+  if (!h || kernel < 0 || kernel > 2) return SPEAR_ERR_INVALID_ARG;
+  h->decode_kernel = kernel;
   return SPEAR_OK;
 }
 
