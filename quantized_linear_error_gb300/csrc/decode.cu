@@ -485,8 +485,112 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
     }
   }
 
+  // One 128-channel unit of this warp's tiles: wa[t] is this lane's first 16
+  // bytes of tile t's codes (the unit's second k64 block is 512 bytes on), sa[t]
+  // the scale/zero word of row g (row g + 8 is 32 bytes on), xa the lane's
+  // ldmatrix row address of the unit's first k64 block of x, unswizzled.
+  auto unit = [&](const uint32_t (&wa)[T], const uint32_t (&sa)[T], uint32_t xa) {
+    uint4 wv[T][2];
+    uint32_t zz[T][2];
+    float sc[T][2];
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      const int tl = pw_i * T + t;
+      if (t == 0 || tl < Pc) {
+        wv[t][0] = lds128(wa[t]);
+        wv[t][1] = lds128(wa[t] + 512);
+        if constexpr (!PC) {
+          const uint32_t w0 = lds32(sa[t]);
+          const uint32_t w1 = lds32(sa[t] + 32);
+          zz[t][0] = biased_zero_x2_of_word(w0);
+          zz[t][1] = biased_zero_x2_of_word(w1);
+          sc[t][0] = bf16_bits_to_float(w0 & 0xFFFF);
+          sc[t][1] = bf16_bits_to_float(w1 & 0xFFFF);
+        } else {
+          zz[t][0] = zzpc[t][0];
+          zz[t][1] = zzpc[t][1];
+        }
+      }
+    }
+    uint32_t lane_base[8];
+    // M <= 8: all eight k16 steps' x fragments at once (16 registers, four
+    // ldmatrix.x4); wider M: per k16 step
+    uint32_t bb[MT == 1 ? 8 : 1][MT][2];
+    if constexpr (MT == 1) {
+      const uint32_t a0 = xa + swz1[0], a1 = xa + swz1[1];
+      ldsm_x4(bb[0][0][0], bb[0][0][1], bb[1][0][0], bb[1][0][1], a0);
+      ldsm_x4(bb[2][0][0], bb[2][0][1], bb[3][0][0], bb[3][0][1], a1);
+      ldsm_x4(bb[4][0][0], bb[4][0][1], bb[5][0][0], bb[5][0][1], a0 + Mp * 128);
+      ldsm_x4(bb[6][0][0], bb[6][0][1], bb[7][0][0], bb[7][0][1], a1 + Mp * 128);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) lane_base[c] = xa + swz[c];
+    }
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t bk[MT][2];
+      if constexpr (MT > 1) load_kk_x_frags<MT>(lane_base, kk, bk);
+      const uint32_t(&b)[MT][2] = MT == 1 ? bb[MT == 1 ? kk : 0] : bk;
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        const int tl = pw_i * T + t;
+        if (t == 0 || tl < Pc) {
+          const uint32_t w = word_of(wv[t][kk >> 2], kk & 3);
+          const uint32_t a[4] = {bf16x2_sub(int4_pair_to_bf16x2_biased(w), zz[t][0]),
+                                 bf16x2_sub(int4_pair_to_bf16x2_biased(w >> 4), zz[t][1]),
+                                 bf16x2_sub(int4_pair_to_bf16x2_biased(w >> 8), zz[t][0]),
+                                 bf16x2_sub(int4_pair_to_bf16x2_biased(w >> 12), zz[t][1])};
+#pragma unroll
+          for (int n = 0; n < MT; ++n) {
+            // grouped scales restart the chains every group (folded below)
+            if (!PC && kk < NC)
+              mma_bf16_16816_zero(accg[t][kk % NC][n], a, b[n][0], b[n][1]);
+            else
+              mma_bf16_16816(accg[t][kk % NC][n], a, b[n][0], b[n][1]);
+          }
+        }
+      }
+    }
+    if constexpr (!PC) {
+      // grouped scales: fold the chains into acc once per group
+#pragma unroll
+      for (int t = 0; t < T; ++t)
+#pragma unroll
+        for (int n = 0; n < MT; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float v = accg[t][0][n][e];
+#pragma unroll
+            for (int c = 1; c < NC; ++c) v += accg[t][c][n][e];
+            acc[t][n][e] = fmaf(sc[t][e >> 1], v, acc[t][n][e]);
+          }
+    }
+  };
+
   // warps without a tile skip the stages (they are not counted on `empty`)
   const bool busy = pw_i * T < Pc;
+  const uint32_t x_lane = MT == 1 ? lane_off1 : lane_off;
+  // Full stages (KC channels) whose KC / 128 units split evenly over the K
+  // warps: each warp takes the same NU <= 2 units of every stage (units
+  // kw_i + j KW, j < NU), at offsets from the stage base fixed here.
+  const int units_full = KC / 128;
+  const int NU = units_full % p.KW == 0 && units_full / p.KW <= 2 ? units_full / p.KW : 0;
+  const int n_fast = NU > 0 ? K / KC : 0;  // stages taken by the fixed-offset path
+  uint32_t wo[2][T], so[2][T], xo[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int u = kw_i + j * p.KW;
+    const int sr = u >> 1, uin = u & 1;
+    const uint32_t run = p.bytes_x + (uint32_t)sr * (uint32_t)run_full;
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      const int tl = pw_i * T + t;
+      wo[j][t] = run + (uint32_t)((tl * (kDecodeRun / 64) + 2 * uin) * 32 + lane) * 16;
+      so[j][t] = run + (uint32_t)(Pc * (kDecodeRun / 64) * 512) +
+                 (uint32_t)((tl * (kDecodeRun / 128) + uin) * 16 + g) * 4;
+    }
+    xo[j] = (uint32_t)(2 * u) * (Mp * 128) + x_lane;
+  }
   for (int i = 0; i < p.n_stages && ok && busy; ++i) {
     const int slot = i % p.NS;
     if (!mbar_wait_bounded(&full[slot], (i / p.NS) & 1, p.wait_ns)) {
@@ -494,94 +598,40 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
       break;
     }
     const uint32_t st = stages_s + (uint32_t)slot * p.stage_bytes;
-    const int kcw = min(KC, K - i * KC);
-    const int units = kcw / 128;
-    // unit u of stage i is unit i * (KC / 128) + u of the whole K range; the
-    // KW warps of a row group take those round-robin
-    int u0 = kw_i - (i * (KC / 128)) % p.KW;
-    if (u0 < 0) u0 += p.KW;
-    for (int u = u0; u < units; u += p.KW) {
-      // unit u is half uin of layout run sr inside this stage
-      const int sr = u >> 1, uin = u & 1;
-      const int kcw_r = min(kDecodeRun, kcw - sr * kDecodeRun);
-      const uint32_t wsm = st + p.bytes_x + sr * (uint32_t)run_full;
-      const uint32_t szs = wsm + (uint32_t)(Pc * (kcw_r / 64) * 512);
-      uint4 wv[T][2];
-      uint32_t zz[T][2];
-      float sc[T][2];
+    if (i < n_fast) {
 #pragma unroll
-      for (int t = 0; t < T; ++t) {
-        const int tl = pw_i * T + t;
-        if (t == 0 || tl < Pc) {
-          wv[t][0] = lds128(wsm + ((tl * (kcw_r / 64) + 2 * uin) * 32 + lane) * 16);
-          wv[t][1] = lds128(wsm + ((tl * (kcw_r / 64) + 2 * uin + 1) * 32 + lane) * 16);
-          if constexpr (!PC) {
-            const uint32_t w0 = lds32(szs + ((tl * (kcw_r / 128) + uin) * 16 + g) * 4);
-            const uint32_t w1 = lds32(szs + ((tl * (kcw_r / 128) + uin) * 16 + g + 8) * 4);
-            zz[t][0] = biased_zero_x2_of_word(w0);
-            zz[t][1] = biased_zero_x2_of_word(w1);
-            sc[t][0] = bf16_bits_to_float(w0 & 0xFFFF);
-            sc[t][1] = bf16_bits_to_float(w1 & 0xFFFF);
-          } else {
-            zz[t][0] = zzpc[t][0];
-            zz[t][1] = zzpc[t][1];
+      for (int j = 0; j < 2; ++j) {
+        if (j < NU) {
+          uint32_t wa[T], sa[T];
+#pragma unroll
+          for (int t = 0; t < T; ++t) {
+            wa[t] = st + wo[j][t];
+            sa[t] = st + so[j][t];
           }
+          unit(wa, sa, st + xo[j]);
         }
       }
-      uint32_t lane_base[8];
-      // M <= 8: all eight k16 steps' x fragments at once (16 registers, four
-      // ldmatrix.x4); wider M: per k16 step
-      uint32_t bb[MT == 1 ? 8 : 1][MT][2];
-      if constexpr (MT == 1) {
-        const uint32_t ub1 = st + (uint32_t)(2 * u) * (Mp * 128) + lane_off1;
-        const uint32_t a0 = ub1 + swz1[0], a1 = ub1 + swz1[1];
-        ldsm_x4(bb[0][0][0], bb[0][0][1], bb[1][0][0], bb[1][0][1], a0);
-        ldsm_x4(bb[2][0][0], bb[2][0][1], bb[3][0][0], bb[3][0][1], a1);
-        ldsm_x4(bb[4][0][0], bb[4][0][1], bb[5][0][0], bb[5][0][1], a0 + Mp * 128);
-        ldsm_x4(bb[6][0][0], bb[6][0][1], bb[7][0][0], bb[7][0][1], a1 + Mp * 128);
-      } else {
-        const uint32_t ub = st + (uint32_t)(2 * u) * (Mp * 128) + lane_off;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) lane_base[c] = ub + swz[c];
-      }
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        uint32_t bk[MT][2];
-        if constexpr (MT > 1) load_kk_x_frags<MT>(lane_base, kk, bk);
-        const uint32_t(&b)[MT][2] = MT == 1 ? bb[MT == 1 ? kk : 0] : bk;
+    } else {
+      const int kcw = min(KC, K - i * KC);
+      const int units = kcw / 128;
+      // unit u of stage i is unit i * (KC / 128) + u of the whole K range; the
+      // KW warps of a row group take those round-robin
+      int u0 = kw_i - (i * units_full) % p.KW;
+      if (u0 < 0) u0 += p.KW;
+      for (int u = u0; u < units; u += p.KW) {
+        // unit u is half uin of layout run sr inside this stage
+        const int sr = u >> 1, uin = u & 1;
+        const int kcw_r = min(kDecodeRun, kcw - sr * kDecodeRun);
+        const uint32_t wsm = st + p.bytes_x + sr * (uint32_t)run_full;
+        const uint32_t szs = wsm + (uint32_t)(Pc * (kcw_r / 64) * 512);
+        uint32_t wa[T], sa[T];
 #pragma unroll
         for (int t = 0; t < T; ++t) {
           const int tl = pw_i * T + t;
-          if (t == 0 || tl < Pc) {
-            const uint32_t w = word_of(wv[t][kk >> 2], kk & 3);
-            const uint32_t a[4] = {bf16x2_sub(int4_pair_to_bf16x2_biased(w), zz[t][0]),
-                                   bf16x2_sub(int4_pair_to_bf16x2_biased(w >> 4), zz[t][1]),
-                                   bf16x2_sub(int4_pair_to_bf16x2_biased(w >> 8), zz[t][0]),
-                                   bf16x2_sub(int4_pair_to_bf16x2_biased(w >> 12), zz[t][1])};
-#pragma unroll
-            for (int n = 0; n < MT; ++n) {
-              // grouped scales restart the chains every group (folded below)
-              if (!PC && kk < NC)
-                mma_bf16_16816_zero(accg[t][kk % NC][n], a, b[n][0], b[n][1]);
-              else
-                mma_bf16_16816(accg[t][kk % NC][n], a, b[n][0], b[n][1]);
-            }
-          }
+          wa[t] = wsm + ((tl * (kcw_r / 64) + 2 * uin) * 32 + lane) * 16;
+          sa[t] = szs + ((tl * (kcw_r / 128) + uin) * 16 + g) * 4;
         }
-      }
-      if constexpr (!PC) {
-        // grouped scales: fold the chains into acc once per group
-#pragma unroll
-        for (int t = 0; t < T; ++t)
-#pragma unroll
-          for (int n = 0; n < MT; ++n)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float v = accg[t][0][n][e];
-#pragma unroll
-              for (int c = 1; c < NC; ++c) v += accg[t][c][n][e];
-              acc[t][n][e] = fmaf(sc[t][e >> 1], v, acc[t][n][e]);
-            }
+        unit(wa, sa, st + (uint32_t)(2 * u) * (Mp * 128) + x_lane);
       }
     }
     __syncwarp();
