@@ -111,6 +111,12 @@ SPEAR_DEVINL void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1,
       : "memory");
 }
 
+// Fetch a tensor map (a kernel parameter) into the copy engine's descriptor
+// cache ahead of its first use.
+SPEAR_DEVINL void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 // Warm L2 with [src, src + bytes) (16-byte aligned, multiple of 16 bytes).
 SPEAR_DEVINL void prefetch_l2(const void* src, unsigned bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");

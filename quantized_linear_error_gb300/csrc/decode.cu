@@ -335,6 +335,7 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
         const int slot = i % p.NS;
         tma_load_3d(stages + (size_t)slot * p.stage_bytes, &xmap, 0, 0, i * (KC / 64), &full[slot]);
       };
+      prefetch_tensormap(&xmap);
       for (int i = 0; i < prefetch; ++i) issue_weights(i);
       if (EC) {
         // B rows of this CTA's tiles are read with ordinary loads at the end:
@@ -413,25 +414,26 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(ubar);  // release: this warp's share of u is visible to the consumers
       // The last CTA (over the grid) to have read z clears it and the counters
-      // for the next call.
+      // for the next call. Every load of z in this CTA has returned (its value
+      // is in shared memory), so one release fence orders them before the
+      // departure; the clearing stores need no fence of their own, as the next
+      // call touches z only after its grid-dependency wait, i.e. after this
+      // grid has completed.
       ec_bar();
       if (ew == 0) {
         int last = 0;
         if (lane == 0 && arrived) {
           __threadfence();
           last = atomicAdd(&p.sync->depart, 1u) == gridDim.x - 1;
-          __threadfence();
         }
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
+          __threadfence();  // acquire: every other CTA's reads of z precede the clearing
           for (int idx = lane; idx < p.rank * 8; idx += 32)
             reinterpret_cast<float4*>(p.z)[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
-          __syncwarp();
           if (lane == 0) {
-            __threadfence();
             p.sync->arrive = 0;
             p.sync->depart = 0;
-            __threadfence();
           }
         }
       }
