@@ -90,6 +90,14 @@ SPEAR_DEVINL void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t*
       : "memory");
 }
 
+// Same, destination given as a shared-space address.
+SPEAR_DEVINL void bulk_g2s_shared_u32(uint32_t dst, const void* src, unsigned bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Same, with an L2 evict-first hint for data read exactly once (weights).
 SPEAR_DEVINL void bulk_g2s_stream(void* dst, const void* src, unsigned bytes, uint64_t* bar,
                                   uint64_t policy) {

@@ -63,17 +63,15 @@ SPEAR_DEVINL void consumer_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory");
 }
 
-// B fragments (k16 x n8, col) for MT token tiles from a token-major smem
-// buffer: base[token * stride + k] (used for the gate output u).
+// ldmatrix.x4 on a shared-space address.
 SPEAR_DEVINL void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
-SPEAR_DEVINL void ldsm_x2(uint32_t& r0, uint32_t& r1, uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
-}
 
+// B fragments (k16 x n8, col) for MT token tiles from a token-major smem
+// buffer: base[token * stride + k] (used for the gate output u).
 template <int MT>
 SPEAR_DEVINL void load_token_frags(const __nv_bfloat16* base, int stride, int koff, int lane,
                                    uint32_t (&b)[MT][2]) {
@@ -86,36 +84,6 @@ SPEAR_DEVINL void load_token_frags(const __nv_bfloat16* base, int stride, int ko
       const int token = 8 * (2 * p + (mat >> 1)) + r;
       ldmatrix_x4(b[2 * p][0], b[2 * p][1], b[2 * p + 1][0], b[2 * p + 1][1],
                   base + token * stride + koff + 8 * (mat & 1));
-    }
-  }
-}
-
-// B fragments of x from a staged box laid out [k64 block][token][64] with the
-// 128-byte swizzle (16-byte chunk c of token row r sits at chunk c ^ (r & 7)).
-// Plain 32-bit shared loads, which the compiler can schedule around the MMAs
-// (the mbarrier wait and arrival, which clobber memory, still bound them).
-// Lane (g, t) reads token 8n + g at k = koff + 2t and koff + 2t + 8; the XOR
-// with g puts the 8 rows on 8 different chunks, so 32 lanes hit 32 banks.
-// All x fragments of one 128-channel unit (8 k16 steps) at once, so that one
-// load latency covers the unit, with ldmatrix on the swizzled box: lane l
-// gives the row address of matrix l / 8 (token tile pair half l / 16, k half
-// (l / 8) % 2), row l % 8; `lane_base[c]` is that address for chunk c of the
-// unit's first k64 block (the chunk XOR-ed with the token row, l % 8).
-// ldmatrix matrices: (tokens 8n.., k lo) -> b0 of n-tile n, (k hi) -> b1.
-template <int MT>
-SPEAR_DEVINL void load_unit_x_frags(const uint32_t (&lane_base)[8], uint32_t (&b)[8][MT][2]) {
-  constexpr int Mp = 8 * MT;
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const int c = (2 * kk) & 7;                 // chunk of k16 step kk inside its k64 block
-    const uint32_t blk = (kk >> 2) * Mp * 128;  // second k64 block for kk >= 4
-    if constexpr (MT == 1) {
-      ldsm_x2(b[kk][0][0], b[kk][0][1], lane_base[c] + blk);
-    } else {
-#pragma unroll
-      for (int pr = 0; pr < MT / 2; ++pr)
-        ldsm_x4(b[kk][2 * pr][0], b[kk][2 * pr][1], b[kk][2 * pr + 1][0], b[kk][2 * pr + 1][1],
-                lane_base[c] + blk + pr * 16 * 128);
     }
   }
 }
@@ -147,10 +115,6 @@ SPEAR_DEVINL void load_kk_x_frags(const uint32_t (&lane_base)[8], int kk, uint32
 
 SPEAR_DEVINL uint32_t word_of(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-
-SPEAR_DEVINL float gate_apply(float z, int gate) {
-  return gate == SPEAR_GATE_ONE ? z : z * (1.0f / (1.0f + expf(-z)));
 }
 
 // A does not depend on the previous kernel: pull this warp's units of it
@@ -275,6 +239,7 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
   uint64_t* empty = full + 16;
   uint64_t* szbar = full + 32;
   uint64_t* ubar = full + 33;  // compensator warp -> consumers: u is in shared memory
+  uint64_t* bbar = full + 34;  // B fragments of this CTA's tiles are in shared memory
   // stage buffers start on a 1024-byte boundary (the swizzle pattern of the x
   // box is defined on absolute shared-memory address bits)
   const uint32_t s0 = smem_u32(smem + kBarrierBytes);
@@ -284,6 +249,9 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
   __nv_bfloat16* uh = reinterpret_cast<__nv_bfloat16*>(szpc + (PC ? p.P * 16 : 0));
   __nv_bfloat16* ul = uh + Mp * us;
   float* zs_mlp = reinterpret_cast<float*>(ul + Mp * us);  // MLP gate: z [M][rank], then hidden [M][gh]
+  // B fragments of this CTA's tiles [Pc][rank / 16][32] uint4 (16-byte aligned)
+  const uint32_t bbuf_s =
+      (smem_u32(zs_mlp + (p.gh > 0 ? p.M * (p.rank + p.gh) : 0)) + 15u) & ~15u;
 
   const uint32_t stages_s = smem_u32(stages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -302,6 +270,7 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
     }
     mbar_init(szbar, 1);
     mbar_init(ubar, kEcWarps);
+    mbar_init(bbar, 1);
     fence_mbar_init();
   }
   // Token rows M..Mp-1 of the staged x boxes are zero-filled by the copy
@@ -338,9 +307,11 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
       prefetch_tensormap(&xmap);
       for (int i = 0; i < prefetch; ++i) issue_weights(i);
       if (EC) {
-        // B rows of this CTA's tiles are read with ordinary loads at the end:
-        // start pulling them into L2 now.
-        prefetch_l2(p.b_frag + (size_t)tile0 * (p.rank / 16) * 32, Pc * (p.rank / 16) * 512);
+        // B fragments of this CTA's tiles (contiguous, constant since create)
+        // into shared memory for the final up-projection.
+        const unsigned bbytes = (unsigned)(Pc * (p.rank / 16) * 512);
+        mbar_arrive_expect_tx(bbar, bbytes);
+        bulk_g2s_shared_u32(bbuf_s, p.b_frag + (size_t)tile0 * (p.rank / 16) * 32, bbytes, bbar);
       }
       asm volatile("griddepcontrol.wait;" ::: "memory");
       for (int i = 0; i < prefetch; ++i) issue_x(i);
@@ -444,6 +415,8 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
   // ------------------------------------------------------------ consumer warps
   const int pw_i = warp / p.KW, kw_i = warp % p.KW;
   const int g = lane >> 2, tq = lane & 3;
+  // The staged x box is laid out [k64 block][token][64] with the 128-byte
+  // swizzle (16-byte chunk c of token row r sits at chunk c ^ (r & 7)).
   // x box addressing for ldmatrix: this lane supplies row (lane % 8) of matrix
   // lane / 8, i.e. token 8 * (lane / 16) + lane % 8 and k half (lane / 8) % 2
   const int mrow = lane & 7, mkh = (lane >> 3) & 1, mtok = 8 * (lane >> 4) + mrow;
@@ -671,18 +644,8 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
   }
 
   // ------------------------------------------------------------ compensator term
-  // B fragments of this warp's first tile: loads in flight while u is awaited
-  constexpr int kBPre = MT == 1 ? 4 : 2;
-  uint4 bpre[kBPre];
-  if constexpr (EC) {
-#pragma unroll
-    for (int j = 0; j < kBPre; ++j)
-      bpre[j] = (warp < Pc && j < p.rank / 16)
-                    ? __ldg(p.b_frag + ((size_t)(tile0 + warp) * (p.rank / 16) + j) * 32 + lane)
-                    : make_uint4(0u, 0u, 0u, 0u);
-  }
   bool ec_ok = false;
-  if constexpr (EC) ec_ok = mbar_wait_bounded(ubar, 0, 2 * p.wait_ns);
+  if constexpr (EC) ec_ok = mbar_wait_bounded(ubar, 0, 2 * p.wait_ns) && mbar_wait_bounded(bbar, 0, p.wait_ns);
   consumer_bar<NW>();  // partial sums of all K warps are in shared memory
 
   // ------------------------------------------------------------ finalize tiles
@@ -703,27 +666,17 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
     if constexpr (EC) {
       if (ec_ok) {
         const int nj = p.rank / 16;
-        for (int j0 = 0; j0 < nj; j0 += kBPre) {
-          uint4 bf[kBPre];
+        const uint32_t bt = bbuf_s + (uint32_t)(((tl * nj) * 32 + lane) * 16);
+#pragma unroll 1
+        for (int j = 0; j < nj; ++j) {
+          const uint4 bf = lds128(bt + (uint32_t)j * 512);
+          const uint32_t a[4] = {bf.x, bf.y, bf.z, bf.w};
 #pragma unroll
-          for (int jj = 0; jj < kBPre; ++jj)
-            bf[jj] = (tl == warp && j0 == 0)
-                         ? bpre[jj]
-                         : (j0 + jj < nj ? __ldg(p.b_frag + ((size_t)tile * nj + j0 + jj) * 32 + lane)
-                                         : make_uint4(0u, 0u, 0u, 0u));
+          for (int part = 0; part < 2; ++part) {  // u = hi + lo
+            uint32_t bu[MT][2];
+            load_token_frags<MT>(part ? ul : uh, us, j * 16, lane, bu);
 #pragma unroll
-          for (int jj = 0; jj < kBPre; ++jj) {
-            if (j0 + jj < nj) {
-              const uint32_t a[4] = {bf[jj].x, bf[jj].y, bf[jj].z, bf[jj].w};
-              uint32_t bh[MT][2], bl[MT][2];
-              load_token_frags<MT>(uh, us, (j0 + jj) * 16, lane, bh);
-              load_token_frags<MT>(ul, us, (j0 + jj) * 16, lane, bl);
-#pragma unroll
-              for (int n = 0; n < MT; ++n) {
-                mma_bf16_16816(c[n], a, bh[n][0], bh[n][1]);
-                mma_bf16_16816(c[n], a, bl[n][0], bl[n][1]);
-              }
-            }
+            for (int n = 0; n < MT; ++n) mma_bf16_16816(c[n], a, bu[n][0], bu[n][1]);
           }
         }
       }
@@ -826,8 +779,9 @@ spear_status_t spear_launch_decode(spear_linear_s* h, const __nv_bfloat16* x, __
   const size_t u_bytes = ec ? (size_t)2 * Mp * (h->rank + 8) * 2 : 0;
   const size_t mlp_bytes = h->gate_hidden > 0 ? (size_t)M * (h->rank + h->gate_hidden) * 4 : 0;
   const size_t pc_bytes = h->per_channel ? (size_t)P * 64 : 0;
+  const size_t b_bytes = ec ? (size_t)P * (h->rank / 16) * 512 + 16 : 0;
   // barriers, alignment slack, per-channel words, u (hi and lo)
-  const size_t fixed = kBarrierBytes + 1024 + pc_bytes + u_bytes + mlp_bytes;
+  const size_t fixed = kBarrierBytes + 1024 + pc_bytes + u_bytes + mlp_bytes + b_bytes;
   const size_t budget = kSmemCap > fixed ? kSmemCap - fixed : 0;
   int NS = (int)(budget / p.stage_bytes);
   if (NS > kMaxStages) NS = kMaxStages;
