@@ -70,24 +70,6 @@ SPEAR_DEVINL void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3
                : "r"(addr));
 }
 
-// B fragments (k16 x n8, col) for MT token tiles from a token-major smem
-// buffer: base[token * stride + k] (used for the gate output u).
-template <int MT>
-SPEAR_DEVINL void load_token_frags(const __nv_bfloat16* base, int stride, int koff, int lane,
-                                   uint32_t (&b)[MT][2]) {
-  const int mat = lane >> 3, r = lane & 7;
-  if constexpr (MT == 1) {
-    ldmatrix_x2(b[0][0], b[0][1], base + r * stride + koff + 8 * (mat & 1));
-  } else {
-#pragma unroll
-    for (int p = 0; p < MT / 2; ++p) {
-      const int token = 8 * (2 * p + (mat >> 1)) + r;
-      ldmatrix_x4(b[2 * p][0], b[2 * p][1], b[2 * p + 1][0], b[2 * p + 1][1],
-                  base + token * stride + koff + 8 * (mat & 1));
-    }
-  }
-}
-
 // D = A B (no accumulator input: the first k16 step of a chain).
 SPEAR_DEVINL void mma_bf16_16816_zero(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -649,50 +631,46 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
   consumer_bar<NW>();  // partial sums of all K warps are in shared memory
 
   // ------------------------------------------------------------ finalize tiles
-  for (int tl = warp; tl < Pc; tl += NW) {
-    float c[MT][4];
-#pragma unroll
-    for (int n = 0; n < MT; ++n)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) c[n][e] = 0.f;
+  // One (tile, 8-token column block) per warp and step, so that with several
+  // token blocks (M > 8) all consumer warps share the reduction over the K
+  // warps, the up-projection and the stores.
+  const int mat = lane >> 3, mr = lane & 7;
+  for (int it = warp; it < Pc * MT; it += NW) {
+    const int tl = it / MT, n = it % MT;
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
     for (int kw = 0; kw < p.KW; ++kw) {
-      const float* src = red + ((size_t)(tl * p.KW + kw) * 32 + lane) * 4 * MT;
+      const float* src = red + ((size_t)(tl * p.KW + kw) * 32 + lane) * 4 * MT + n * 4;
 #pragma unroll
-      for (int n = 0; n < MT; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) c[n][e] += src[n * 4 + e];
+      for (int e = 0; e < 4; ++e) c[e] += src[e];
     }
     const int tile = tile0 + tl;
     if constexpr (EC) {
       if (ec_ok) {
         const int nj = p.rank / 16;
         const uint32_t bt = bbuf_s + (uint32_t)(((tl * nj) * 32 + lane) * 16);
-#pragma unroll 1
+        // this lane's ldmatrix row of u: token 8 n + lane % 8, k half lane / 8 % 2
+        const int uoff = (8 * n + mr) * us + 8 * (mat & 1);
+#pragma unroll 2
         for (int j = 0; j < nj; ++j) {
           const uint4 bf = lds128(bt + (uint32_t)j * 512);
           const uint32_t a[4] = {bf.x, bf.y, bf.z, bf.w};
-#pragma unroll
-          for (int part = 0; part < 2; ++part) {  // u = hi + lo
-            uint32_t bu[MT][2];
-            load_token_frags<MT>(part ? ul : uh, us, j * 16, lane, bu);
-#pragma unroll
-            for (int n = 0; n < MT; ++n) mma_bf16_16816(c[n], a, bu[n][0], bu[n][1]);
-          }
+          uint32_t h0, h1, l0, l1;  // u = hi + lo
+          ldmatrix_x2(h0, h1, uh + uoff + j * 16);
+          ldmatrix_x2(l0, l1, ul + uoff + j * 16);
+          mma_bf16_16816(c, a, h0, h1);
+          mma_bf16_16816(c, a, l0, l1);
         }
       }
     }
     const int row0 = tile * 16 + g, row1 = row0 + 8;
-#pragma unroll
-    for (int n = 0; n < MT; ++n) {
-      const int m0 = 8 * n + 2 * tq, m1 = m0 + 1;
-      if (row0 < p.N) {
-        if (m0 < p.M) p.y[(size_t)m0 * p.N + row0] = __float2bfloat16_rn(c[n][0]);
-        if (m1 < p.M) p.y[(size_t)m1 * p.N + row0] = __float2bfloat16_rn(c[n][1]);
-      }
-      if (row1 < p.N) {
-        if (m0 < p.M) p.y[(size_t)m0 * p.N + row1] = __float2bfloat16_rn(c[n][2]);
-        if (m1 < p.M) p.y[(size_t)m1 * p.N + row1] = __float2bfloat16_rn(c[n][3]);
-      }
+    const int m0 = 8 * n + 2 * tq, m1 = m0 + 1;
+    if (row0 < p.N) {
+      if (m0 < p.M) p.y[(size_t)m0 * p.N + row0] = __float2bfloat16_rn(c[0]);
+      if (m1 < p.M) p.y[(size_t)m1 * p.N + row0] = __float2bfloat16_rn(c[1]);
+    }
+    if (row1 < p.N) {
+      if (m0 < p.M) p.y[(size_t)m0 * p.N + row1] = __float2bfloat16_rn(c[2]);
+      if (m1 < p.M) p.y[(size_t)m1 * p.N + row1] = __float2bfloat16_rn(c[3]);
     }
   }
 }
