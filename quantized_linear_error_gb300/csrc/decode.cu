@@ -3,7 +3,8 @@
 // Recovery", section 2.2A: in the memory-bound decode phase the compensator is
 // fused into the low-bit GEMM so the correction path is a single kernel).
 //
-// Design (one CTA per SM; 16 consumer warps, 8 for M > 16 with <= 2 tiles per CTA, + 1 producer warp):
+// Design (one CTA per SM; 16 consumer warps, or 8 / 10 for M > 16 with 2 / 5
+// tiles per CTA, + 1 producer warp + 4 compensator warps):
 //  * The CTA owns P consecutive 16-row tiles of W. A producer warp streams K
 //    in stages: per stage one bulk copy brings the tiles' packed codes and
 //    scale/zero words (laid out at create as one contiguous run per CTA and
@@ -780,7 +781,8 @@ spear_status_t spear_launch_decode(spear_linear_s* h, const __nv_bfloat16* x, __
   else if (MT == 2)
     e = launch_t<16, 2, 1>(p, xmap, pc, ec, grid, smem, stream);
   else
-    e = NW == 8 ? launch_t<8, 4, 1>(p, xmap, pc, ec, grid, smem, stream)
-                : launch_t<16, 4, 1>(p, xmap, pc, ec, grid, smem, stream);
+    e = NW == 8    ? launch_t<8, 4, 1>(p, xmap, pc, ec, grid, smem, stream)
+        : NW == 10 ? launch_t<10, 4, 1>(p, xmap, pc, ec, grid, smem, stream)
+                   : launch_t<16, 4, 1>(p, xmap, pc, ec, grid, smem, stream);
   return e == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
 }

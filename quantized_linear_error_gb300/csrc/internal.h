@@ -126,8 +126,10 @@ inline int decode_tiles_per_cta(int nt16, int sm_count) { return (nt16 + sm_coun
 // whole number of layout runs).
 inline void decode_plan(int P, int K, int M, int* NW, int* T, int* KW, int* KC) {
   // M > 16: with one or two tiles per CTA, 8 warps already split K four ways
-  // (measured faster than 16); with more tiles 16 warps keep every warp busy.
-  *NW = (M > 16 && P <= 2) ? 8 : 16;
+  // (measured faster than 16); five tiles take 10 warps (two K warps per tile,
+  // and no register spills, which the 16-warp variant has at M > 16); other
+  // tile counts take 16 warps to keep every warp busy.
+  *NW = (M > 16 && P <= 2) ? 8 : (M > 16 && P == 5) ? 10 : 16;
   *T = P > *NW ? 2 : 1;
   const int pw = (P + *T - 1) / *T;  // warps along rows
   *KW = *NW / pw;                    // warps along K; 128-channel units go round-robin
