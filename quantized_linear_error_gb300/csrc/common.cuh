@@ -204,6 +204,48 @@ SPEAR_DEVINL uint32_t biased_zero_x2_of_word(uint32_t w) {
 
 SPEAR_DEVINL float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
 
+// ---------------------------------------------------------------- decode-layout A fragments
+// One code word w of the decode layout holds nibble j and j + 4 of A-fragment
+// register j (j = 0..3; registers 0 and 2 are row g, 1 and 3 row g + 8).
+// Masked without a shift, a nibble pair reads as a bf16 pair of tiny values:
+// (w & 0x000F000F) puts code q in the mantissa with a zero exponent field, i.e.
+// q * 2^-133; (w & 0x00F000F0) puts 16 q in bits 0..7, whose top bit is the
+// exponent field's lowest bit, and since the subnormal binade and the first
+// normal one share the spacing 2^-133 it reads as 16 q * 2^-133 for every q.
+// One fma.rn.bf16x2 by 2^126 plus c, with c = -z * 2^-7 for the low nibbles
+// and -z * 2^-3 for the high ones, then yields (q - z) * 2^-7 and
+// (q - z) * 2^-3, both exact (bf16 arithmetic keeps subnormal inputs), so
+// rows g carry the factor 2^-7 and rows g + 8 the factor 2^-3, which an exact
+// fp32 multiplication by kFragScaleLo / kFragScaleHi takes back before the
+// scale is applied (scaling s instead could overflow). One shift, four masks and
+// four fmas per word, against three shifts, four masks and four subtractions
+// for the biased form (bias 128 in the exponent, minus 128 + z).
+constexpr float kFragScaleLo = 128.f;  // rows g: fragment values are (q - z) * 2^-7
+constexpr float kFragScaleHi = 8.f;    // rows g + 8: fragment values are (q - z) * 2^-3
+
+SPEAR_DEVINL uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
+// The additive terms from the pair bf16(128 + z) in both halves (exact).
+SPEAR_DEVINL uint32_t frag_zero_lo(uint32_t biased_zz) {  // -z * 2^-7 = 1 - (128 + z) * 2^-7
+  return bf16x2_fma(biased_zz, 0xBC00BC00u /* -2^-7 */, 0x3F803F80u /* 1 */);
+}
+SPEAR_DEVINL uint32_t frag_zero_hi(uint32_t biased_zz) {  // -z * 2^-3 = 16 - (128 + z) * 2^-3
+  return bf16x2_fma(biased_zz, 0xBE00BE00u /* -2^-3 */, 0x41804180u /* 16 */);
+}
+
+SPEAR_DEVINL void decode_frag_unpack(uint32_t w, uint32_t c_lo, uint32_t c_hi, uint32_t (&a)[4]) {
+  constexpr uint32_t k2p126 = 0x7E807E80u;  // 2^126 in both halves
+  const uint32_t w8 = w >> 8;
+  a[0] = bf16x2_fma(w & 0x000F000Fu, k2p126, c_lo);
+  a[1] = bf16x2_fma(w & 0x00F000F0u, k2p126, c_hi);
+  a[2] = bf16x2_fma(w8 & 0x000F000Fu, k2p126, c_lo);
+  a[3] = bf16x2_fma(w8 & 0x00F000F0u, k2p126, c_hi);
+}
+
 SPEAR_DEVINL uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

@@ -12,8 +12,10 @@
 //    copy brings x[0:Mp, k-slice] with a 128-byte swizzle (tokens past M are
 //    zero-filled by the copy engine), both counted on one mbarrier.
 //  * Consumer warps turn each 32-bit word into four bf16 A-fragment registers
-//    with one LOP3 per pair (codes land in the mantissa of 128 + code) and one
-//    bf16x2 subtraction of 128 + zero, which leaves the exact integer q - z.
+//    with one shift, one mask per pair (the codes land in the mantissa of a
+//    bf16 pair with an exponent field of 0 or 1) and one bf16x2 fma by 2^126
+//    with -z * 2^-7 or -z * 2^-3, which leaves the exact (q - z) * 2^-7 or
+//    (q - z) * 2^-3; the power of two is taken back in fp32.
 //    Warp MMA (m16n8k16, fp32 accumulate) takes x as the 8-wide N operand
 //    (tokens), and the group scale is applied once per group to the fp32
 //    partial sum.
@@ -436,8 +438,8 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
     for (int t = 0; t < T; ++t) {
       const int tl = pw_i * T + t;
       const uint32_t w0 = tl < Pc ? szpc[tl * 16 + g] : 0u, w1 = tl < Pc ? szpc[tl * 16 + g + 8] : 0u;
-      zzpc[t][0] = biased_zero_x2(w0 >> 16);
-      zzpc[t][1] = biased_zero_x2(w1 >> 16);
+      zzpc[t][0] = frag_zero_lo(biased_zero_x2(w0 >> 16));
+      zzpc[t][1] = frag_zero_hi(biased_zero_x2(w1 >> 16));
       spc[t][0] = bf16_bits_to_float(w0 & 0xFFFF);
       spc[t][1] = bf16_bits_to_float(w1 & 0xFFFF);
     }
@@ -460,8 +462,8 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
         if constexpr (!PC) {
           const uint32_t w0 = lds32(sa[t]);
           const uint32_t w1 = lds32(sa[t] + 32);
-          zz[t][0] = biased_zero_x2_of_word(w0);
-          zz[t][1] = biased_zero_x2_of_word(w1);
+          zz[t][0] = frag_zero_lo(biased_zero_x2_of_word(w0));
+          zz[t][1] = frag_zero_hi(biased_zero_x2_of_word(w1));
           sc[t][0] = bf16_bits_to_float(w0 & 0xFFFF);
           sc[t][1] = bf16_bits_to_float(w1 & 0xFFFF);
         } else {
@@ -494,10 +496,8 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
         const int tl = pw_i * T + t;
         if (t == 0 || tl < Pc) {
           const uint32_t w = word_of(wv[t][kk >> 2], kk & 3);
-          const uint32_t a[4] = {bf16x2_sub(int4_pair_to_bf16x2_biased(w), zz[t][0]),
-                                 bf16x2_sub(int4_pair_to_bf16x2_biased(w >> 4), zz[t][1]),
-                                 bf16x2_sub(int4_pair_to_bf16x2_biased(w >> 8), zz[t][0]),
-                                 bf16x2_sub(int4_pair_to_bf16x2_biased(w >> 12), zz[t][1])};
+          uint32_t a[4];
+          decode_frag_unpack(w, zz[t][0], zz[t][1], a);
 #pragma unroll
           for (int n = 0; n < MT; ++n) {
             // grouped scales restart the chains every group (folded below)
@@ -520,7 +520,7 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
             float v = accg[t][0][n][e];
 #pragma unroll
             for (int c = 1; c < NC; ++c) v += accg[t][c][n][e];
-            acc[t][n][e] = fmaf(sc[t][e >> 1], v, acc[t][n][e]);
+            acc[t][n][e] = fmaf(sc[t][e >> 1], v * ((e >> 1) ? kFragScaleHi : kFragScaleLo), acc[t][n][e]);
           }
     }
   };
@@ -607,7 +607,7 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
           float v = accg[t][0][n][e];
 #pragma unroll
           for (int c = 1; c < NC; ++c) v += accg[t][c][n][e];
-          acc[t][n][e] = v * spc[t][e >> 1];
+          acc[t][n][e] = (v * ((e >> 1) ? kFragScaleHi : kFragScaleLo)) * spc[t][e >> 1];
         }
   }
 

@@ -110,12 +110,13 @@ __global__ void copy_pad_rows(const uint16_t* __restrict__ m, int rows, int rows
     out[i] = (i / cols) < rows ? m[i] : (uint16_t)0;
 }
 
-// (q - z) * s with one rounding: the exact integer difference comes from the
-// kernels' own unpack (biased bf16 pair minus biased zero), the product of an
-// integer |d| <= 15 and a bf16 scale is exact in fp32, and the conversion to
+// (q - z) * s with one rounding: the exact difference d = (q - z) * 2^-e comes
+// from the kernels' own unpack (e = 0 for the prefill layout; e = 7 or 3 for
+// the decode layout), d * 2^e is exact, its product with s is exact in fp32
+// (at most 4 + 8 significant bits) unless it overflows, and the conversion to
 // bf16 rounds once to nearest even.
-__device__ __forceinline__ __nv_bfloat16 scaled(uint32_t diff_bits16, float s) {
-  return __float2bfloat16_rn(bf16_bits_to_float(diff_bits16) * s);
+__device__ __forceinline__ __nv_bfloat16 scaled(uint32_t diff_bits16, float s, float pow2 = 1.f) {
+  return __float2bfloat16_rn((bf16_bits_to_float(diff_bits16) * pow2) * s);
 }
 
 __global__ void dequant_from_decode(const uint8_t* __restrict__ wq, const uint32_t* __restrict__ sz_pc, int K, int N,
@@ -130,29 +131,29 @@ __global__ void dequant_from_decode(const uint8_t* __restrict__ wq, const uint32
     const uint32_t* szb = L.per_channel ? sz_pc + (size_t)tile * 16
                                         : reinterpret_cast<const uint32_t*>(wq + L.sz_offset(tile, (kb * 64) / 128));
     const uint32_t sz0 = szb[g], sz1 = szb[g + 8];
-    const uint32_t zz0 = biased_zero_x2(sz0 >> 16), zz1 = biased_zero_x2(sz1 >> 16);
+    const uint32_t c0 = frag_zero_lo(biased_zero_x2(sz0 >> 16)), c1 = frag_zero_hi(biased_zero_x2(sz1 >> 16));
     const float s0 = bf16_bits_to_float(sz0 & 0xFFFF), s1 = bf16_bits_to_float(sz1 & 0xFFFF);
     const uint4 v = *reinterpret_cast<const uint4*>(wq + L.w_offset(tile, kb) + lane * 16);
     const uint32_t words[4] = {v.x, v.y, v.z, v.w};
     const int r0 = tile * 16 + g, r1 = r0 + 8;
     for (int s = 0; s < 4; ++s) {
-      const uint32_t w = words[s];
-      const uint32_t d0 = bf16x2_sub(int4_pair_to_bf16x2_biased(w), zz0);        // (r0, k), (r0, k+1)
-      const uint32_t d1 = bf16x2_sub(int4_pair_to_bf16x2_biased(w >> 4), zz1);   // (r1, k), (r1, k+1)
-      const uint32_t d2 = bf16x2_sub(int4_pair_to_bf16x2_biased(w >> 8), zz0);   // (r0, k+8), (r0, k+9)
-      const uint32_t d3 = bf16x2_sub(int4_pair_to_bf16x2_biased(w >> 12), zz1);  // (r1, k+8), (r1, k+9)
+      // the decode kernel's own unpack: (q - z) * 2^-7 for rows r0, (q - z) * 2^-3
+      // for rows r1, taken back by an exact power-of-two product before the scale
+      uint32_t d[4];
+      decode_frag_unpack(words[s], c0, c1, d);
+      const uint32_t d0 = d[0], d1 = d[1], d2 = d[2], d3 = d[3];  // (r0, k..k+1) (r1, k..) (r0, k+8..) (r1, k+8..)
       const int k = kb * 64 + s * 16 + 2 * t;
       if (r0 < N) {
-        out[(size_t)r0 * K + k] = scaled(d0 & 0xFFFF, s0);
-        out[(size_t)r0 * K + k + 1] = scaled(d0 >> 16, s0);
-        out[(size_t)r0 * K + k + 8] = scaled(d2 & 0xFFFF, s0);
-        out[(size_t)r0 * K + k + 9] = scaled(d2 >> 16, s0);
+        out[(size_t)r0 * K + k] = scaled(d0 & 0xFFFF, s0, kFragScaleLo);
+        out[(size_t)r0 * K + k + 1] = scaled(d0 >> 16, s0, kFragScaleLo);
+        out[(size_t)r0 * K + k + 8] = scaled(d2 & 0xFFFF, s0, kFragScaleLo);
+        out[(size_t)r0 * K + k + 9] = scaled(d2 >> 16, s0, kFragScaleLo);
       }
       if (r1 < N) {
-        out[(size_t)r1 * K + k] = scaled(d1 & 0xFFFF, s1);
-        out[(size_t)r1 * K + k + 1] = scaled(d1 >> 16, s1);
-        out[(size_t)r1 * K + k + 8] = scaled(d3 & 0xFFFF, s1);
-        out[(size_t)r1 * K + k + 9] = scaled(d3 >> 16, s1);
+        out[(size_t)r1 * K + k] = scaled(d1 & 0xFFFF, s1, kFragScaleHi);
+        out[(size_t)r1 * K + k + 1] = scaled(d1 >> 16, s1, kFragScaleHi);
+        out[(size_t)r1 * K + k + 8] = scaled(d3 & 0xFFFF, s1, kFragScaleHi);
+        out[(size_t)r1 * K + k + 9] = scaled(d3 >> 16, s1, kFragScaleHi);
       }
     }
   }
