@@ -35,6 +35,7 @@ namespace {
 
 constexpr int kMaxStages = 8;
 constexpr int kEcWarps = 4;  // compensator warps per CTA
+constexpr int kEcSmemUnits = 4;  // units of the CTA's share of A staged in shared memory (4 KB each)
 constexpr int kBarrierBytes = 1024;
 constexpr size_t kSmemCap = 200 * 1024;
 
@@ -102,18 +103,29 @@ SPEAR_DEVINL uint32_t word_of(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-// A does not depend on the previous kernel: pull this warp's units of it
-// (4 KB each, contiguous in fragment order) into L2 before waiting for x.
-SPEAR_DEVINL void ec_prefetch(const DecodeParams& p, int ew, int lane) {
+// This CTA's share [u0, u1) of the projection units (one unit: 16 A rows x 128
+// channels, 4 KB contiguous in fragment order).
+SPEAR_DEVINL void ec_share(const DecodeParams& p, int& u0, int& u1) {
+  // units <= 16 * (K / 128) and grid <= SM count keep the products in 32 bits
+  const unsigned units = (unsigned)((p.rank / 16) * (p.K / 128));
+  u0 = (int)(blockIdx.x * units / gridDim.x);
+  u1 = (int)((blockIdx.x + 1) * units / gridDim.x);
+}
+
+SPEAR_DEVINL const uint4* ec_unit_ptr(const DecodeParams& p, int ua) {
   const int kb128 = p.K / 128;
-  const int units = (p.rank / 16) * kb128;
-  const int u0 = (int)((long)blockIdx.x * units / gridDim.x);
-  const int u1 = (int)((long)(blockIdx.x + 1) * units / gridDim.x);
+  return p.a_frag + ((size_t)(ua / kb128) * (p.K / 16) + (ua % kb128) * 8) * 32;
+}
+
+// A does not depend on the previous kernel: the producer copies the first
+// kEcSmemUnits units of the share into shared memory ahead of the weights;
+// pull this warp's remaining units into L2 before waiting for x.
+SPEAR_DEVINL void ec_prefetch(const DecodeParams& p, int ew, int lane) {
+  int u0, u1;
+  ec_share(p, u0, u1);
   if (lane == 0)
-    for (int ua = u0 + ew; ua < u1; ua += kEcWarps) {
-      const int at = ua / kb128, kb = ua % kb128;
-      prefetch_l2(p.a_frag + ((size_t)at * (p.K / 16) + kb * 8) * 32, 8 * 32 * 16);
-    }
+    for (int ua = u0 + ew; ua < u1; ua += kEcWarps)
+      if (ua - u0 >= kEcSmemUnits) prefetch_l2(ec_unit_ptr(p, ua), 8 * 32 * 16);
 }
 
 // Bottleneck-MLP gate ("SPEAR", section 2.1A: gamma is a bottleneck MLP):
@@ -144,13 +156,13 @@ SPEAR_DEVINL float dot_bf16_f32(const uint4* w, const float4* v, int n8) {
 }
 
 template <int Mp>
-SPEAR_DEVINL void ec_u_mlp(const DecodeParams& p, bool arrived, int tid, float* zs, float* ts, __nv_bfloat16* uh,
-                           __nv_bfloat16* ul, int us) {
+SPEAR_DEVINL void ec_u_mlp(const DecodeParams& p, const float* z, bool arrived, int tid, float* zs, float* ts,
+                           __nv_bfloat16* uh, __nv_bfloat16* ul, int us) {
   constexpr int kThr = kEcWarps * 32;
   const int r = p.rank, hh = p.gh, M = p.M;
   for (int i = tid; i < M * r; i += kThr) {
     const int m = i / r, j = i - m * r;
-    zs[i] = arrived ? __ldcg(p.z + j * 32 + m) : 0.f;
+    zs[i] = arrived ? __ldcg(z + j * 32 + m) : 0.f;
   }
   ec_bar();
   for (int i = tid; i < M * hh; i += kThr) {
@@ -176,19 +188,21 @@ SPEAR_DEVINL void ec_u_mlp(const DecodeParams& p, bool arrived, int tid, float* 
 
 // z += A[:, this CTA's share] x, via warp MMA with A rows as the M side.
 template <int MT>
-SPEAR_DEVINL void ec_project(const DecodeParams& p, int ew, int lane) {
+SPEAR_DEVINL void ec_project(const DecodeParams& p, float* z, int ew, int lane, uint32_t abuf_s) {
   const int kb128 = p.K / 128;
-  const int units = (p.rank / 16) * kb128;
-  const int u0 = (int)((long)blockIdx.x * units / gridDim.x);
-  const int u1 = (int)((long)(blockIdx.x + 1) * units / gridDim.x);
+  int u0, u1;
+  ec_share(p, u0, u1);
   const int g = lane >> 2, tq = lane & 3;
   for (int ua = u0 + ew; ua < u1; ua += kEcWarps) {
     const int at = ua / kb128, kb = ua % kb128;
+    const bool staged = ua - u0 < kEcSmemUnits;
+    const uint4* ag = ec_unit_ptr(p, ua) + lane;
+    const uint32_t as = abuf_s + (uint32_t)(((ua - u0) * 256 + lane) * 16);
     float c[2][MT][4] = {};
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       const int k16 = kb * 8 + kk;
-      const uint4 af = __ldg(p.a_frag + ((size_t)at * (p.K / 16) + k16) * 32 + lane);
+      const uint4 af = staged ? lds128(as + kk * 512) : __ldg(ag + kk * 32);
       const uint32_t a[4] = {af.x, af.y, af.z, af.w};
 #pragma unroll
       for (int n = 0; n < MT; ++n) {
@@ -204,8 +218,8 @@ SPEAR_DEVINL void ec_project(const DecodeParams& p, int ew, int lane) {
     }
 #pragma unroll
     for (int n = 0; n < MT; ++n) {
-      red_add_v2(p.z + (16 * at + g) * 32 + 8 * n + 2 * tq, c[0][n][0] + c[1][n][0], c[0][n][1] + c[1][n][1]);
-      red_add_v2(p.z + (16 * at + g + 8) * 32 + 8 * n + 2 * tq, c[0][n][2] + c[1][n][2], c[0][n][3] + c[1][n][3]);
+      red_add_v2(z + (16 * at + g) * 32 + 8 * n + 2 * tq, c[0][n][0] + c[1][n][0], c[0][n][1] + c[1][n][1]);
+      red_add_v2(z + (16 * at + g + 8) * 32 + 8 * n + 2 * tq, c[0][n][2] + c[1][n][2], c[0][n][3] + c[1][n][3]);
     }
   }
 }
@@ -225,6 +239,7 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
   uint64_t* szbar = full + 32;
   uint64_t* ubar = full + 33;  // compensator warp -> consumers: u is in shared memory
   uint64_t* bbar = full + 34;  // B fragments of this CTA's tiles are in shared memory
+  uint64_t* abar = full + 35;  // the staged units of this CTA's share of A are in shared memory
   // stage buffers start on a 1024-byte boundary (the swizzle pattern of the x
   // box is defined on absolute shared-memory address bits)
   const uint32_t s0 = smem_u32(smem + kBarrierBytes);
@@ -237,6 +252,8 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
   // B fragments of this CTA's tiles [Pc][rank / 16][32] uint4 (16-byte aligned)
   const uint32_t bbuf_s =
       (smem_u32(zs_mlp + (p.gh > 0 ? p.M * (p.rank + p.gh) : 0)) + 15u) & ~15u;
+  // staged units of A [kEcSmemUnits][8][32] uint4, after the B fragments
+  const uint32_t abuf_s = bbuf_s + (uint32_t)(p.P * (p.rank / 16) * 512);
 
   const uint32_t stages_s = smem_u32(stages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -256,6 +273,7 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
     mbar_init(szbar, 1);
     mbar_init(ubar, kEcWarps);
     mbar_init(bbar, 1);
+    mbar_init(abar, 1);
     fence_mbar_init();
   }
   // Token rows M..Mp-1 of the staged x boxes are zero-filled by the copy
@@ -275,8 +293,12 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
         mbar_arrive_expect_tx(szbar, Pc * 64);
         bulk_g2s(szpc, p.sz + (size_t)tile0 * 16, Pc * 64, szbar);
       }
-      // Weights (constant since create) of the first NS stages go out before
-      // the wait on the previous kernel; x, which that kernel may produce, after.
+      // Weights and compensator factors are constant since create, x may be
+      // produced by the previous kernel. The CTA that lands on the SM freed
+      // last by the previous grid reaches the wait only after the issues made
+      // before it, so before it go only the first stage's weights (and the
+      // staged units of A); right after it, the first stage's x, then the
+      // other stages and the B fragments.
       const int prefetch = min(p.NS, p.n_stages);
       auto issue_weights = [&](int i) {
         const int slot = i % p.NS;
@@ -290,7 +312,22 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
         tma_load_3d(stages + (size_t)slot * p.stage_bytes, &xmap, 0, 0, i * (KC / 64), &full[slot]);
       };
       prefetch_tensormap(&xmap);
-      for (int i = 0; i < prefetch; ++i) issue_weights(i);
+      if (EC) {
+        // the first units of this CTA's share of A, ahead of the weights: the
+        // projection they feed is on the path to every CTA's final result
+        int u0, u1;
+        ec_share(p, u0, u1);
+        const int ns = min(u1 - u0, kEcSmemUnits);
+        mbar_arrive_expect_tx(abar, (unsigned)(ns * 4096));
+        for (int j = 0; j < ns; ++j) bulk_g2s_shared_u32(abuf_s + j * 4096, ec_unit_ptr(p, u0 + j), 4096, abar);
+      }
+      issue_weights(0);
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      issue_x(0);
+      for (int i = 1; i < prefetch; ++i) {
+        issue_weights(i);
+        issue_x(i);
+      }
       if (EC) {
         // B fragments of this CTA's tiles (contiguous, constant since create)
         // into shared memory for the final up-projection.
@@ -298,8 +335,6 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
         mbar_arrive_expect_tx(bbar, bbytes);
         bulk_g2s_shared_u32(bbuf_s, p.b_frag + (size_t)tile0 * (p.rank / 16) * 32, bbytes, bbar);
       }
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-      for (int i = 0; i < prefetch; ++i) issue_x(i);
       for (int i = prefetch; i < p.n_stages; ++i) {
         const int slot = i % p.NS;
         if (!mbar_wait_bounded(&empty[slot], ((i / p.NS) - 1) & 1, p.wait_ns)) {
@@ -320,18 +355,37 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
       volatile int* ec_flag = reinterpret_cast<volatile int*>(smem + 512);
       ec_prefetch(p, ew, lane);
       asm volatile("griddepcontrol.wait;" ::: "memory");
-      ec_project<MT>(p, ew, lane);
+      // Calls alternate between two z buffers. `epoch` (calls completed so
+      // far) is read by every CTA before its arrival and advanced by the last
+      // CTA to arrive, after which no CTA of this call reads it; this call adds
+      // into z[epoch % 2] and clears z[(epoch + 1) % 2] for the next call (the
+      // previous call, which used that buffer, has completed). The arrival
+      // counter is never reset: a call is complete at (epoch + 1) * grid.
+      const unsigned ep = __ldcg(&p.sync->epoch);
+      float* zc = p.z + (ep & 1u) * kZDecFloats;
+      {
+        float4* zn = reinterpret_cast<float4*>(p.z + ((ep + 1u) & 1u) * kZDecFloats);
+        const int n4 = p.rank * 8;  // float4 of [rank][32]
+        const int c0 = (int)((long)blockIdx.x * n4 / gridDim.x), c1 = (int)((long)(blockIdx.x + 1) * n4 / gridDim.x);
+        for (int i = c0 + ew * 32 + lane; i < c1; i += kEcWarps * 32) zn[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (!mbar_wait_bounded(abar, 0, p.wait_ns) && lane == 0) atomicOr(&p.sync->status, kStatusTimeoutPipe);
+      ec_project<MT>(p, zc, ew, lane, abuf_s);
       // Every lane's additions into z are visible device-wide before the
       // CTA's single arrival (release) on the grid-wide counter.
       __threadfence();
       ec_bar();
       if (ew == 0 && lane == 0) {
-        if (!p.skip_arrive) atomicAdd(&p.sync->arrive, 1u);
-        const unsigned target = gridDim.x;
-        bool arrived = ld_acquire_gpu(&p.sync->arrive) >= target;
+        const unsigned target = (ep + 1u) * gridDim.x;
+        if (!p.skip_arrive) {
+          const unsigned old = atomicAdd(&p.sync->arrive_acc, 1u);
+          if (old == target - 1u) p.sync->epoch = ep + 1u;  // last to arrive: every CTA has read epoch
+        }
+        auto reached = [&]() { return (int)(ld_acquire_gpu(&p.sync->arrive_acc) - target) >= 0; };
+        bool arrived = reached();
         if (!arrived) {
           const uint64_t t0 = globaltimer();
-          while (!(arrived = ld_acquire_gpu(&p.sync->arrive) >= target)) {
+          while (!(arrived = reached())) {
             if (globaltimer() - t0 > p.wait_ns) break;
             __nanosleep(64);  // one poller per CTA, spaced out on the counter's L2 line
           }
@@ -343,7 +397,7 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
       ec_bar();
       const bool arrived = *ec_flag != 0;
       if (p.gate == SPEAR_GATE_MLP) {
-        ec_u_mlp<Mp>(p, arrived, ew * 32 + lane, zs_mlp, zs_mlp + p.M * p.rank, uh, ul, us);
+        ec_u_mlp<Mp>(p, zc, arrived, ew * 32 + lane, zs_mlp, zs_mlp + p.M * p.rank, uh, ul, us);
       } else {
         // u = alpha * gamma(z) * z for 4 tokens per float4 of z ([rank][32] fp32).
         // Kept compact (two loads in flight, fast exp and division for the
@@ -353,7 +407,7 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
 #pragma unroll 2
         for (int idx = ew * 32 + lane; idx < nv; idx += kEcWarps * 32) {
           const int j = idx / (Mp / 4), m0 = (idx % (Mp / 4)) * 4;
-          const float4 v = arrived ? __ldcg(reinterpret_cast<const float4*>(p.z + j * 32 + m0))
+          const float4 v = arrived ? __ldcg(reinterpret_cast<const float4*>(zc + j * 32 + m0))
                                    : make_float4(0.f, 0.f, 0.f, 0.f);
           const float zz[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -369,30 +423,6 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(ubar);  // release: this warp's share of u is visible to the consumers
-      // The last CTA (over the grid) to have read z clears it and the counters
-      // for the next call. Every load of z in this CTA has returned (its value
-      // is in shared memory), so one release fence orders them before the
-      // departure; the clearing stores need no fence of their own, as the next
-      // call touches z only after its grid-dependency wait, i.e. after this
-      // grid has completed.
-      ec_bar();
-      if (ew == 0) {
-        int last = 0;
-        if (lane == 0 && arrived) {
-          __threadfence();
-          last = atomicAdd(&p.sync->depart, 1u) == gridDim.x - 1;
-        }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-          __threadfence();  // acquire: every other CTA's reads of z precede the clearing
-          for (int idx = lane; idx < p.rank * 8; idx += 32)
-            reinterpret_cast<float4*>(p.z)[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (lane == 0) {
-            p.sync->arrive = 0;
-            p.sync->depart = 0;
-          }
-        }
-      }
     }
     return;
   }
@@ -732,7 +762,7 @@ spear_status_t spear_launch_decode(spear_linear_s* h, const __nv_bfloat16* x, __
   p.b_frag = h->b_dec;
   p.x = x;
   p.y = y;
-  p.z = h->z_dec;
+  p.z = h->z_mma;
   p.sync = h->sync;
   p.K = h->K;
   p.N = h->N;
@@ -758,7 +788,7 @@ spear_status_t spear_launch_decode(spear_linear_s* h, const __nv_bfloat16* x, __
   const size_t u_bytes = ec ? (size_t)2 * Mp * (h->rank + 8) * 2 : 0;
   const size_t mlp_bytes = h->gate_hidden > 0 ? (size_t)M * (h->rank + h->gate_hidden) * 4 : 0;
   const size_t pc_bytes = h->per_channel ? (size_t)P * 64 : 0;
-  const size_t b_bytes = ec ? (size_t)P * (h->rank / 16) * 512 + 16 : 0;
+  const size_t b_bytes = ec ? (size_t)P * (h->rank / 16) * 512 + 16 + (size_t)kEcSmemUnits * 4096 : 0;
   // barriers, alignment slack, per-channel words, u (hi and lo)
   const size_t fixed = kBarrierBytes + 1024 + pc_bytes + u_bytes + mlp_bytes + b_bytes;
   const size_t budget = kSmemCap > fixed ? kSmemCap - fixed : 0;

@@ -69,6 +69,7 @@ struct spear_linear_s {
   void* ws = nullptr;
   spear::SyncWords* sync = nullptr;
   float* z_dec = nullptr;
+  float* z_mma = nullptr;            // warp-MMA decode: z [2][256][32] fp32, alternating by call
   float* z_pre = nullptr;            // [max_tokens][rank] fp32 (prefill projection)
   __nv_bfloat16* u_pre = nullptr;    // [max_tokens][rank] bf16 (prefill gated, alpha-scaled)
   unsigned* pre_done = nullptr;      // [ceil(max_tokens / 128)] split counters of the pre-kernel

@@ -136,8 +136,10 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
   const size_t K = h->K, r = h->rank, mt = h->max_tokens;
   const size_t pre_tiles = (mt + 127) / 128;
   const size_t y32_tc_floats = ((size_t)h->sm_count + 2 * (size_t)h->nt128) * 128 * 32;
-  const size_t ws_bytes = sizeof(spear::SyncWords) + kZDecFloats * 4 + mt * r * 4 + mt * r * 2 + pre_tiles * 4 +
-                          256 + y32_tc_floats * 4 + (size_t)h->nt128 * 4 + 256;
+  const size_t ws_base = sizeof(spear::SyncWords) + kZDecFloats * 4 + mt * r * 4 + mt * r * 2 + pre_tiles * 4 +
+                         256 + y32_tc_floats * 4 + (size_t)h->nt128 * 4 + 256;
+  const size_t z_mma_off = (ws_base + 127) / 128 * 128;
+  const size_t ws_bytes = z_mma_off + 2 * kZDecFloats * 4;
   h->ws_bytes = ws_bytes;
   cudaError_t e = cudaSuccess;
   auto A = [&](cudaError_t x) {
@@ -169,6 +171,7 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
   char* w = static_cast<char*>(h->ws);
   h->sync = reinterpret_cast<spear::SyncWords*>(w);
   h->z_dec = reinterpret_cast<float*>(w + sizeof(spear::SyncWords));
+  h->z_mma = reinterpret_cast<float*>(w + z_mma_off);
   h->z_pre = h->z_dec + kZDecFloats;
   h->u_pre = reinterpret_cast<__nv_bfloat16*>(h->z_pre + mt * r);
   h->pre_done = reinterpret_cast<unsigned*>(h->u_pre + mt * r);
