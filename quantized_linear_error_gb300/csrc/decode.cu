@@ -322,6 +322,18 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
         for (int j = 0; j < ns; ++j) bulk_g2s_shared_u32(abuf_s + j * 4096, ec_unit_ptr(p, u0 + j), 4096, abar);
       }
       issue_weights(0);
+      // CTAs start in block order as SMs free up, so high-numbered ones tend
+      // to start last, when the previous grid ends; warm L2 with the first two
+      // stages of the CTA half a grid away, whose own loads would otherwise
+      // start only then. Measured worth it only with more than two stages:
+      // on shorter calls the extra L2 traffic delays the compensator's
+      // round trips more than it saves.
+      if (p.n_stages > 2) {
+        const int pb = (int)((blockIdx.x + gridDim.x / 2) % gridDim.x);
+        for (int i = 0; i < 2; ++i)
+          prefetch_l2(p.wq + L.run_offset(pb, i * (KC / kDecodeRun)),
+                      (unsigned)(L.pc(pb) * L.stage_tile_bytes(min(KC, K - i * KC))));
+      }
       asm volatile("griddepcontrol.wait;" ::: "memory");
       issue_x(0);
       for (int i = 1; i < prefetch; ++i) {
