@@ -35,7 +35,6 @@ namespace {
 
 constexpr int kMaxStages = 8;
 constexpr int kEcWarps = 4;  // compensator warps per CTA
-constexpr int kEcSmemUnits = 4;  // units of the CTA's share of A staged in shared memory (4 KB each)
 constexpr int kBarrierBytes = 1024;
 constexpr size_t kSmemCap = 200 * 1024;
 
@@ -117,15 +116,13 @@ SPEAR_DEVINL const uint4* ec_unit_ptr(const DecodeParams& p, int ua) {
   return p.a_frag + ((size_t)(ua / kb128) * (p.K / 16) + (ua % kb128) * 8) * 32;
 }
 
-// A does not depend on the previous kernel: the producer copies the first
-// kEcSmemUnits units of the share into shared memory ahead of the weights;
-// pull this warp's remaining units into L2 before waiting for x.
+// A does not depend on the previous kernel: pull this warp's units of it into
+// L2 before waiting for x.
 SPEAR_DEVINL void ec_prefetch(const DecodeParams& p, int ew, int lane) {
   int u0, u1;
   ec_share(p, u0, u1);
   if (lane == 0)
-    for (int ua = u0 + ew; ua < u1; ua += kEcWarps)
-      if (ua - u0 >= kEcSmemUnits) prefetch_l2(ec_unit_ptr(p, ua), 8 * 32 * 16);
+    for (int ua = u0 + ew; ua < u1; ua += kEcWarps) prefetch_l2(ec_unit_ptr(p, ua), 8 * 32 * 16);
 }
 
 // Bottleneck-MLP gate ("SPEAR", section 2.1A: gamma is a bottleneck MLP):
@@ -188,21 +185,19 @@ SPEAR_DEVINL void ec_u_mlp(const DecodeParams& p, const float* z, bool arrived, 
 
 // z += A[:, this CTA's share] x, via warp MMA with A rows as the M side.
 template <int MT>
-SPEAR_DEVINL void ec_project(const DecodeParams& p, float* z, int ew, int lane, uint32_t abuf_s) {
+SPEAR_DEVINL void ec_project(const DecodeParams& p, float* z, int ew, int lane) {
   const int kb128 = p.K / 128;
   int u0, u1;
   ec_share(p, u0, u1);
   const int g = lane >> 2, tq = lane & 3;
   for (int ua = u0 + ew; ua < u1; ua += kEcWarps) {
     const int at = ua / kb128, kb = ua % kb128;
-    const bool staged = ua - u0 < kEcSmemUnits;
     const uint4* ag = ec_unit_ptr(p, ua) + lane;
-    const uint32_t as = abuf_s + (uint32_t)(((ua - u0) * 256 + lane) * 16);
     float c[2][MT][4] = {};
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       const int k16 = kb * 8 + kk;
-      const uint4 af = staged ? lds128(as + kk * 512) : __ldg(ag + kk * 32);
+      const uint4 af = __ldg(ag + kk * 32);
       const uint32_t a[4] = {af.x, af.y, af.z, af.w};
 #pragma unroll
       for (int n = 0; n < MT; ++n) {
@@ -239,7 +234,6 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
   uint64_t* szbar = full + 32;
   uint64_t* ubar = full + 33;  // compensator warp -> consumers: u is in shared memory
   uint64_t* bbar = full + 34;  // B fragments of this CTA's tiles are in shared memory
-  uint64_t* abar = full + 35;  // the staged units of this CTA's share of A are in shared memory
   // stage buffers start on a 1024-byte boundary (the swizzle pattern of the x
   // box is defined on absolute shared-memory address bits)
   const uint32_t s0 = smem_u32(smem + kBarrierBytes);
@@ -252,8 +246,6 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
   // B fragments of this CTA's tiles [Pc][rank / 16][32] uint4 (16-byte aligned)
   const uint32_t bbuf_s =
       (smem_u32(zs_mlp + (p.gh > 0 ? p.M * (p.rank + p.gh) : 0)) + 15u) & ~15u;
-  // staged units of A [kEcSmemUnits][8][32] uint4, after the B fragments
-  const uint32_t abuf_s = bbuf_s + (uint32_t)(p.P * (p.rank / 16) * 512);
 
   const uint32_t stages_s = smem_u32(stages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -273,7 +265,6 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
     mbar_init(szbar, 1);
     mbar_init(ubar, kEcWarps);
     mbar_init(bbar, 1);
-    mbar_init(abar, 1);
     fence_mbar_init();
   }
   // Token rows M..Mp-1 of the staged x boxes are zero-filled by the copy
@@ -296,9 +287,9 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
       // Weights and compensator factors are constant since create, x may be
       // produced by the previous kernel. The CTA that lands on the SM freed
       // last by the previous grid reaches the wait only after the issues made
-      // before it, so before it go only the first stage's weights (and the
-      // staged units of A); right after it, the first stage's x, then the
-      // other stages and the B fragments.
+      // before it, so before it go only the first stage's weights; right
+      // after it, the first stage's x, then the other stages and the B
+      // fragments. (Staging A here as well was measured to delay the wait.)
       const int prefetch = min(p.NS, p.n_stages);
       auto issue_weights = [&](int i) {
         const int slot = i % p.NS;
@@ -312,15 +303,6 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
         tma_load_3d(stages + (size_t)slot * p.stage_bytes, &xmap, 0, 0, i * (KC / 64), &full[slot]);
       };
       prefetch_tensormap(&xmap);
-      if (EC) {
-        // the first units of this CTA's share of A, ahead of the weights: the
-        // projection they feed is on the path to every CTA's final result
-        int u0, u1;
-        ec_share(p, u0, u1);
-        const int ns = min(u1 - u0, kEcSmemUnits);
-        mbar_arrive_expect_tx(abar, (unsigned)(ns * 4096));
-        for (int j = 0; j < ns; ++j) bulk_g2s_shared_u32(abuf_s + j * 4096, ec_unit_ptr(p, u0 + j), 4096, abar);
-      }
       issue_weights(0);
       // CTAs start in block order as SMs free up, so high-numbered ones tend
       // to start last, when the previous grid ends; warm L2 with the first two
@@ -381,8 +363,7 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
         const int c0 = (int)((long)blockIdx.x * n4 / gridDim.x), c1 = (int)((long)(blockIdx.x + 1) * n4 / gridDim.x);
         for (int i = c0 + ew * 32 + lane; i < c1; i += kEcWarps * 32) zn[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      if (!mbar_wait_bounded(abar, 0, p.wait_ns) && lane == 0) atomicOr(&p.sync->status, kStatusTimeoutPipe);
-      ec_project<MT>(p, zc, ew, lane, abuf_s);
+      ec_project<MT>(p, zc, ew, lane);
       // Every lane's additions into z are visible device-wide before the
       // CTA's single arrival (release) on the grid-wide counter.
       __threadfence();
@@ -800,7 +781,7 @@ spear_status_t spear_launch_decode(spear_linear_s* h, const __nv_bfloat16* x, __
   const size_t u_bytes = ec ? (size_t)2 * Mp * (h->rank + 8) * 2 : 0;
   const size_t mlp_bytes = h->gate_hidden > 0 ? (size_t)M * (h->rank + h->gate_hidden) * 4 : 0;
   const size_t pc_bytes = h->per_channel ? (size_t)P * 64 : 0;
-  const size_t b_bytes = ec ? (size_t)P * (h->rank / 16) * 512 + 16 + (size_t)kEcSmemUnits * 4096 : 0;
+  const size_t b_bytes = ec ? (size_t)P * (h->rank / 16) * 512 + 16 : 0;
   // barriers, alignment slack, per-channel words, u (hi and lo)
   const size_t fixed = kBarrierBytes + 1024 + pc_bytes + u_bytes + mlp_bytes + b_bytes;
   const size_t budget = kSmemCap > fixed ? kSmemCap - fixed : 0;
