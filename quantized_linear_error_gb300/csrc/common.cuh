@@ -127,6 +127,11 @@ SPEAR_DEVINL void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Warm L2 with the 128-byte line holding p (an ordinary load-path prefetch).
+SPEAR_DEVINL void prefetch_l2_line(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
 // Warm L2 with [src, src + bytes) (16-byte aligned, multiple of 16 bytes).
 SPEAR_DEVINL void prefetch_l2(const void* src, unsigned bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");

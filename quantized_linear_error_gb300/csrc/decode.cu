@@ -117,12 +117,14 @@ SPEAR_DEVINL const uint4* ec_unit_ptr(const DecodeParams& p, int ua) {
 }
 
 // A does not depend on the previous kernel: pull this warp's units of it into
-// L2 before waiting for x.
+// L2 before waiting for x, one 128-byte line per lane and unit through the
+// load path (a bulk prefetch would queue behind the weight copies of the
+// copy engine and hold this warp back from its dependency wait).
 SPEAR_DEVINL void ec_prefetch(const DecodeParams& p, int ew, int lane) {
   int u0, u1;
   ec_share(p, u0, u1);
-  if (lane == 0)
-    for (int ua = u0 + ew; ua < u1; ua += kEcWarps) prefetch_l2(ec_unit_ptr(p, ua), 8 * 32 * 16);
+  for (int ua = u0 + ew; ua < u1; ua += kEcWarps)
+    prefetch_l2_line(reinterpret_cast<const uint8_t*>(ec_unit_ptr(p, ua)) + lane * 128);
 }
 
 // Bottleneck-MLP gate ("SPEAR", section 2.1A: gamma is a bottleneck MLP):
