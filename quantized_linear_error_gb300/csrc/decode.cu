@@ -395,24 +395,37 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
         ec_u_mlp<Mp>(p, zc, arrived, ew * 32 + lane, zs_mlp, zs_mlp + p.M * p.rank, uh, ul, us);
       } else {
         // u = alpha * gamma(z) * z for 4 tokens per float4 of z ([rank][32] fp32).
-        // Kept compact (two loads in flight, fast exp and division for the
-        // sigmoid, ~1e-6 relative): this code runs once per launch, and a
-        // large unrolled body here costs the consumer warps instruction fetch.
+        // Kept compact (fast exp and division for the sigmoid, ~1e-6
+        // relative): this code runs once per launch, and a large unrolled
+        // body here costs the consumer warps instruction fetch.
+        // All loads of a round of four float4 per thread are issued before
+        // any use, so that a round costs one L2 round trip.
         const int nv = p.rank * (Mp / 4);
-#pragma unroll 2
-        for (int idx = ew * 32 + lane; idx < nv; idx += kEcWarps * 32) {
-          const int j = idx / (Mp / 4), m0 = (idx % (Mp / 4)) * 4;
-          const float4 v = arrived ? __ldcg(reinterpret_cast<const float4*>(zc + j * 32 + m0))
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-          const float zz[4] = {v.x, v.y, v.z, v.w};
+        constexpr int kR = 4;
+        for (int base = ew * 32 + lane; base < nv; base += kR * kEcWarps * 32) {
+          float4 v[kR];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float g = p.gate == SPEAR_GATE_ONE ? 1.0f : __fdividef(1.0f, 1.0f + __expf(-zz[e]));
-            const float uval = (m0 + e < p.M) ? p.alpha * zz[e] * g : 0.f;
-            __nv_bfloat16 hi, lo;
-            split_bf16(uval, hi, lo);
-            uh[(m0 + e) * us + j] = hi;
-            ul[(m0 + e) * us + j] = lo;
+          for (int r = 0; r < kR; ++r) {
+            const int idx = base + r * kEcWarps * 32;
+            const int j = idx / (Mp / 4), m0 = (idx % (Mp / 4)) * 4;
+            v[r] = (arrived && idx < nv) ? __ldcg(reinterpret_cast<const float4*>(zc + j * 32 + m0))
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int r = 0; r < kR; ++r) {
+            const int idx = base + r * kEcWarps * 32;
+            if (idx >= nv) break;
+            const int j = idx / (Mp / 4), m0 = (idx % (Mp / 4)) * 4;
+            const float zz[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float g = p.gate == SPEAR_GATE_ONE ? 1.0f : __fdividef(1.0f, 1.0f + __expf(-zz[e]));
+              const float uval = (m0 + e < p.M) ? p.alpha * zz[e] * g : 0.f;
+              __nv_bfloat16 hi, lo;
+              split_bf16(uval, hi, lo);
+              uh[(m0 + e) * us + j] = hi;
+              ul[(m0 + e) * us + j] = lo;
+            }
           }
         }
       }
