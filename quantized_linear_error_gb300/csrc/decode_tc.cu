@@ -181,12 +181,11 @@ SPEAR_DEVINL void ec_project(const TcParams& p, int ew, int lane) {
 #pragma unroll
       for (int n = 0; n < MT; ++n) {
         const int tok = 8 * n + g;
-        uint32_t b0 = 0, b1 = 0;
-        if (tok < p.M) {
-          const uint32_t* xr = reinterpret_cast<const uint32_t*>(p.x + (size_t)tok * p.K + k16 * 16 + 2 * tq);
-          b0 = __ldg(xr);
-          b1 = __ldg(xr + 4);
-        }
+        // A's columns are in the quad order of the layout: lane tq takes
+        // channels 4 tq .. 4 tq + 3 of the step, one 8-byte load
+        uint2 bx = make_uint2(0u, 0u);
+        if (tok < p.M) bx = __ldg(reinterpret_cast<const uint2*>(p.x + (size_t)tok * p.K + k16 * 16 + 4 * tq));
+        const uint32_t b0 = bx.x, b1 = bx.y;
         mma_bf16_16816(c[kk & 1][n], a, b0, b1);
       }
     }

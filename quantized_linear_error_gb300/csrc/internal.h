@@ -31,7 +31,8 @@
 // pipeline stage of any whole number of runs is a single bulk copy.
 //   wq_dec  bytes, nt16 * dec_tile_bytes
 //   sz_dec  u32 [nt16][16] (per-channel only)
-//   a_dec   uint4 [rank/16][K/16][32]    A in A-fragment order (bf16 pairs)
+//   a_dec   uint4 [rank/16][K/16][32]    A in A-fragment order (bf16 pairs), the 16 columns
+//                                         of a k16 step in quad order (lane t: 4t .. 4t + 3)
 //   b_dec   uint4 [nt16][rank/16][32]    B in A-fragment order (bf16 pairs)
 //
 // Prefill layout (row-major 16-byte chunks for the tensor-core tile loader).

@@ -85,7 +85,11 @@ __global__ void repack_sz(const uint16_t* __restrict__ s, const uint8_t* __restr
 }
 
 // bf16 matrix [rows][cols] into m16n8k16 A-fragment order [rows/16][cols/16][32] uint4.
-__global__ void repack_frag(const uint16_t* __restrict__ m, int rows, int cols, int row_tiles,
+// With `quad`, the 16 columns of a k16 step are taken in the order that gives
+// lane t the four consecutive columns 4t .. 4t + 3 (fragment columns 2t, 2t + 1,
+// 2t + 8, 2t + 9), so that the matching B fragment of a row-major activation is
+// one 8-byte load (the compensator's down-projection A).
+__global__ void repack_frag(const uint16_t* __restrict__ m, int rows, int cols, int row_tiles, bool quad,
                             uint4* __restrict__ out) {
   const int ks = cols / 16;
   const long total = (long)row_tiles * ks * 32;
@@ -95,10 +99,11 @@ __global__ void repack_frag(const uint16_t* __restrict__ m, int rows, int cols, 
     const int tile = i / (32L * ks);
     const int g = lane >> 2, t = lane & 3;
     const int r0 = tile * 16 + g, r1 = r0 + 8;
-    const int k = kk * 16 + 2 * t;
+    const int k = kk * 16 + (quad ? 4 * t : 2 * t);
+    const int k2 = quad ? k + 2 : k + 8;  // columns of registers 2 and 3
     auto at = [&](int r, int c) -> uint32_t { return r < rows ? (uint32_t)m[(size_t)r * cols + c] : 0u; };
     out[i] = make_uint4(at(r0, k) | at(r0, k + 1) << 16, at(r1, k) | at(r1, k + 1) << 16,
-                        at(r0, k + 8) | at(r0, k + 9) << 16, at(r1, k + 8) | at(r1, k + 9) << 16);
+                        at(r0, k2) | at(r0, k2 + 1) << 16, at(r1, k2) | at(r1, k2 + 1) << 16);
   }
 }
 
@@ -218,9 +223,9 @@ spear_status_t spear_build_layouts(spear_linear_s* h, const spear_linear_desc_t*
     const uint16_t* A = static_cast<const uint16_t*>(d->A);
     const uint16_t* B = static_cast<const uint16_t*>(d->B);
     n = (long)(r / 16) * (K / 16) * 32;
-    repack_frag<<<grid_for(n, T), T, 0, st>>>(A, r, K, r / 16, h->a_dec);
+    repack_frag<<<grid_for(n, T), T, 0, st>>>(A, r, K, r / 16, true, h->a_dec);
     n = (long)h->nt16 * (r / 16) * 32;
-    repack_frag<<<grid_for(n, T), T, 0, st>>>(B, N, r, h->nt16, h->b_dec);
+    repack_frag<<<grid_for(n, T), T, 0, st>>>(B, N, r, h->nt16, false, h->b_dec);
     n = (long)r * K;
     copy_pad_rows<<<grid_for(n, T), T, 0, st>>>(A, r, r, K, reinterpret_cast<uint16_t*>(h->a_pre));
     n = (long)h->nt128 * 128 * r;
