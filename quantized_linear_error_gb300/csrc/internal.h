@@ -71,6 +71,8 @@ struct spear_linear_s {
   spear::SyncWords* sync = nullptr;
   float* z_dec = nullptr;
   float* z_mma = nullptr;            // warp-MMA decode: z [2][256][32] fp32, alternating by call
+  float* part = nullptr;             // prefill split over K: fp32 partial tiles, at most [sm_count][256][128]
+  unsigned* part_cnt = nullptr;      // prefill split over K: [sm_count] splits finished per tile
   float* z_pre = nullptr;            // [max_tokens][rank] fp32 (prefill projection)
   __nv_bfloat16* u_pre = nullptr;    // [max_tokens][rank] bf16 (prefill gated, alpha-scaled)
   unsigned* pre_done = nullptr;      // [ceil(max_tokens / 128)] split counters of the pre-kernel

@@ -25,6 +25,7 @@
 // warp 1 issues tcgen05.mma (one thread), warps 2-5 dequantise and then run
 // the epilogue (warp w reads TMEM lanes 32 (w % 4) .. + 31). Every mbarrier
 // wait is bounded; a timeout latches the handle's status word.
+#include <algorithm>
 #include <cstring>
 
 #include "internal.h"
@@ -70,6 +71,12 @@ struct GemmParams {
   float* zacc;          // pre-kernel: fp32 [M][rank] partial sums of z (zero between calls)
   unsigned* tile_done;  // pre-kernel: per 128-token tile, splits finished
   int splits;
+  // main kernel split over K (gridDim.z splits of kps K blocks; the last one
+  // also runs the compensator K-tail): fp32 partial tiles
+  // part [split][tile][128][TN] and per-tile counters of finished splits
+  int kps;
+  float* part;
+  unsigned* part_cnt;
 };
 
 SPEAR_DEVINL void fail(const GemmParams& p) { atomicOr(p.status, kStatusTimeoutPipe); }
@@ -131,17 +138,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full_tma + 16;
   uint64_t* acc_full = full_tma + 24;
   uint64_t* a_empty = full_tma + 25;  // main kernel: A ring in tensor memory free again
+  uint64_t* part_bar = full_tma + 32;  // main kernel split over K: the other splits' partials are in smem
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 384);
   uint8_t* stages = smem + kBarrierBytes;
   const uint32_t stages_s = smem_u32(stages);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a0 = blockIdx.x * 128;
-  // main kernel: blockIdx.y is the token tile; pre-kernel: the K split
+  // main kernel: blockIdx.y is the token tile, blockIdx.z the K split;
+  // pre-kernel: blockIdx.y is the K split
   const int b0 = EPI == 2 ? 0 : blockIdx.y * p.TN;
-  const int kb0 = EPI == 2 ? blockIdx.y * p.kblocks : 0;
-  const int kmain = EPI == 2 ? min(p.kblocks, p.kb_total - kb0) : p.kblocks;
-  const int total = kmain + p.tail_blocks;
+  const int kb0 = EPI == 2 ? blockIdx.y * p.kblocks : (DEQ ? blockIdx.z * p.kps : 0);
+  const int kmain = EPI == 2 ? min(p.kblocks, p.kb_total - kb0) : (DEQ ? min(p.kps, p.kb_total - kb0) : p.kblocks);
+  const int tail = (DEQ && blockIdx.z + 1 != gridDim.z) ? 0 : p.tail_blocks;
+  const int total = kmain + tail;
   volatile int& last_split = *reinterpret_cast<volatile int*>(smem + 512);
 
   if (threadIdx.x == 0) {
@@ -154,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&a_empty[s], 1);
     }
     mbar_init(acc_full, 1);
+    mbar_init(part_bar, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -172,14 +183,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   // compensator it waits for its predecessor here. Either kernel lets the
   // next one launch early; the next one waits for it before reading anything
   // it writes.
-  const bool late_wait = DEQ && p.tail_blocks > 0;
+  const bool late_wait = DEQ && tail > 0;
   if (!late_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
-      if (DEQ && p.tail_blocks > 0) prefetch_l2(p.bt + (size_t)a0 * p.rank, 128u * p.rank * 2u);
+      if (DEQ && tail > 0) prefetch_l2(p.bt + (size_t)a0 * p.rank, 128u * p.rank * 2u);
       for (int it = 0; it < total; ++it) {
         const int s = it % p.NS;
         if (it >= p.NS && !mbar_wait_bounded(&empty[s], ((it / p.NS) - 1) & 1, p.wait_ns)) {
@@ -193,9 +204,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it < kmain) {
           if constexpr (DEQ) {
             mbar_arrive_expect_tx(&full_tma[s], kRawBytes + p.b_bytes);
-            bulk_g2s(raw, p.wq + ((size_t)blockIdx.x * p.kblocks + it) * 1024, kRawWBytes, &full_tma[s]);
-            bulk_g2s(raw + kRawWBytes, p.sz + ((size_t)blockIdx.x * p.n_groups + (it * 64) / p.G) * 128, 512,
-                     &full_tma[s]);
+            bulk_g2s(raw, p.wq + ((size_t)blockIdx.x * p.kb_total + kb0 + it) * 1024, kRawWBytes, &full_tma[s]);
+            bulk_g2s(raw + kRawWBytes, p.sz + ((size_t)blockIdx.x * p.n_groups + ((kb0 + it) * 64) / p.G) * 128,
+                     512, &full_tma[s]);
           } else {
             mbar_arrive_expect_tx(&full_tma[s], kATileBytes + p.b_bytes);
             tma_load_2d(A, &mapA, (kb0 + it) * 64, a0, &full_tma[s]);
@@ -316,19 +327,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------------------------------------------------- epilogue
-    const bool ok = mbar_wait_bounded(acc_full, 0, 4 * p.wait_ns);
+    bool ok = mbar_wait_bounded(acc_full, 0, 4 * p.wait_ns);
     if (!ok && lane == 0) fail(p);
     tc_fence_after_sync();
     const int q = warp & 3;
     const int row = a0 + 32 * q + lane;
+    // Split over K (main kernel): splits 0 .. S-2 store their fp32 partial
+    // tile ([column][row]) and count themselves done; split S-1, which also
+    // ran the compensator K-tail, waits for that count, pulls the S-1
+    // partials into its now idle stage memory with one bulk copy each, and
+    // adds them in split order to its own accumulator before the single
+    // rounding to bf16. (A last-arriver pass that re-read every partial
+    // through the load path was latency-bound.)
+    const bool split = EPI == 0 && gridDim.z > 1;
+    const bool leader = split && blockIdx.z + 1 == gridDim.z;
+    const unsigned tile_id = blockIdx.y * gridDim.x + blockIdx.x;
+    const size_t part_tile = (size_t)p.TN * 128;  // floats of one partial tile
+    if (leader) {
+      if (threadIdx.x == 64) {
+        bool got = false;
+        if (ok) {
+          const unsigned want = gridDim.z - 1;
+          const uint64_t t0 = globaltimer();
+          while (!(got = ld_acquire_gpu(&p.part_cnt[tile_id]) >= want)) {
+            if (globaltimer() - t0 > 4 * p.wait_ns) break;
+            __nanosleep(64);
+          }
+          if (!got) fail(p);
+        }
+        last_split = got ? 1 : 0;
+        if (got) {
+          p.part_cnt[tile_id] = 0;  // every other split has counted itself: reset for the next call
+          mbar_arrive_expect_tx(part_bar, (unsigned)(part_tile * 4 * (gridDim.z - 1)));
+          for (unsigned z = 0; z + 1 < gridDim.z; ++z)
+            bulk_g2s(stages + z * part_tile * 4, p.part + ((size_t)z * gridDim.x * gridDim.y + tile_id) * part_tile,
+                     (unsigned)(part_tile * 4), part_bar);
+        }
+      }
+      epilogue_bar();
+      ok = last_split != 0 && mbar_wait_bounded(part_bar, 0, 4 * p.wait_ns);
+      if (last_split != 0 && !ok && lane == 0) fail(p);
+    }
     if (ok) {
       for (int c0 = 0; c0 < p.TN; c0 += 16) {
         uint32_t v[16];
         tmem_ld_x16(tmem_d + ((uint32_t)(32 * q) << 16) + c0, v);
         tmem_ld_wait();
         if constexpr (EPI == 0) {
-          // y[m][n]: lane = n, columns = tokens
-          if (row < p.a_rows) {
+          if (split && !leader) {
+            // this split's fp32 partial tile, [column][row], so that a warp's
+            // 32 rows of one column are 128 contiguous bytes
+            float* dst = p.part + ((size_t)blockIdx.z * gridDim.x * gridDim.y + tile_id) * part_tile +
+                         (size_t)c0 * 128 + 32 * q + lane;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) __stcg(dst + j * 128, __uint_as_float(v[j]));
+          } else if (row < p.a_rows) {
+            if (leader) {
+              // add the other splits' partials, in split order, from shared memory
+              const float* ps = reinterpret_cast<const float*>(stages) + (size_t)c0 * 128 + 32 * q + lane;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                float a = __uint_as_float(v[j]);
+                for (unsigned z = 0; z + 1 < gridDim.z; ++z) a = ps[z * part_tile + j * 128] + a;
+                v[j] = __float_as_uint(a);
+              }
+            }
+            // y[m][n]: lane = n, columns = tokens
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int m = b0 + c0 + j;
@@ -358,6 +422,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+    }
+    if (split && !leader) {
+      // publish this split's partial tile to the leader
+      __threadfence();
+      epilogue_bar();
+      if (threadIdx.x == 64 && ok) atomicAdd(&p.part_cnt[tile_id], 1u);
     }
     if constexpr (EPI == 2) {
       // The last split of this 128-token tile applies the gate to the complete z,
@@ -503,6 +573,7 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
   CUtensorMap none;
   memset(&none, 0, sizeof none);
   cudaError_t e;
+  int pre_ctas = 0;  // CTAs of the compensator pre-kernel
 
   if (r > 0) {
     // ---- compensator projection and gate: u' [M][r]
@@ -550,6 +621,7 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
     }
     p.tmem_cols = tmem_cols_for(r);
     const size_t smem = kBarrierBytes + 1024 + (size_t)p.NS * p.stage_bytes;
+    pre_ctas = mt * splits;
     e = launch<false, 2>(p, dim3(mt, splits), smem, stream, mx, ma, none, none);
     if (e != cudaSuccess) return SPEAR_ERR_CUDA;
   }
@@ -564,8 +636,22 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
     mut = none;
   }
   GemmParams p{};
-  p.kblocks = K / 64;
-  p.kb_total = K / 64;
+  const int kbt = K / 64, ntt = (M + TN - 1) / TN, tiles = h->nt128 * ntt;
+  // Split K when the tiles fill less than one wave of CTAs (one per SM): up to
+  // four splits of at least eight K blocks, with the (split, tile) pairs and
+  // the compensator pre-kernel's CTAs, which run alongside, within the SMs.
+  int ks = 1;
+  const int avail = h->sm_count - pre_ctas;
+  if (h->part && tiles < avail) {
+    ks = std::min(std::min(4, avail / tiles), kbt / 8);
+    if (ks < 1) ks = 1;
+  }
+  p.kps = (kbt + ks - 1) / ks;
+  ks = (kbt + p.kps - 1) / p.kps;
+  p.part = h->part;
+  p.part_cnt = h->part_cnt;
+  p.kblocks = kbt;
+  p.kb_total = kbt;
   p.splits = 1;
   p.tail_blocks = (r + 63) / 64;
   p.TN = TN;
@@ -589,8 +675,14 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
   p.raw_bytes = kRawBytes;
   p.stage_bytes = (p.a_bytes + p.b_bytes + kRawBytes + 1023) / 1024 * 1024;
   p.NS = stages_for(p.stage_bytes);
+  // the split leader pulls the other splits' partial tiles into the stage area
+  while (ks > 1 && (size_t)(ks - 1) * TN * 512 > (size_t)p.NS * p.stage_bytes) {
+    --ks;
+    p.kps = (kbt + ks - 1) / ks;
+    ks = (kbt + p.kps - 1) / p.kps;
+  }
   p.tmem_cols = 512;  // accumulator (TN <= 256 columns) + the A ring from column 256
   const size_t smem = kBarrierBytes + 1024 + (size_t)p.NS * p.stage_bytes;
-  e = launch<true, 0>(p, dim3(h->nt128, (M + TN - 1) / TN), smem, stream, none, mx, none, mut);
+  e = launch<true, 0>(p, dim3(h->nt128, ntt, ks), smem, stream, none, mx, none, mut);
   return e == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
 }

@@ -139,7 +139,14 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
   const size_t ws_base = sizeof(spear::SyncWords) + kZDecFloats * 4 + mt * r * 4 + mt * r * 2 + pre_tiles * 4 +
                          256 + y32_tc_floats * 4 + (size_t)h->nt128 * 4 + 256;
   const size_t z_mma_off = (ws_base + 127) / 128 * 128;
-  const size_t ws_bytes = z_mma_off + 2 * kZDecFloats * 4;
+  // Prefill splits K when its tiles fill less than one wave: at most sm_count
+  // (split, tile) pairs of 128 rows x 256 tokens in fp32, for handles sized
+  // for more than decode token counts.
+  const bool want_part = mt > (size_t)kDecodeMaxTokens;
+  const size_t part_off = z_mma_off + 2 * kZDecFloats * 4;
+  const size_t part_floats = want_part ? (size_t)h->sm_count * 128 * 256 : 0;
+  const size_t cnt_off = part_off + part_floats * 4;
+  const size_t ws_bytes = cnt_off + (size_t)h->sm_count * 4;
   h->ws_bytes = ws_bytes;
   cudaError_t e = cudaSuccess;
   auto A = [&](cudaError_t x) {
@@ -172,6 +179,8 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
   h->sync = reinterpret_cast<spear::SyncWords*>(w);
   h->z_dec = reinterpret_cast<float*>(w + sizeof(spear::SyncWords));
   h->z_mma = reinterpret_cast<float*>(w + z_mma_off);
+  h->part = want_part ? reinterpret_cast<float*>(w + part_off) : nullptr;
+  h->part_cnt = reinterpret_cast<unsigned*>(w + cnt_off);
   h->z_pre = h->z_dec + kZDecFloats;
   h->u_pre = reinterpret_cast<__nv_bfloat16*>(h->z_pre + mt * r);
   h->pre_done = reinterpret_cast<unsigned*>(h->u_pre + mt * r);

@@ -70,3 +70,20 @@ def test_config5_linears(idx, M):
     _check(w, M, rows)
     nw = wl.LinearWeights(with_spec(w, rank=0).spec, w.q, w.s, w.z, None, None, w.outliers)
     _check(nw, M, rows)
+
+
+@pytest.mark.parametrize("M", [17, 100, 300])
+@pytest.mark.parametrize("group_size,rank", [(128, 64), (0, 32), (128, 0)])
+def test_split_over_k(M, group_size, rank):
+    """Few row tiles: the main kernel splits K (up to four splits, the last
+    one also running the compensator K-tail) and the last split to finish
+    sums the fp32 partials in split order."""
+    sp = wl.LinearSpec(f"split/g{group_size}/r{rank}", 4096, 1024, group_size, rank)
+    w = wl.make_weights(sp, 14)
+    lin = spear.from_weights(w, max_tokens=512)
+    y1 = _check(w, M, lin=lin)
+    y2 = _check(w, M, lin=lin)  # counters and partials are reused by the next call
+    if rank == 0:
+        # the partials are added in split order: repeated calls agree bit for bit
+        # (with a compensator, the pre-kernel's atomic split-K sum of z does not)
+        np.testing.assert_array_equal(y1, y2)
