@@ -356,14 +356,10 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
       // into z[epoch % 2] and clears z[(epoch + 1) % 2] for the next call (the
       // previous call, which used that buffer, has completed). The arrival
       // counter is never reset: a call is complete at (epoch + 1) * grid.
+      // (The epoch load is in flight during the projection's loads; only
+      // the additions into z wait for it.)
       const unsigned ep = __ldcg(&p.sync->epoch);
       float* zc = p.z + (ep & 1u) * kZDecFloats;
-      {
-        float4* zn = reinterpret_cast<float4*>(p.z + ((ep + 1u) & 1u) * kZDecFloats);
-        const int n4 = p.rank * 8;  // float4 of [rank][32]
-        const int c0 = (int)((long)blockIdx.x * n4 / gridDim.x), c1 = (int)((long)(blockIdx.x + 1) * n4 / gridDim.x);
-        for (int i = c0 + ew * 32 + lane; i < c1; i += kEcWarps * 32) zn[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
       ec_project<MT>(p, zc, ew, lane);
       // Every lane's additions into z are visible device-wide before the
       // CTA's single arrival (release) on the grid-wide counter.
@@ -387,6 +383,14 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
         if (!arrived) atomicOr(&p.sync->status, kStatusTimeoutZ);
         *ec_flag = arrived ? 1 : 0;
         __threadfence_block();
+      } else if (ew > 0) {
+        // While warp 0 waits for the grid, clear this CTA's slice of the
+        // other buffer (after the arrival fence, which need not wait for
+        // these stores; the next call reads it only after this grid ends).
+        float4* zn = reinterpret_cast<float4*>(p.z + ((ep + 1u) & 1u) * kZDecFloats);
+        const int n4 = p.rank * 8;  // float4 of [rank][32]
+        const int c0 = (int)((long)blockIdx.x * n4 / gridDim.x), c1 = (int)((long)(blockIdx.x + 1) * n4 / gridDim.x);
+        for (int i = c0 + (ew - 1) * 32 + lane; i < c1; i += (kEcWarps - 1) * 32) zn[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
       ec_bar();
       const bool arrived = *ec_flag != 0;
