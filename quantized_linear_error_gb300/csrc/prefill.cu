@@ -368,6 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = last_split != 0 && mbar_wait_bounded(part_bar, 0, 4 * p.wait_ns);
       if (last_split != 0 && !ok && lane == 0) fail(p);
     }
+    // main kernel: the bf16 y tile, after the leader's partials in the idle stage memory
+    const uint32_t ytile_s = stages_s + (leader ? (uint32_t)((gridDim.z - 1) * part_tile * 4) : 0u);
     if (ok) {
       for (int c0 = 0; c0 < p.TN; c0 += 16) {
         uint32_t v[16];
@@ -383,20 +385,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 16; ++j) __stcg(dst + j * 128, __uint_as_float(v[j]));
           } else if (row < p.a_rows) {
             if (leader) {
-              // add the other splits' partials, in split order, from shared memory
-              const float* ps = reinterpret_cast<const float*>(stages) + (size_t)c0 * 128 + 32 * q + lane;
+              // add the other splits' partials, in split order, from shared
+              // memory (shared-space loads, all 16 of a split in flight at once)
+              const uint32_t ps = stages_s + (uint32_t)((c0 * 128 + 32 * q + lane) * 4);
+              float acc16[16];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                float a = __uint_as_float(v[j]);
-                for (unsigned z = 0; z + 1 < gridDim.z; ++z) a = ps[z * part_tile + j * 128] + a;
-                v[j] = __float_as_uint(a);
+              for (int j = 0; j < 16; ++j) acc16[j] = 0.f;
+              for (unsigned z = 0; z + 1 < gridDim.z; ++z) {
+                uint32_t w16[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) w16[j] = lds32(ps + (uint32_t)((z * part_tile + j * 128) * 4));
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc16[j] = z == 0 ? __uint_as_float(w16[j]) : acc16[j] + __uint_as_float(w16[j]);
               }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(acc16[j] + __uint_as_float(v[j]));
             }
-            // y[m][n]: lane = n, columns = tokens
+            // y tile staged in shared memory as bf16 [token][128 rows], stored below
+            // with 16-byte vectors along n (lane = n here, columns = tokens)
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const int m = b0 + c0 + j;
-              if (m < p.b_rows) p.out[(size_t)m * p.ld_out + row] = __float2bfloat16_rn(__uint_as_float(v[j]));
+              const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(v[j]));
+              asm volatile("st.shared.b16 [%0], %1;" ::"r"(ytile_s + (uint32_t)(((c0 + j) * 128 + 32 * q + lane) * 2)),
+                           "h"(*reinterpret_cast<const unsigned short*>(&h)));
             }
           }
         } else if constexpr (EPI == 1) {
@@ -420,6 +431,23 @@ __global__ void __launch_bounds__(kThreads, 1)
               red_add_v4(dst + j, __uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
                          __uint_as_float(v[j + 3]));
           }
+        }
+      }
+    }
+    if (EPI == 0 && !(split && !leader)) {
+      // 16-byte stores of the staged tile: token m, rows a0 + 8 c8 .. + 7
+      // (the barrier is unconditional: every epilogue warp reaches it)
+      epilogue_bar();
+      const int t = threadIdx.x - 64;  // the four epilogue warps
+      for (int i = t; ok && i < p.TN * 16; i += 128) {
+        const int mm = i >> 4, c8 = i & 15;
+        const int m = b0 + mm, n0 = a0 + 8 * c8;
+        if (m < p.b_rows && n0 < p.a_rows) {
+          uint4 w;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                       : "r"(ytile_s + (uint32_t)((mm * 128 + 8 * c8) * 2)));
+          *reinterpret_cast<uint4*>(p.out + (size_t)m * p.ld_out + n0) = w;
         }
       }
     }
@@ -638,11 +666,12 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
   GemmParams p{};
   const int kbt = K / 64, ntt = (M + TN - 1) / TN, tiles = h->nt128 * ntt;
   // Split K when the tiles fill less than one wave of CTAs (one per SM): up to
-  // four splits of at least eight K blocks, with the (split, tile) pairs and
-  // the compensator pre-kernel's CTAs, which run alongside, within the SMs.
+  // four splits of at least eight K blocks, (split, tile) pairs within the
+  // SMs. Not with a compensator: its pre-kernel's CTAs run alongside, and the
+  // split that runs the K-tail waits for them (measured slower than no split).
   int ks = 1;
   const int avail = h->sm_count - pre_ctas;
-  if (h->part && tiles < avail) {
+  if (h->part && r == 0 && tiles < avail) {
     ks = std::min(std::min(4, avail / tiles), kbt / 8);
     if (ks < 1) ks = 1;
   }
@@ -675,8 +704,10 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
   p.raw_bytes = kRawBytes;
   p.stage_bytes = (p.a_bytes + p.b_bytes + kRawBytes + 1023) / 1024 * 1024;
   p.NS = stages_for(p.stage_bytes);
-  // the split leader pulls the other splits' partial tiles into the stage area
-  while (ks > 1 && (size_t)(ks - 1) * TN * 512 > (size_t)p.NS * p.stage_bytes) {
+  // the split leader pulls the other splits' partial tiles into the stage area,
+  // followed there by the bf16 y tile of the epilogue
+  if ((size_t)TN * 256 > (size_t)p.NS * p.stage_bytes) return SPEAR_ERR_UNSUPPORTED;
+  while (ks > 1 && (size_t)(ks - 1) * TN * 512 + (size_t)TN * 256 > (size_t)p.NS * p.stage_bytes) {
     --ks;
     p.kps = (kbt + ks - 1) / ks;
     ks = (kbt + p.kps - 1) / p.kps;

@@ -75,9 +75,9 @@ def test_config5_linears(idx, M):
 @pytest.mark.parametrize("M", [17, 100, 300])
 @pytest.mark.parametrize("group_size,rank", [(128, 64), (0, 32), (128, 0)])
 def test_split_over_k(M, group_size, rank):
-    """Few row tiles: the main kernel splits K (up to four splits, the last
-    one also running the compensator K-tail) and the last split to finish
-    sums the fp32 partials in split order."""
+    """Few row tiles: without a compensator the main kernel splits K (up to
+    four splits) and the last split adds the others' fp32 partials in split
+    order; with one it does not split. Both give the oracle's result."""
     sp = wl.LinearSpec(f"split/g{group_size}/r{rank}", 4096, 1024, group_size, rank)
     w = wl.make_weights(sp, 14)
     lin = spear.from_weights(w, max_tokens=512)
