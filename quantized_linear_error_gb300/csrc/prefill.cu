@@ -12,11 +12,12 @@
 //  2. Main kernel: A = W rows, dequantised in the CTA: the TMA warp brings
 //     the packed INT4 tile and its scale/zero words, four warps turn them into
 //     bf16 (q - z) * s (one rounding, the exported dequantised value), one
-//     row per thread, and write them straight into a 4-deep ring of A
-//     operands in tensor memory (tcgen05.st), so the dequantised tile never
-//     passes through shared memory; B = x tokens by TMA. After the K blocks of W
+//     row per thread, and write them straight into the stage's A slot in
+//     tensor memory (tcgen05.st; one slot per pipeline stage), so the
+//     dequantised tile never passes through shared memory; B = x tokens by
+//     TMA. After the K blocks of W
 //     come ceil(rank / 64) more K blocks with A = rows of the compensator's B
-//     matrix (read by the same four warps into the same ring) and B = u' by
+//     matrix (read by the same four warps into the same slots) and B = u' by
 //     TMA: since W x + B u' = [W | B] [x ; u'],
 //     the same accumulator absorbs the compensator term. The epilogue reads
 //     TMEM (lane = output row n, column = token) and stores y in bf16.
@@ -24,7 +25,11 @@
 // Warp roles: warp 0 issues TMA (one thread) and owns the TMEM allocation,
 // warp 1 issues tcgen05.mma (one thread), warps 2-5 dequantise and then run
 // the epilogue (warp w reads TMEM lanes 32 (w % 4) .. + 31). Every mbarrier
-// wait is bounded; a timeout latches the handle's status word.
+// wait is bounded; a timeout latches the handle's status word. The MMA
+// thread's loop is on the critical path (a few hundred cycles of its own
+// latency per K block would idle the tensor core), so it waits on one barrier
+// per stage (TMA bytes and the dequantisers' arrivals together) and commits
+// once, and all roles step the stage index by counting.
 #include <algorithm>
 #include <cstring>
 
@@ -40,8 +45,8 @@ constexpr int kRawWBytes = 128 * 8 * 4;        // 128 rows x 64 codes, packed
 constexpr int kRawBytes = kRawWBytes + 128 * 4;  // plus one scale/zero word per row
 constexpr int kBarrierBytes = 1024;
 constexpr int kMaxStages = 6;
-constexpr int kNA = 4;                 // A operands in tensor memory (main kernel)
-constexpr uint32_t kTmemA = 256;       // first column of the A ring (after the accumulator)
+constexpr uint32_t kTmemA = 256;       // main kernel: A operand of stage s at column 256 + 32 s (after the accumulator)
+static_assert(kTmemA + 32 * kMaxStages <= 512, "the A slots of every stage fit in tensor memory");
 
 struct GemmParams {
   int kblocks;      // K blocks of 64 from the main operands (per split for the pre-kernel)
@@ -133,12 +138,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
-  uint64_t* full_tma = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* full_a = full_tma + 8;
-  uint64_t* empty = full_tma + 16;
-  uint64_t* acc_full = full_tma + 24;
-  uint64_t* a_empty = full_tma + 25;  // main kernel: A ring in tensor memory free again
-  uint64_t* part_bar = full_tma + 32;  // main kernel split over K: the other splits' partials are in smem
+  // Per stage s: full[s] = the stage's operands are ready for the MMA (B, and
+  // A, in shared memory by TMA; main kernel: B by TMA plus the A operand in
+  // tensor memory from the four dequantising warps), raw_full[s] = main
+  // kernel: the packed W tile and its scale/zero words have landed (the
+  // dequantisers' input), empty[s] = the MMAs of the stage have completed, so
+  // its shared memory and its A slot in tensor memory may be refilled.
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* raw_full = full + 8;
+  uint64_t* empty = full + 16;
+  uint64_t* acc_full = full + 24;
+  uint64_t* part_bar = full + 32;  // main kernel split over K: the other splits' partials are in smem
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 384);
   uint8_t* stages = smem + kBarrierBytes;
   const uint32_t stages_s = smem_u32(stages);
@@ -156,12 +166,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
-      mbar_init(&full_tma[s], 1);
+      mbar_init(&full[s], DEQ ? 5 : 1);
+      mbar_init(&raw_full[s], 1);
       mbar_init(&empty[s], 1);
-    }
-    for (int s = 0; s < kNA; ++s) {
-      mbar_init(&full_a[s], 4);
-      mbar_init(&a_empty[s], 1);
     }
     mbar_init(acc_full, 1);
     mbar_init(part_bar, 1);
@@ -191,9 +198,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
       if (DEQ && tail > 0) prefetch_l2(p.bt + (size_t)a0 * p.rank, 128u * p.rank * 2u);
+      // stage s and the parity of its current fill, advanced by counting (the
+      // loops of the three roles are short enough that a division by the
+      // runtime stage count would show in the time per K block)
+      int s = 0;
+      unsigned ph = 0;
       for (int it = 0; it < total; ++it) {
-        const int s = it % p.NS;
-        if (it >= p.NS && !mbar_wait_bounded(&empty[s], ((it / p.NS) - 1) & 1, p.wait_ns)) {
+        if (it >= p.NS && !mbar_wait_bounded(&empty[s], ph ^ 1u, p.wait_ns)) {
           fail(p);
           break;
         }
@@ -203,22 +214,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* raw = B + p.b_bytes;
         if (it < kmain) {
           if constexpr (DEQ) {
-            mbar_arrive_expect_tx(&full_tma[s], kRawBytes + p.b_bytes);
-            bulk_g2s(raw, p.wq + ((size_t)blockIdx.x * p.kb_total + kb0 + it) * 1024, kRawWBytes, &full_tma[s]);
+            mbar_arrive_expect_tx(&raw_full[s], kRawBytes);
+            bulk_g2s(raw, p.wq + ((size_t)blockIdx.x * p.kb_total + kb0 + it) * 1024, kRawWBytes, &raw_full[s]);
             bulk_g2s(raw + kRawWBytes, p.sz + ((size_t)blockIdx.x * p.n_groups + ((kb0 + it) * 64) / p.G) * 128,
-                     512, &full_tma[s]);
+                     512, &raw_full[s]);
+            mbar_arrive_expect_tx(&full[s], p.b_bytes);
           } else {
-            mbar_arrive_expect_tx(&full_tma[s], kATileBytes + p.b_bytes);
-            tma_load_2d(A, &mapA, (kb0 + it) * 64, a0, &full_tma[s]);
+            mbar_arrive_expect_tx(&full[s], kATileBytes + p.b_bytes);
+            tma_load_2d(A, &mapA, (kb0 + it) * 64, a0, &full[s]);
           }
-          tma_load_2d(B, &mapB, (kb0 + it) * 64, b0, &full_tma[s]);
+          tma_load_2d(B, &mapB, (kb0 + it) * 64, b0, &full[s]);
         } else {
-          // compensator K-tail: A rows come through the tensor-memory ring,
-          // B = u' from the pre-kernel
+          // compensator K-tail: A rows (read from global memory by the
+          // dequantisers, who may fill the stage's A slot from now on) through
+          // tensor memory, B = u' from the pre-kernel
           const int t = it - kmain;
+          if (DEQ) mbar_arrive(&raw_full[s]);
           if (t == 0 && late_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
-          mbar_arrive_expect_tx(&full_tma[s], p.b_bytes);
-          tma_load_2d(B, &mapBt, t * 64, b0, &full_tma[s]);
+          mbar_arrive_expect_tx(&full[s], p.b_bytes);
+          tma_load_2d(B, &mapBt, t * 64, b0, &full[s]);
+        }
+        if (++s == p.NS) {
+          s = 0;
+          ph ^= 1u;
         }
       }
     }
@@ -226,28 +244,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(128, p.TN);
+      int s = 0;
+      unsigned ph = 0;
+      uint32_t a_s = stages_s;
       for (int it = 0; it < total; ++it) {
-        const int s = it % p.NS;
-        const unsigned par = (it / p.NS) & 1;
-        if (!mbar_wait_bounded(&full_tma[s], par, p.wait_ns)) {
-          fail(p);
-          break;
-        }
-        const int ab = it % kNA;
-        if (DEQ && !mbar_wait_bounded(&full_a[ab], (it / kNA) & 1, p.wait_ns)) {
+        if (!mbar_wait_bounded(&full[s], ph, p.wait_ns)) {
           fail(p);
           break;
         }
         tc_fence_after_sync();
-        const uint32_t a_s = stages_s + s * p.stage_bytes;
         const uint32_t b_s = a_s + p.a_bytes;
         if (DEQ) {
-          // A from the tensor-memory ring: 8 columns (16 channels) per k16 step
+          // A from tensor memory: 8 columns (16 channels) per k16 step
 #pragma unroll
           for (int k16 = 0; k16 < 4; ++k16)
-            umma_ts_bf16(tmem_d, tmem_d + kTmemA + 32 * ab + 8 * k16, sw128_kmajor_desc(b_s + 32 * k16), idesc,
+            umma_ts_bf16(tmem_d, tmem_d + kTmemA + 32 * s + 8 * k16, sw128_kmajor_desc(b_s + 32 * k16), idesc,
                          (it | k16) != 0);
-          umma_commit(&a_empty[ab]);
         } else {
 #pragma unroll
           for (int k16 = 0; k16 < 4; ++k16)
@@ -255,6 +267,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                       (it | k16) != 0);
         }
         umma_commit(&empty[s]);
+        a_s += p.stage_bytes;
+        if (++s == p.NS) {
+          s = 0;
+          ph ^= 1u;
+          a_s = stages_s;
+        }
       }
       umma_commit(acc_full);  // the accumulator is complete once every MMA above has finished
     }
@@ -263,23 +281,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     // One thread per row: warp w owns tensor-memory lanes 32 (w % 4) .. + 31,
     // i.e. rows r = 32 (w % 4) + lane of the tile. Per K block a thread reads
     // its row's 8 packed words and scale/zero word, makes 32 bf16 pairs (pair
-    // c = channels 2c, 2c + 1) and stores them as 32 columns of the A ring.
+    // c = channels 2c, 2c + 1) and stores them as the 32 columns of the
+    // stage's A slot. raw_full[s] also says that the slot is free: the
+    // producer refills a stage only after the MMAs that read it completed.
     // The store of block it is still in flight while block it + 1 is
-    // converted; block it is published (full_a) once its store has completed.
+    // converted; block it counts towards full[s] once its store has completed.
     if constexpr (DEQ) {
       const int q = warp & 3;
       const int r = 32 * q + lane;
       const uint32_t lane_base = tmem_d + ((uint32_t)(32 * q) << 16) + kTmemA;
-      int pending = -1;  // block whose store is in flight
+      int s = 0;
+      unsigned ph = 0;
+      uint32_t raw_sa = stages_s + p.a_bytes + p.b_bytes;
+      int pending = -1;  // stage whose A store is in flight
       for (int it = 0; it < total; ++it) {
-        const int s = it % p.NS, ab = it % kNA;
         uint32_t v[32];
         if (it < kmain) {
-          if (!mbar_wait_bounded(&full_tma[s], (it / p.NS) & 1, p.wait_ns)) {
+          if (!mbar_wait_bounded(&raw_full[s], ph, p.wait_ns)) {
             fail(p);
             break;
           }
-          const uint32_t raw_sa = stages_s + s * p.stage_bytes + p.a_bytes + p.b_bytes;
           const uint4 w0 = lds128(raw_sa + (uint32_t)(r * 32));
           const uint4 w1 = lds128(raw_sa + (uint32_t)(r * 32 + 16));
           const uint32_t szw = lds32(raw_sa + kRawWBytes + r * 4);
@@ -303,26 +324,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[4 * c8 + 2] = w.z;
             v[4 * c8 + 3] = w.w;
           }
+          if (!mbar_wait_bounded(&raw_full[s], ph, p.wait_ns)) {
+            fail(p);
+            break;
+          }
         }
         if (pending >= 0) {
           tmem_st_wait();
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&full_a[pending % kNA]);
+          if (lane == 0) mbar_arrive(&full[pending]);
         }
-        if (it >= kNA && !mbar_wait_bounded(&a_empty[ab], ((it / kNA) - 1) & 1, p.wait_ns)) {
-          fail(p);
-          pending = -1;
-          break;
+        tc_fence_after_sync();
+        tmem_st_x32(lane_base + 32 * s, v);
+        pending = s;
+        raw_sa += p.stage_bytes;
+        if (++s == p.NS) {
+          s = 0;
+          ph ^= 1u;
+          raw_sa = stages_s + p.a_bytes + p.b_bytes;
         }
-        tmem_st_x32(lane_base + 32 * ab, v);
-        pending = it;
       }
       if (pending >= 0) {
         tmem_st_wait();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&full_a[pending % kNA]);
+        if (lane == 0) mbar_arrive(&full[pending]);
       }
     }
 
@@ -712,7 +739,7 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
     p.kps = (kbt + ks - 1) / ks;
     ks = (kbt + p.kps - 1) / p.kps;
   }
-  p.tmem_cols = 512;  // accumulator (TN <= 256 columns) + the A ring from column 256
+  p.tmem_cols = 512;  // accumulator (TN <= 256 columns) + one A slot per stage from column 256
   const size_t smem = kBarrierBytes + 1024 + (size_t)p.NS * p.stage_bytes;
   e = launch<true, 0>(p, dim3(h->nt128, ntt, ks), smem, stream, none, mx, none, mut);
   return e == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
