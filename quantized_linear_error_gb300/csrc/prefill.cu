@@ -45,6 +45,7 @@ constexpr int kRawWBytes = 128 * 8 * 4;        // 128 rows x 64 codes, packed
 constexpr int kRawBytes = kRawWBytes + 128 * 4;  // plus one scale/zero word per row
 constexpr int kBarrierBytes = 1024;
 constexpr int kMaxStages = 6;
+constexpr uint32_t kHintNs = 100;  // suspend-time hint of the pipeline waits
 constexpr uint32_t kTmemA = 256;       // main kernel: A operand of stage s at column 256 + 32 s (after the accumulator)
 static_assert(kTmemA + 32 * kMaxStages <= 512, "the A slots of every stage fit in tensor memory");
 
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int s = 0;
       unsigned ph = 0;
       for (int it = 0; it < total; ++it) {
-        if (it >= p.NS && !mbar_wait_bounded(&empty[s], ph ^ 1u, p.wait_ns)) {
+        if (it >= p.NS && !mbar_wait_bounded_hint(&empty[s], ph ^ 1u, p.wait_ns, kHintNs)) {
           fail(p);
           break;
         }
@@ -248,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       unsigned ph = 0;
       uint32_t a_s = stages_s;
       for (int it = 0; it < total; ++it) {
-        if (!mbar_wait_bounded(&full[s], ph, p.wait_ns)) {
+        if (!mbar_wait_bounded_hint(&full[s], ph, p.wait_ns, kHintNs)) {
           fail(p);
           break;
         }
@@ -297,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0; it < total; ++it) {
         uint32_t v[32];
         if (it < kmain) {
-          if (!mbar_wait_bounded(&raw_full[s], ph, p.wait_ns)) {
+          if (!mbar_wait_bounded_hint(&raw_full[s], ph, p.wait_ns, kHintNs)) {
             fail(p);
             break;
           }
@@ -324,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[4 * c8 + 2] = w.z;
             v[4 * c8 + 3] = w.w;
           }
-          if (!mbar_wait_bounded(&raw_full[s], ph, p.wait_ns)) {
+          if (!mbar_wait_bounded_hint(&raw_full[s], ph, p.wait_ns, kHintNs)) {
             fail(p);
             break;
           }
