@@ -107,3 +107,41 @@ def test_pins_reject_planted_rtn_mistakes(bad, monkeypatch):
         except (AssertionError, FloatingPointError):
             failed += 1
     assert failed > 0
+
+
+# ------------------------------------------------------------------ pack_codes
+def test_pack_codes_hand_packed():
+    """The user layout (even k in the low nibble of byte k / 2) by hand: codes
+    [1, 2] are the byte 0x21; a row 0..15 is 0x10, 0x32, ..., 0xFE; 15 and 0
+    give 0x0F (the high nibble is the odd channel)."""
+    np.testing.assert_array_equal(rtn.pack_codes(np.array([[1, 2]])), [[0x21]])
+    np.testing.assert_array_equal(rtn.pack_codes(np.arange(16)[None, :]),
+                                  [[0x10, 0x32, 0x54, 0x76, 0x98, 0xBA, 0xDC, 0xFE]])
+    np.testing.assert_array_equal(rtn.pack_codes(np.array([[15, 0], [0, 15]])), [[0x0F], [0xF0]])
+
+
+def test_pack_codes_round_trip_by_bit_ops():
+    """Unpacking each byte with its own shift and mask (written here, not
+    taken from the oracle) gives back every code of a random matrix."""
+    rng = np.random.default_rng(9)
+    codes = rng.integers(0, 16, size=(7, 96))
+    b = rtn.pack_codes(codes)
+    assert b.dtype == np.uint8 and b.shape == (7, 48)
+    back = np.empty_like(codes)
+    for n in range(7):
+        for j in range(48):
+            back[n, 2 * j] = int(b[n, j]) & 0xF
+            back[n, 2 * j + 1] = int(b[n, j]) >> 4
+    np.testing.assert_array_equal(back, codes)
+
+
+def test_pins_reject_planted_nibble_swap(monkeypatch):
+    """A packer that puts the even channel in the high nibble must fail the
+    hand-packed pin."""
+    monkeypatch.setattr(rtn, "pack_codes",
+                        lambda c: (np.asarray(c, np.uint8)[:, 1::2] | (np.asarray(c, np.uint8)[:, 0::2] << 4))
+                        .astype(np.uint8))
+    with pytest.raises(AssertionError):
+        test_pack_codes_hand_packed()
+    with pytest.raises(AssertionError):
+        test_pack_codes_round_trip_by_bit_ops()
