@@ -8,15 +8,17 @@
 // layouts and a workspace). spear_linear_forward_decode_noalloc serves them:
 // it reads the weights straight from the caller's buffers in the documented
 // user layout, and the only scratch it needs (the compensator's projection
-// z = A x and a CTA arrival counter) lives in the file-scope array below,
-// which every GPU that loads this library holds until the process exits.
+// z = A x) lives in the file-scope array below, which every GPU that loads
+// this library holds until the process exits.
 //
-// The kernel is a plain CUDA-core variant of the fused decode kernel: each
-// CTA first computes whole rows of z (so no atomics are needed) and bumps an
-// arrival counter, waits (bounded by %globaltimer) until every CTA has
-// arrived, applies the gate u = alpha * gamma(z) * z in shared memory, then
-// computes its output rows y = W x + B u with fp32 accumulation and one bf16
-// rounding. It trades speed for having no set-up at all.
+// Two plain CUDA-core kernels on the caller's stream, ordered by the stream
+// alone (no counter, no wait across blocks, nothing to clear between calls):
+//  1. projection: one warp per row j of A writes z[j][0..M) (the whole dot
+//     product over K, so every entry is written, never accumulated);
+//  2. output: every CTA applies the gate u = alpha * gamma(z) * z into shared
+//     memory, then one warp per output row n computes W x + B u with fp32
+//     accumulation and one bf16 rounding. A lane reads 16 bytes of codes
+//     (32 channels of one group) per step, the group's scale and zero once.
 #include <mutex>
 
 #include "internal.h"
@@ -27,9 +29,8 @@ namespace {
 constexpr int kNoallocMaxRank = 256;
 constexpr int kNoallocMaxTokens = 32;
 constexpr int kNoallocThreads = 256;
-// Layout: [0, 256) counters (arrive, status); [256, 256 + 256 * 32 * 4) z [rank][32] fp32.
-constexpr size_t kNoallocCounterBytes = 256;
-constexpr size_t kNoallocScratchBytes = kNoallocCounterBytes + (size_t)kNoallocMaxRank * kNoallocMaxTokens * 4;
+// z [rank][32] fp32
+constexpr size_t kNoallocScratchBytes = (size_t)kNoallocMaxRank * kNoallocMaxTokens * 4;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
@@ -41,107 +42,118 @@ struct NoallocParams {
   const uint16_t* B;
   const __nv_bfloat16* x;
   __nv_bfloat16* y;
-  unsigned* counters;  // [0] arrivals, [1] status
-  float* z;            // [rank][32]
+  float* z;  // [rank][32]
   int K, N, G, n_groups, rank, M, gate;
   float alpha;
-  uint64_t wait_ns;
 };
 
 __device__ __forceinline__ float bf(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__device__ __forceinline__ float block_sum(float v, float* red) {
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float t = 0.f;
-  if (threadIdx.x < kNoallocThreads / 32) t = red[threadIdx.x];
-  if (warp == 0)
-    for (int o = 4; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-  return t;  // valid in thread 0
+// Sum of 8 products of a bf16 octet (16 bytes) with another.
+__device__ __forceinline__ float dot8(const uint4& a, const uint4& b) {
+  float s = bf_lo(a.x) * bf_lo(b.x);
+  s = fmaf(bf_hi(a.x), bf_hi(b.x), s);
+  s = fmaf(bf_lo(a.y), bf_lo(b.y), s);
+  s = fmaf(bf_hi(a.y), bf_hi(b.y), s);
+  s = fmaf(bf_lo(a.z), bf_lo(b.z), s);
+  s = fmaf(bf_hi(a.z), bf_hi(b.z), s);
+  s = fmaf(bf_lo(a.w), bf_lo(b.w), s);
+  return fmaf(bf_hi(a.w), bf_hi(b.w), s);
 }
 
-__global__ void __launch_bounds__(kNoallocThreads) noalloc_decode_kernel(const NoallocParams p) {
-  __shared__ float u[kNoallocMaxTokens * kNoallocMaxRank];  // u[m * rank + j]
-  __shared__ float red[kNoallocThreads / 32];
-  __shared__ int ok_s;
+__device__ __forceinline__ float warp_sum(float v) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// z[j][m] = sum_k A[j][k] x[m][k]: warp w of CTA b takes row j = 8 b + w; lane
+// l reads channels 8 l .. 8 l + 7 of every 256-channel step (16-byte loads).
+__global__ void __launch_bounds__(kNoallocThreads) noalloc_project_kernel(const NoallocParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = blockIdx.x * (kNoallocThreads / 32) + warp;
+  if (j >= p.rank) return;
+  float acc[kNoallocMaxTokens];
+#pragma unroll
+  for (int m = 0; m < kNoallocMaxTokens; ++m) acc[m] = 0.f;
+  const uint4* arow = reinterpret_cast<const uint4*>(p.A + (size_t)j * p.K);
+  for (int k8 = lane; k8 < p.K / 8; k8 += 32) {
+    const uint4 a = __ldg(arow + k8);
+#pragma unroll
+    for (int m = 0; m < kNoallocMaxTokens; ++m)
+      if (m < p.M) acc[m] += dot8(a, __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)m * p.K) + k8));
+  }
+#pragma unroll
+  for (int m = 0; m < kNoallocMaxTokens; ++m) {
+    if (m >= p.M) break;
+    const float v = warp_sum(acc[m]);
+    if (lane == 0) p.z[j * kNoallocMaxTokens + m] = v;
+  }
+}
 
-  // ---- compensator projection: CTA b owns rows j = b, b + grid, ... of z
-  for (int j = blockIdx.x; j < p.rank; j += gridDim.x) {
-    for (int m = 0; m < p.M; ++m) {
-      float acc = 0.f;
-      for (int k = threadIdx.x; k < p.K; k += kNoallocThreads)
-        acc += bf(p.A[(size_t)j * p.K + k]) * __bfloat162float(p.x[(size_t)m * p.K + k]);
-      acc = block_sum(acc, red);
-      if (threadIdx.x == 0) p.z[j * 32 + m] = acc;
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(&p.counters[0], 1u);
-  }
-
-  // ---- wait for every CTA's rows of z, then gate
-  if (threadIdx.x == 0) {
-    int ok = 1;
-    if (p.rank > 0) {
-      const uint64_t t0 = globaltimer();
-      while (ld_acquire_gpu(&p.counters[0]) < gridDim.x) {
-        if (globaltimer() - t0 > p.wait_ns) {
-          ok = 0;
-          atomicOr(&p.counters[1], kStatusTimeoutZ);
-          break;
-        }
-      }
-    }
-    ok_s = ok;
-  }
-  __syncthreads();
+// y = W x + B u for one warp per output row n.
+__global__ void __launch_bounds__(kNoallocThreads) noalloc_output_kernel(const NoallocParams p) {
+  __shared__ float u[kNoallocMaxTokens * kNoallocMaxRank];  // u[m * rank + j]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < p.M * p.rank; i += kNoallocThreads) {
     const int m = i / p.rank, j = i % p.rank;
-    float v = 0.f;
-    if (ok_s) {
-      const float zz = __ldcg(p.z + j * 32 + m);
-      v = p.alpha * (p.gate == SPEAR_GATE_ONE ? zz : zz * (1.0f / (1.0f + expf(-zz))));
-    }
-    u[i] = v;
+    const float zz = p.z[j * kNoallocMaxTokens + m];
+    u[i] = p.alpha * (p.gate == SPEAR_GATE_ONE ? zz : zz * (1.0f / (1.0f + expf(-zz))));
   }
   __syncthreads();
 
-  // ---- output rows: one warp per row, lanes stride over K
   const int nwarps = kNoallocThreads / 32;
   for (int n = blockIdx.x * nwarps + warp; n < p.N; n += gridDim.x * nwarps) {
     float acc[kNoallocMaxTokens];
 #pragma unroll
     for (int m = 0; m < kNoallocMaxTokens; ++m) acc[m] = 0.f;
-    for (int k = lane; k < p.K; k += 32) {
-      const uint8_t byte = p.q[(size_t)n * (p.K / 2) + (k >> 1)];
-      const int code = (k & 1) ? (byte >> 4) : (byte & 0xF);
-      const int g = k / p.G;
-      const int zero = p.zp ? p.zp[(size_t)n * p.n_groups + g] : 8;
-      const float w = (float)(code - zero) * bf(p.s[(size_t)n * p.n_groups + g]);
+    const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (size_t)n * (p.K / 2));
+    // lane l takes the 32 channels k0 = 32 (l + 32 i) .. k0 + 31, one group
+    for (int c = lane; c < p.K / 32; c += 32) {
+      const int k0 = 32 * c, g = k0 / p.G;
+      const uint4 qv = __ldg(qrow + c);
+      const float zero = p.zp ? (float)p.zp[(size_t)n * p.n_groups + g] : 8.f;
+      const float sc = bf(p.s[(size_t)n * p.n_groups + g]);
+      // (q - z) for the 32 channels, exact in fp32
+      float w[32];
+      const uint32_t words[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-      for (int m = 0; m < kNoallocMaxTokens; ++m)
-        if (m < p.M) acc[m] += w * __bfloat162float(p.x[(size_t)m * p.K + k]);
+      for (int b = 0; b < 4; ++b)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[8 * b + i] = (float)((words[b] >> (4 * i)) & 0xFu) - zero;
+#pragma unroll
+      for (int m = 0; m < kNoallocMaxTokens; ++m) {
+        if (m >= p.M) break;
+        const uint4* xr = reinterpret_cast<const uint4*>(p.x + (size_t)m * p.K + k0);
+        float part = 0.f;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const uint4 xv = __ldg(xr + b);
+          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            part = fmaf(w[8 * b + 2 * i], bf_lo(xw[i]), part);
+            part = fmaf(w[8 * b + 2 * i + 1], bf_hi(xw[i]), part);
+          }
+        }
+        acc[m] = fmaf(sc, part, acc[m]);
+      }
     }
 #pragma unroll
     for (int m = 0; m < kNoallocMaxTokens; ++m) {
       if (m >= p.M) break;
-      float v = acc[m];
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      const float v = warp_sum(acc[m]);
       float ec = 0.f;
       for (int j = lane; j < p.rank; j += 32) ec += bf(p.B[(size_t)n * p.rank + j]) * u[m * p.rank + j];
-      for (int o = 16; o > 0; o >>= 1) ec += __shfl_xor_sync(0xffffffffu, ec, o);
+      ec = warp_sum(ec);
       if (lane == 0) p.y[(size_t)m * p.N + n] = __float2bfloat16_rn(v + ec);
     }
   }
 }
 
-// Device address of the scratch array, looked up once per device.
+// Device address of the scratch array, looked up once per device (with that
+// device current) and cached.
 void* scratch_address(spear_status_t* st) {
   static std::mutex mu;
   static void* addr[128] = {};
@@ -164,6 +176,8 @@ void* scratch_address(spear_status_t* st) {
   return addr[dev];
 }
 
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 }  // namespace
 }  // namespace spear
 
@@ -179,15 +193,14 @@ extern "C" spear_status_t spear_linear_forward_decode_noalloc(const spear_linear
   if (d->rank < 0 || d->rank % 16 != 0 || (d->rank > 0 && (!d->A || !d->B))) return SPEAR_ERR_INVALID_ARG;
   if (d->gate == SPEAR_GATE_MLP) return SPEAR_ERR_UNSUPPORTED;
   if (d->gate != SPEAR_GATE_SIGMOID && d->gate != SPEAR_GATE_ONE) return SPEAR_ERR_INVALID_ARG;
+  // 16-byte loads of codes, x and A
+  if (!aligned16(x) || !aligned16(d->qweight) || (d->rank > 0 && !aligned16(d->A))) return SPEAR_ERR_INVALID_ARG;
   // beyond the scratch array's capacity
   if (M > kNoallocMaxTokens || d->rank > kNoallocMaxRank) return SPEAR_ERR_INVALID_ARG;
 
   spear_status_t st;
   unsigned char* scratch = static_cast<unsigned char*>(scratch_address(&st));
   if (st != SPEAR_OK) return st;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return SPEAR_ERR_CUDA;
 
   NoallocParams p{};
   p.q = d->qweight;
@@ -197,8 +210,7 @@ extern "C" spear_status_t spear_linear_forward_decode_noalloc(const spear_linear
   p.B = static_cast<const uint16_t*>(d->B);
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.y = static_cast<__nv_bfloat16*>(y);
-  p.counters = reinterpret_cast<unsigned*>(scratch);
-  p.z = reinterpret_cast<float*>(scratch + kNoallocCounterBytes);
+  p.z = reinterpret_cast<float*>(scratch);
   p.K = d->K;
   p.N = d->N;
   p.G = d->group_size == 0 ? d->K : d->group_size;
@@ -207,14 +219,11 @@ extern "C" spear_status_t spear_linear_forward_decode_noalloc(const spear_linear
   p.M = M;
   p.gate = d->gate;
   p.alpha = d->alpha;
-  p.wait_ns = 100000000ull;
-  // The array keeps the previous call's contents: start from zero counters.
-  if (cudaMemsetAsync(scratch, 0, kNoallocCounterBytes, stream) != cudaSuccess) return SPEAR_ERR_CUDA;
-  // One CTA per SM at most, so that all CTAs are resident for the z wait.
   const int rows_per_cta = kNoallocThreads / 32;
-  int grid = (d->N + rows_per_cta - 1) / rows_per_cta;
-  if (grid > sms) grid = sms;
-  if (grid < 1) grid = 1;
-  noalloc_decode_kernel<<<grid, kNoallocThreads, 0, stream>>>(p);
+  if (p.rank > 0) {
+    noalloc_project_kernel<<<(p.rank + rows_per_cta - 1) / rows_per_cta, kNoallocThreads, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return SPEAR_ERR_CUDA;
+  }
+  noalloc_output_kernel<<<(d->N + rows_per_cta - 1) / rows_per_cta, kNoallocThreads, 0, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
 }
