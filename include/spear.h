@@ -89,8 +89,14 @@ typedef struct {
  * rank not a multiple of 16 or > 256, max_tokens < 1; for SPEAR_GATE_MLP:
  * rank == 0, gate_hidden outside 1..64, null or unaligned gate weights),
  * UNSUPPORTED (shape outside the kernels' limits: N > 16 * 16 * SM count for
- * the decode path), OOM, CUDA. On error *out is left NULL and nothing is
- * leaked. */
+ * the decode path, or a decode grid that cannot be resident on the device all
+ * at once, which its grid-wide compensator dependency needs), OOM, CUDA. On
+ * error *out is left NULL and nothing is leaked.
+ * Co-residency: the decode kernel runs at most one CTA per SM and its CTAs
+ * wait for each other (bounded). Kernels of other streams or processes that
+ * hold SMs while a decode call starts can delay some of its CTAs; if that
+ * outlasts the wait limit, the call leaves the compensator out and latches
+ * TIMEOUT, which spear_linear_check reports. */
 spear_status_t spear_linear_create(const spear_linear_desc_t* desc, cudaStream_t stream,
                                    spear_linear_t* out);
 
@@ -122,8 +128,10 @@ spear_status_t spear_linear_forward(spear_linear_t h, const void* x, void* y, in
 spear_status_t spear_linear_forward_host(spear_linear_t h, const void* x_host, void* y_host,
                                          int32_t M, cudaStream_t stream);
 
-/* Free every device allocation of the handle (synchronises the device first).
- * NULL is accepted. */
+/* Free every device allocation of the handle. cudaFree, which this calls,
+ * waits for work already queued on the device, so forwards still in flight
+ * finish first; the handle must not be used (or enqueued) afterwards. NULL is
+ * accepted. */
 spear_status_t spear_linear_destroy(spear_linear_t h);
 
 /* Test surface: write the dequantised weight bf16_RNE((q - z) * s) as bf16
@@ -139,18 +147,17 @@ spear_status_t spear_linear_dequantize(spear_linear_t h, int32_t path, void* w_o
 spear_status_t spear_linear_check(spear_linear_t h, cudaStream_t stream);
 
 /* Test surface for the bounded waits: wait_ns sets the device-side wait limit
- * (0 restores the default of 100 ms); skip_arrive != 0 makes the decode
- * kernel's CTAs skip their "compensator projection done" arrival so that the
- * wait must run out (the kernel then leaves the compensator out of y and
- * latches TIMEOUT). */
+ * (0 restores the default of 100 ms); skip_arrive != 0 makes CTAs skip the
+ * arrival another CTA waits for, so that the wait must run out:
+ *  - decode: the "compensator projection done" arrival (the kernel then leaves
+ *    the compensator out of y and latches TIMEOUT);
+ *  - prefill, when the main kernel splits K (a handle without compensator and
+ *    too few tiles to fill the SMs): the splits' "partial tile stored"
+ *    arrival (the split that adds the partials then gives up, writes nothing
+ *    for its tile and latches TIMEOUT).
+ * The prefill pre-kernel -> main kernel dependency is a stream (programmatic
+ * launch) dependency that the hardware resolves; it has no arrival to skip. */
 spear_status_t spear_linear_debug_set(spear_linear_t h, int64_t wait_ns, int32_t skip_arrive);
-
-/* Choose the decode kernel of the handle: 0 automatic (the default), 1 the
- * warp-MMA kernel (mma.sync, dequantised fragments in registers), 2 the
- * tensor-core kernel (tcgen05: weights streamed by bulk copies, dequantised
- * into tensor memory, compensator up-projection as an extra K block). Both
- * compute the same y up to summation order. Errors: INVALID_ARG. */
-spear_status_t spear_linear_select_decode(spear_linear_t h, int32_t kernel);
 
 /* Decode forward that allocates nothing (the paper has no counterpart; this is
  * a deployment convenience). For callers that cannot call cudaMalloc at all,
@@ -160,21 +167,25 @@ spear_status_t spear_linear_select_decode(spear_linear_t h, int32_t kernel);
  * so this call takes everything from the caller.
  *   desc: the same descriptor spear_linear_create takes (device pointers to
  *         the user-layout q, scales, zeros, A, B; max_tokens is ignored);
- *   x: device bf16 [M][K]; y: device bf16 [M][N]; 1 <= M <= 32 (0 is a no-op).
+ *         qweight and A 16-byte aligned;
+ *   x: device bf16 [M][K], 16-byte aligned; y: device bf16 [M][N];
+ *   1 <= M <= 32 (0 is a no-op).
  * Result: y = bf16_RNE(W_q x + alpha B (gamma(Ax) (.) Ax)), fp32 accumulation,
  * as spear_linear_forward_decode computes (summation order differs).
  * SPEAR_GATE_MLP is not supported here (SPEAR_ERR_UNSUPPORTED).
- * Scratch: the compensator projection z and an arrival counter live in one
- * static device array of the library (33,024 bytes, held on every GPU that
- * loads the library until the process exits); it bounds rank <= 256 and
- * M <= 32, and larger values return SPEAR_ERR_INVALID_ARG. The first call on a
- * device looks the array's address up (cudaGetSymbolAddress) and caches it;
- * make that first call before any stream capture. Every call clears the
- * counters (cudaMemsetAsync on `stream`), then launches one kernel; no
- * allocation, no synchronisation. All calls share the array, so calls that
- * overlap on the GPU (different streams, or devices' streams racing on one
- * device) race with each other: serialise them. Slower than the handle-based
- * decode path (it reads the unpacked user layout on CUDA cores). */
+ * Scratch: the compensator projection z lives in one static device array of
+ * the library (32,768 bytes, held on every GPU that loads the library until
+ * the process exits); it bounds rank <= 256 and M <= 32, and larger values
+ * return SPEAR_ERR_INVALID_ARG. The first call on a device looks the array's
+ * address up (cudaGetSymbolAddress, with that device current) and caches it;
+ * make that first call before any stream capture. Each call enqueues two
+ * kernels on `stream` (z = A x into the array, then the output rows), ordered
+ * by the stream alone: no wait across blocks, no allocation, no
+ * synchronisation. Every z entry a call reads was written by the same call,
+ * so nothing needs clearing between calls. All calls share the array, so
+ * calls that overlap on the GPU (different streams, or several host threads)
+ * race with each other: serialise them. Slower than the handle-based decode
+ * path (it reads the unpacked user layout on CUDA cores). */
 spear_status_t spear_linear_forward_decode_noalloc(const spear_linear_desc_t* desc, const void* x, void* y,
                                                    int32_t M, cudaStream_t stream);
 

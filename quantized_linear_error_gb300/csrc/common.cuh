@@ -18,13 +18,12 @@ enum : unsigned {
 
 // Workspace of one handle (device memory, zero-initialised at create).
 struct SyncWords {
-  unsigned arrive;     // CTAs that finished their share of z = A x (tensor-core decode)
-  unsigned depart;     // CTAs that finished reading z (tensor-core decode)
   unsigned status;     // kStatus* bits
-  unsigned epoch;      // warp-MMA decode: calls completed (selects the z buffer)
-  unsigned arrive_acc; // warp-MMA decode: CTA arrivals summed over all calls (epoch * grid at a call's start)
-  unsigned pad[27];    // keep the z buffer 128-byte aligned
+  unsigned epoch;      // decode: calls completed (selects the z buffer)
+  unsigned arrive_acc; // decode: CTA arrivals summed over all calls (epoch * grid at a call's start)
+  unsigned pad[29];    // keep the z buffer 128-byte aligned
 };
+static_assert(sizeof(SyncWords) == 128, "the decode z buffer follows at a 128-byte boundary");
 
 SPEAR_DEVINL uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

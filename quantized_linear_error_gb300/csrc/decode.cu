@@ -717,62 +717,59 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
   }
 }
 
-template <int NW, int MT, int T, bool PC, bool EC>
-cudaError_t launch_one(const DecodeParams& p, const CUtensorMap& xmap, int grid, size_t smem, cudaStream_t st) {
-  static bool configured = false;
-  auto k = decode_kernel<NW, MT, T, PC, EC>;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3((NW + 1 + kEcWarps) * 32);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, p, xmap);
+// The kernel instantiation for (NW, MT, PC, EC) and the set-up it needs on a
+// device (its shared-memory limit raised, once per device); T = 1 for every
+// plan (create limits P to 16 tiles, one per consumer warp).
+using DecodeKernelFn = void (*)(const DecodeParams, const CUtensorMap);
+struct DecodeKernelRef {
+  DecodeKernelFn fn = nullptr;
+  cudaError_t (*configure)() = nullptr;
+};
+
+template <int NW, int MT, bool PC, bool EC>
+cudaError_t configure_t() {
+  static std::atomic<uint64_t> configured{0};  // devices whose limit is raised
+  return smem_limit_once(reinterpret_cast<const void*>(decode_kernel<NW, MT, 1, PC, EC>), configured);
 }
 
-template <int NW, int MT, int T>
-cudaError_t launch_t(const DecodeParams& p, const CUtensorMap& m, bool pc, bool ec, int grid, size_t smem,
-                     cudaStream_t st) {
-  if (pc)
-    return ec ? launch_one<NW, MT, T, true, true>(p, m, grid, smem, st)
-              : launch_one<NW, MT, T, true, false>(p, m, grid, smem, st);
-  return ec ? launch_one<NW, MT, T, false, true>(p, m, grid, smem, st)
-            : launch_one<NW, MT, T, false, false>(p, m, grid, smem, st);
+template <int NW, int MT>
+DecodeKernelRef kernel_t(bool pc, bool ec) {
+  if (pc) return ec ? DecodeKernelRef{decode_kernel<NW, MT, 1, true, true>, configure_t<NW, MT, true, true>}
+                    : DecodeKernelRef{decode_kernel<NW, MT, 1, true, false>, configure_t<NW, MT, true, false>};
+  return ec ? DecodeKernelRef{decode_kernel<NW, MT, 1, false, true>, configure_t<NW, MT, false, true>}
+            : DecodeKernelRef{decode_kernel<NW, MT, 1, false, false>, configure_t<NW, MT, false, false>};
 }
 
-}  // namespace
-}  // namespace spear
+DecodeKernelRef kernel_for(int NW, int MT, bool pc, bool ec) {
+  if (MT == 1) return kernel_t<16, 1>(pc, ec);
+  if (MT == 2) return kernel_t<16, 2>(pc, ec);
+  return NW == 8 ? kernel_t<8, 4>(pc, ec) : NW == 10 ? kernel_t<10, 4>(pc, ec) : kernel_t<16, 4>(pc, ec);
+}
 
-using namespace spear;
+// Everything a decode launch needs except the x tensor map.
+struct DecodeLaunch {
+  DecodeParams p;
+  int grid = 0, NW = 0, MT = 0;
+  size_t smem = 0;
+  DecodeKernelRef kernel;
+};
 
-spear_status_t spear_launch_decode(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,
-                                   cudaStream_t stream) {
-  DecodeParams p{};
+spear_status_t decode_config(const spear_linear_s* h, int M, DecodeLaunch* out) {
+  DecodeParams& p = out->p;
+  p = DecodeParams{};
   const int MT = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
   const int Mp = 8 * MT;
   const bool ec = h->rank > 0;
   const int P = h->dec_P;
   int NW, T, KW, KC;
   decode_plan(P, h->K, M, &NW, &T, &KW, &KC);
-  if (P > T * NW) return SPEAR_ERR_UNSUPPORTED;
-  const int grid = (h->nt16 + P - 1) / P;
+  if (P > T * NW || T != 1) return SPEAR_ERR_UNSUPPORTED;
   const DecodeLayout L{h->K, h->nt16, P, h->per_channel};
 
   p.wq = h->wq_dec;
   p.sz = h->sz_dec;
   p.a_frag = h->a_dec;
   p.b_frag = h->b_dec;
-  p.x = x;
-  p.y = y;
   p.z = h->z_mma;
   p.sync = h->sync;
   p.K = h->K;
@@ -809,21 +806,59 @@ spear_status_t spear_launch_decode(spear_linear_s* h, const __nv_bfloat16* x, __
   while ((size_t)NS * p.stage_bytes < red_bytes) ++NS;  // the reduction reuses the stage area
   if (NS < 1 || fixed + (size_t)NS * p.stage_bytes > 227 * 1024) return SPEAR_ERR_UNSUPPORTED;
   p.NS = NS;
-  const size_t smem = fixed + (size_t)NS * p.stage_bytes;
+  out->smem = fixed + (size_t)NS * p.stage_bytes;
+  out->grid = (h->nt16 + P - 1) / P;
+  out->NW = NW;
+  out->MT = MT;
+  out->kernel = kernel_for(NW, MT, h->per_channel, ec);
+  return SPEAR_OK;
+}
 
+}  // namespace
+}  // namespace spear
+
+using namespace spear;
+
+spear_status_t spear_launch_decode(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,
+                                   cudaStream_t stream) {
+  DecodeLaunch d;
+  spear_status_t st = decode_config(h, M, &d);
+  if (st != SPEAR_OK) return st;
+  d.p.x = x;
+  d.p.y = y;
   CUtensorMap xmap;
-  if (!encode_x_map(&xmap, x, M, h->K, Mp, KC)) return SPEAR_ERR_CUDA;
+  if (!encode_x_map(&xmap, x, M, h->K, 8 * d.MT, d.p.KC)) return SPEAR_ERR_CUDA;
+  if (d.kernel.configure() != cudaSuccess) return SPEAR_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(d.grid);
+  cfg.blockDim = dim3((d.NW + 1 + kEcWarps) * 32);
+  cfg.dynamicSmemBytes = d.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, d.kernel.fn, d.p, xmap) == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
+}
 
-  const bool pc = h->per_channel;
-  cudaError_t e;
-  // one tile per consumer warp at most (create limits P to 16)
-  if (MT == 1)
-    e = launch_t<16, 1, 1>(p, xmap, pc, ec, grid, smem, stream);
-  else if (MT == 2)
-    e = launch_t<16, 2, 1>(p, xmap, pc, ec, grid, smem, stream);
-  else
-    e = NW == 8    ? launch_t<8, 4, 1>(p, xmap, pc, ec, grid, smem, stream)
-        : NW == 10 ? launch_t<10, 4, 1>(p, xmap, pc, ec, grid, smem, stream)
-                   : launch_t<16, 4, 1>(p, xmap, pc, ec, grid, smem, stream);
-  return e == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
+// The decode kernel's CTAs wait for each other (the compensator's grid-wide
+// z dependency), so a grid must fit on the device at once: one CTA per SM at
+// most, with each plan's shared memory. Checked at create for every token
+// count the handle accepts.
+spear_status_t spear_decode_check_residency(spear_linear_s* h) {
+  const int mmax = h->max_tokens < kDecodeMaxTokens ? h->max_tokens : kDecodeMaxTokens;
+  for (int M : {1, 9, 17}) {
+    if (M > mmax) break;
+    DecodeLaunch d;
+    spear_status_t st = decode_config(h, M, &d);
+    if (st != SPEAR_OK) return st;
+    if (d.kernel.configure() != cudaSuccess) return SPEAR_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, d.kernel.fn, (d.NW + 1 + kEcWarps) * 32, d.smem) !=
+        cudaSuccess)
+      return SPEAR_ERR_CUDA;
+    if ((long)per_sm * h->sm_count < d.grid) return SPEAR_ERR_UNSUPPORTED;
+  }
+  return SPEAR_OK;
 }

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/spear.h"
 #include "common.cuh"
 
@@ -80,9 +82,6 @@ struct spear_linear_s {
   __nv_bfloat16* gate_w1 = nullptr;  // SPEAR_GATE_MLP: W1 [h8][rank], rows h.. zero
   __nv_bfloat16* gate_w2 = nullptr;  // SPEAR_GATE_MLP: W2 [rank][h8], columns h.. zero
   size_t ws_bytes = 0;               // workspace size (zeroed at create and by a TIMEOUT check)
-  float* y32_tc = nullptr;           // tensor-core decode: [sm_count + 2 nt128][128][32] fp32 partials
-  unsigned* tile_cnt_tc = nullptr;   // tensor-core decode: [nt128] contributors done per tile
-  int decode_kernel = 0;             // 0 automatic, 1 warp MMA, 2 tensor cores (tcgen05)
   __nv_bfloat16* x_stage = nullptr;  // host-path staging [max_tokens][K]
   __nv_bfloat16* y_stage = nullptr;  // host-path staging [max_tokens][N]
 
@@ -164,9 +163,24 @@ bool encode_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t
 
 spear_status_t spear_launch_decode(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,
                                    cudaStream_t stream);
+spear_status_t spear_decode_check_residency(spear_linear_s* h);
 spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,
                                     cudaStream_t stream);
-spear_status_t spear_launch_decode_tc(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,
-                                      cudaStream_t stream);
 spear_status_t spear_build_layouts(spear_linear_s* h, const spear_linear_desc_t* d, cudaStream_t stream);
 spear_status_t spear_launch_dequant(spear_linear_s* h, int path, __nv_bfloat16* out, cudaStream_t stream);
+
+// Raise `kernel`'s dynamic shared-memory limit to 227 KB on the current device,
+// once per (kernel, device): `done` is the caller's per-kernel set of devices
+// already configured (bit d for device ordinal d < 64; larger ordinals are
+// configured on every call). Setting the attribute is idempotent, so threads
+// racing on the first launch on a device do no harm.
+inline cudaError_t smem_limit_once(const void* kernel, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}

@@ -66,6 +66,7 @@ struct GemmParams {
   int gate;
   unsigned* status;
   uint64_t wait_ns;
+  int skip_arrive;  // test surface: splits other than the leader skip their arrival on part_cnt
   int NS;
   uint32_t a_bytes, b_bytes, raw_bytes, stage_bytes;
   uint32_t tmem_cols;
@@ -483,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // publish this split's partial tile to the leader
       __threadfence();
       epilogue_bar();
-      if (threadIdx.x == 64 && ok) atomicAdd(&p.part_cnt[tile_id], 1u);
+      if (threadIdx.x == 64 && ok && !p.skip_arrive) atomicAdd(&p.part_cnt[tile_id], 1u);
     }
     if constexpr (EPI == 2) {
       // The last split of this 128-token tile applies the gate to the complete z,
@@ -582,12 +583,11 @@ uint32_t tmem_cols_for(int n) {
 template <bool DEQ, int EPI>
 cudaError_t launch(const GemmParams& p, dim3 grid, size_t smem, cudaStream_t st, const CUtensorMap& mA,
                    const CUtensorMap& mB, const CUtensorMap& mAt, const CUtensorMap& mBt) {
-  static bool configured = false;
+  static std::atomic<uint64_t> configured{0};  // devices whose limit is raised
   auto k = gemm_kernel<DEQ, EPI>;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  {
+    cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(k), configured);
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -707,6 +707,7 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
   ks = (kbt + p.kps - 1) / p.kps;
   p.part = h->part;
   p.part_cnt = h->part_cnt;
+  p.skip_arrive = h->skip_arrive;
   p.kblocks = kbt;
   p.kb_total = kbt;
   p.splits = 1;

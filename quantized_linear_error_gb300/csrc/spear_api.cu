@@ -135,9 +135,7 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
 
   const size_t K = h->K, r = h->rank, mt = h->max_tokens;
   const size_t pre_tiles = (mt + 127) / 128;
-  const size_t y32_tc_floats = ((size_t)h->sm_count + 2 * (size_t)h->nt128) * 128 * 32;
-  const size_t ws_base = sizeof(spear::SyncWords) + kZDecFloats * 4 + mt * r * 4 + mt * r * 2 + pre_tiles * 4 +
-                         256 + y32_tc_floats * 4 + (size_t)h->nt128 * 4 + 256;
+  const size_t ws_base = sizeof(spear::SyncWords) + kZDecFloats * 4 + mt * r * 4 + mt * r * 2 + pre_tiles * 4;
   const size_t z_mma_off = (ws_base + 127) / 128 * 128;
   // Prefill splits K when its tiles fill less than one wave: at most sm_count
   // (split, tile) pairs of 128 rows x 256 tokens in fp32, for handles sized
@@ -184,11 +182,6 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
   h->z_pre = h->z_dec + kZDecFloats;
   h->u_pre = reinterpret_cast<__nv_bfloat16*>(h->z_pre + mt * r);
   h->pre_done = reinterpret_cast<unsigned*>(h->u_pre + mt * r);
-  {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(h->pre_done + pre_tiles);
-    h->y32_tc = reinterpret_cast<float*>((a + 255) & ~uintptr_t(255));
-    h->tile_cnt_tc = reinterpret_cast<unsigned*>(h->y32_tc + y32_tc_floats);
-  }
 
   spear_status_t st = SPEAR_OK;
   if (cudaMemsetAsync(h->ws, 0, ws_bytes, stream) != cudaSuccess) st = SPEAR_ERR_CUDA;
@@ -203,6 +196,7 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
       st = SPEAR_ERR_CUDA;
   }
   if (st == SPEAR_OK && cudaStreamSynchronize(stream) != cudaSuccess) st = SPEAR_ERR_CUDA;
+  if (st == SPEAR_OK) st = spear_decode_check_residency(h);
   if (st != SPEAR_OK) {
     cudaGetLastError();
     free_all(h);
@@ -220,7 +214,6 @@ spear_status_t spear_linear_forward_decode(spear_linear_t h, const void* x, void
   if (M > kDecodeMaxTokens) return SPEAR_ERR_INVALID_ARG;
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
   auto* yb = static_cast<__nv_bfloat16*>(y);
-  if (h->decode_kernel == 2) return spear_launch_decode_tc(h, xb, yb, M, stream);
   return spear_launch_decode(h, xb, yb, M, stream);
 }
 
@@ -254,7 +247,8 @@ spear_status_t spear_linear_forward_host(spear_linear_t h, const void* x_host, v
 
 spear_status_t spear_linear_destroy(spear_linear_t h) {
   if (!h) return SPEAR_OK;
-  cudaDeviceSynchronize();
+  // cudaFree itself waits for the work already queued on the device, so a
+  // forward still in flight never sees its buffers freed under it.
   free_all(h);
   delete h;
   return SPEAR_OK;
@@ -282,12 +276,6 @@ spear_status_t spear_linear_debug_set(spear_linear_t h, int64_t wait_ns, int32_t
   if (!h || wait_ns < 0) return SPEAR_ERR_INVALID_ARG;
   h->wait_ns = wait_ns == 0 ? 100000000ull : (uint64_t)wait_ns;
   h->skip_arrive = skip_arrive != 0;
-  return SPEAR_OK;
-}
-
-spear_status_t spear_linear_select_decode(spear_linear_t h, int32_t kernel) {
-  if (!h || kernel < 0 || kernel > 2) return SPEAR_ERR_INVALID_ARG;
-  h->decode_kernel = kernel;
   return SPEAR_OK;
 }
 

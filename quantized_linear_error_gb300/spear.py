@@ -64,8 +64,6 @@ def load(path: Path | None = None):
     L.spear_linear_dequantize.argtypes = [H, c_int32, c_void_p, H]
     L.spear_linear_check.argtypes = [H, H]
     L.spear_linear_debug_set.argtypes = [H, c_int64, c_int32]
-    L.spear_linear_select_decode.argtypes = [H, c_int32]
-    L.spear_linear_select_decode.restype = c_int
     L.spear_linear_forward_decode_noalloc.argtypes = [POINTER(spear_linear_desc_t), c_void_p, c_void_p, c_int32, H]
     L.spear_linear_forward_decode_noalloc.restype = c_int
     L.spear_sched_create.argtypes = [c_void_p, c_int32, c_void_p, c_int32, c_void_p, POINTER(c_void_p)]
@@ -161,10 +159,6 @@ class SpearLinear:
 
     def debug_set(self, wait_ns: int = 0, skip_arrive: bool = False) -> None:
         _check(load().spear_linear_debug_set(self.h, int(wait_ns), int(bool(skip_arrive))), "spear_linear_debug_set")
-
-    def select_decode(self, kernel: int) -> None:
-        """0 automatic, 1 warp-MMA kernel, 2 tensor-core (tcgen05) kernel."""
-        _check(load().spear_linear_select_decode(self.h, int(kernel)), "spear_linear_select_decode")
 
     def close(self) -> None:
         if getattr(self, "h", None) and self.h.value:

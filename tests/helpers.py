@@ -47,13 +47,7 @@ def with_spec(w: wl.LinearWeights, **kw) -> wl.LinearWeights:
     return wl.LinearWeights(dataclasses.replace(w.spec, **kw), w.q, w.s, w.z, w.A, w.B, w.outliers, w.W1, w.W2)
 
 
-# decode kernel the parity tests run (0 automatic, 1 warp MMA, 2 tensor cores);
-# set per test by the fixtures of the decode test modules
-DECODE_KERNEL = 0
-
-
 def run(lin: spear.SpearLinear, x_bits: np.ndarray, path: str) -> np.ndarray:
-    lin.select_decode(DECODE_KERNEL)
     x = dev_bf16(x_bits)
     y = torch.empty((x.shape[0], lin.N), dtype=torch.bfloat16, device="cuda")
     getattr(lin, f"forward_{path}")(x, y)

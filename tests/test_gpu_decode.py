@@ -14,19 +14,9 @@ from oracle import ref
 from quantized_linear_error_gb300 import spear
 from quantized_linear_error_gb300 import workload as wl
 
-from . import helpers
 from .helpers import codes_equal_zeros, dev_bf16, host_f64, rel_err, run, sample_rows, with_spec
 
 pytestmark = pytest.mark.gpu
-
-
-@pytest.fixture(autouse=True, params=[1, 2], ids=["mma", "tc"])
-def decode_kernel(request):
-    """Every decode parity test runs on both decode kernels."""
-    from . import helpers
-    helpers.DECODE_KERNEL = request.param
-    yield request.param
-    helpers.DECODE_KERNEL = 0
 TOL = 1e-2
 
 
@@ -147,7 +137,6 @@ def test_bounded_wait_times_out_and_recovers():
     x = dev_bf16(wl.make_x(w.spec.K, 8, w.outliers, 0, "to"))
     y = torch.empty((8, w.spec.N), dtype=torch.bfloat16, device="cuda")
     lin.debug_set(wait_ns=2_000_000, skip_arrive=True)
-    lin.select_decode(helpers.DECODE_KERNEL)
     lin.forward_decode(x, y)
     assert lin.check() == spear.SPEAR_ERR_TIMEOUT
     nw = wl.LinearWeights(with_spec(w, rank=0).spec, w.q, w.s, w.z, None, None, w.outliers)

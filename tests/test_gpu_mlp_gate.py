@@ -13,15 +13,6 @@ from quantized_linear_error_gb300 import workload as wl
 from .helpers import codes_equal_zeros, rel_err, run, sample_rows, with_spec
 
 pytestmark = pytest.mark.gpu
-
-
-@pytest.fixture(autouse=True, params=[1, 2], ids=["mma", "tc"])
-def decode_kernel(request):
-    """Every decode parity test runs on both decode kernels."""
-    from . import helpers
-    helpers.DECODE_KERNEL = request.param
-    yield request.param
-    helpers.DECODE_KERNEL = 0
 TOL = 1e-2
 MLP = wl.GATE_MLP
 

@@ -87,3 +87,25 @@ def test_split_over_k(M, group_size, rank):
         # the partials are added in split order: repeated calls agree bit for bit
         # (with a compensator, the pre-kernel's atomic split-K sum of z does not)
         np.testing.assert_array_equal(y1, y2)
+
+
+def test_split_wait_times_out_and_recovers():
+    """The K splits skip their "partial tile stored" arrival: the split that
+    adds the partials waits out its 4 x 2 ms limit, writes nothing for its
+    tile and latches TIMEOUT; check() reports it and resets the workspace, and
+    the next call on the same handle is correct again. Nothing traps or hangs."""
+    import torch
+
+    from .helpers import dev_bf16
+    sp = wl.LinearSpec("split/timeout", 4096, 1024, 128, 0)
+    w = wl.make_weights(sp, 15)
+    lin = spear.from_weights(w, max_tokens=512)
+    M = 100
+    x = dev_bf16(wl.make_x(sp.K, M, w.outliers, 0, sp.name))
+    y = torch.empty((M, sp.N), dtype=torch.bfloat16, device="cuda")
+    lin.debug_set(wait_ns=2_000_000, skip_arrive=True)
+    lin.forward_prefill(x, y)
+    assert lin.check() == spear.SPEAR_ERR_TIMEOUT
+    lin.debug_set(0, False)
+    _check(w, M, lin=lin)
+    assert lin.check() == spear.SPEAR_OK
