@@ -31,6 +31,8 @@ import tempfile
 import time
 from pathlib import Path
 
+import numpy as np
+
 ROOT = Path(__file__).resolve().parent
 sys.path.insert(0, str(ROOT))
 
@@ -156,47 +158,100 @@ def traffic_from_profile(kernel_src: Path, summary: Path):
 
 
 # ------------------------------------------------------------------ CPU oracle
-def cpu_oracle_rate(sample_rows: int = 256, seed: int = 0):
-    """Time the fp64 oracle on all seven linears at M = 1, 8, 32 for the first
-    `sample_rows` output rows of each, and scale to tokens/s of the full step."""
-    from oracle import ref
-    from quantized_linear_error_gb300 import workload as wl
-    ref.build()
-    specs = wl.config_linears(2)
-    ws = [wl.make_weights(sp, seed) for sp in specs]
-    t_full = 0.0
-    for M in DECODE_TOKENS:
-        for w in ws:
-            x = wl.make_x(w.spec.K, M, w.outliers, seed, w.spec.name)
-            rows = slice(0, min(sample_rows, w.spec.N))
-            sub = wl.LinearWeights(w.spec, w.q[rows], w.s[rows], w.z[rows], w.A, w.B[rows], w.outliers)
-            t0 = time.perf_counter()
-            ref.forward(sub.q, sub.s, sub.z, w.spec.K, w.spec.G, sub.A, sub.B, w.spec.alpha, w.spec.gate, x)
-            dt = time.perf_counter() - t0
-            t_full += dt * w.spec.N / (rows.stop - rows.start)
-    tokens = sum(DECODE_TOKENS)
-    return {"value": tokens / t_full, "unit": "tokens/s", "cores": ref.max_threads(), "kind": "oracle",
-            "sample": f"fp64 oracle, all 7 linears at M=1,8,32, first {sample_rows} output rows each, "
-                      f"time scaled by N/{sample_rows} to the full layer set"}, t_full
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in Path("/proc/cpuinfo").read_text().splitlines():
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+class OracleStep:
+    """The fp64 CPU oracle on the decode layer set: all seven linears at
+    M = 1, 8 and 32 (the step the GPU arm times), on the same inputs."""
+
+    def __init__(self, seed: int = 0):
+        from oracle import ref
+        from quantized_linear_error_gb300 import workload as wl
+        ref.build()
+        self.ref = ref
+        self.ws = [wl.make_weights(sp, seed) for sp in wl.config_linears(2)]
+        self.xs = {(M, w.spec.name): wl.make_x(w.spec.K, M, w.outliers, seed, w.spec.name)
+                   for M in DECODE_TOKENS for w in self.ws}
+
+    def run(self, fraction: float = 1.0) -> tuple[float, float]:
+        """One step over the first ceil(fraction * N) output rows of every
+        linear (every row at fraction 1). Returns (seconds measured, seconds
+        for the whole step: the same at fraction 1, else scaled by N / rows)."""
+        import math
+        t_meas = t_full = 0.0
+        for M in DECODE_TOKENS:
+            for w in self.ws:
+                n = w.spec.N if fraction >= 1.0 else max(1, math.ceil(fraction * w.spec.N))
+                rows = None if n == w.spec.N else np.arange(n, dtype=np.int64)
+                t0 = time.perf_counter()
+                self.ref.forward_w(w, self.xs[(M, w.spec.name)], rows)
+                dt = time.perf_counter() - t0
+                t_meas += dt
+                t_full += dt * w.spec.N / n
+        return t_meas, t_full
+
+    def describe(self, fraction: float) -> dict:
+        whole = fraction >= 1.0
+        return {"kind": "oracle", "cores": self.ref.max_threads(), "cpu_model": cpu_model(),
+                "sample": "fp64 oracle, the whole decode layer set (all 7 linears, every output row) at M=1,8,32"
+                          if whole else
+                          f"fp64 oracle, all 7 linears at M=1,8,32, first {fraction:.3%} of each linear's output "
+                          "rows (the rest of the step's time scaled from them)"}
+
+
+def cpu_oracle_rate(reps: int = 3, seed: int = 0):
+    """The oracle timed on the whole layer set: median of `reps` steps."""
+    step = OracleStep(seed)
+    times = sorted(step.run(1.0)[0] for _ in range(reps))
+    t = times[len(times) // 2]
+    return {"value": sum(DECODE_TOKENS) / t, "unit": "tokens/s", **step.describe(1.0),
+            "seconds_per_step": t}, t
 
 
 def run_reference(args, world, rank):
-    """The reference arm: the CPU oracle as it stands, same metric and config."""
+    """The reference arm: the CPU oracle as it stands, same metric and config.
+    Each step is the whole layer set when K + W steps of it fit in about two
+    and a half minutes (the first warm-up step measures it), else the same
+    leading fraction of every linear's rows."""
     if rank != 0:
         return
-    for _ in range(args.warmup):
-        cpu_oracle_rate(sample_rows=32)
-    vals = []
+    step = OracleStep(0)
+    t_whole = step.run(1.0)[0]
+    budget = 150.0
+    fraction = min(1.0, budget / max(1, args.steps + args.warmup) / max(t_whole, 1e-9))
+    for _ in range(max(0, args.warmup - 1)):
+        step.run(fraction)
+    meas, full = [], []
+    t_start = time.perf_counter()
     for _ in range(args.steps):
-        cb, t_full = cpu_oracle_rate(sample_rows=64)
-        vals.append(cb["value"])
-    value = statistics.median(vals)
-    cb["value"] = value
-    cb["sample"] = cb["sample"].replace("first 256", "first 64")
+        a, b = step.run(fraction)
+        meas.append(a)
+        full.append(b)
+    wall = time.perf_counter() - t_start
+    t_step = statistics.median(full)
+    value = sum(DECODE_TOKENS) / t_step
+    cb = {"value": value, "unit": "tokens/s", **step.describe(fraction)}
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sum(DECODE_TOKENS) / value * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / max(1, args.steps) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD, "tokens_per_step": list(DECODE_TOKENS)},
+            "data": "synthetic", "config": {"workload": WORKLOAD, "tokens_per_step": list(DECODE_TOKENS),
+                                            "rows_fraction": fraction},
             "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -333,7 +388,7 @@ def measure_other_configs(args, stream, time_graphs, dev, hbm_peak, bf16_peak, w
             ys = {N: torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for N in (4096, 11008)}
             g = graph_of([lambda h=h, s5=s5: h.forward_prefill(xs[s5.K], ys[s5.N], stream=stream)
                           for h, s5 in zip(hs, specs)])
-            t = time_graphs([g], max(3, args.steps // 200), 2)
+            t = time_graphs([g], max(3, args.steps // 200), 3)
             fl = sum(s5.flops(M) for s5 in specs)
             res[str(M - 64)] = {"tokens": M, "ms_per_step": t, "tokens_per_s": M / (t / 1e3),
                                 "tflops": fl / (t / 1e3) / 1e12, "frac_bf16_peak": fl / (t / 1e3) / 1e12 / bf16_peak}
@@ -392,7 +447,7 @@ def measure_scheduler(args, stream, time_graphs, dev, base):
         with torch.cuda.graph(g, stream=stream):
             for f in calls:
                 f()
-        t = time_graphs([g], max(3, args.steps // 400), 1)
+        t = time_graphs([g], max(3, args.steps // 400), 3)
         del g
         return t
 
@@ -574,58 +629,90 @@ def run_ours(args, world, rank, local):
                          "frac_hbm": b / (t / 1e3) / 1e9 / hbm_peak}
         del gm
 
-    # --- end to end through the host-buffer entry point
+    # --- end to end through the host-buffer entry points: the step's 21 calls
+    # with their copies from and to pinned host memory, one synchronisation
+    # per step (spear_linear_forward_host_batch); and the same with one
+    # synchronous spear_linear_forward_host per call
     hx = {k: v.cpu().pin_memory() for k, v in xs.items()}
     hy = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in ys.items()}
     h2d = sum(M * sp.K * 2 for M in DECODE_TOKENS for sp in specs)
     d2h = sum(M * sp.N * 2 for M in DECODE_TOKENS for sp in specs)
 
-    def e2e_step(i):
+    def e2e_batch(i):
+        hs = handles[True][(i % COPIES) * 7:(i % COPIES + 1) * 7]
+        lins, xl, yl = [], [], []
+        for M in DECODE_TOKENS:
+            for h, sp in zip(hs, specs):
+                lins.append(h)
+                xl.append(hx[(M, sp.K)])
+                yl.append(hy[(M, sp.N)])
+        spear.forward_host_batch(lins, xl, yl, stream=stream)
+
+    def e2e_per_call(i):
         hs = handles[True][(i % COPIES) * 7:(i % COPIES + 1) * 7]
         for M in DECODE_TOKENS:
             for h, sp in zip(hs, specs):
                 h.forward_host(hx[(M, sp.K)], hy[(M, sp.N)], stream=stream)
 
-    for i in range(args.warmup):
-        e2e_step(i)
-    barrier(world)
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        e2e_step(i)
-    e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, world)
-    e2e = {"value": tokens * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "call": "spear_linear_forward_host per linear (pinned host x/y, synchronous)"}
+    def time_host(fn):
+        for i in range(args.warmup):
+            fn(i)
+        barrier(world)
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            fn(i)
+        return max_over_ranks((time.perf_counter() - t0) / args.steps, world)
 
-    # --- prefill: Llama-3-8B MLP at M = 2048 (gate, up 4096->14336; down 14336->4096), EC rank 128
+    e2e_s = time_host(e2e_batch)
+    e2e_call_s = time_host(e2e_per_call)
+    e2e = {"value": tokens * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": e2e_s * 1e3,
+           "call": "spear_linear_forward_host_batch: the step's 21 calls with their H2D/D2H copies (pinned host "
+                   "x/y), one synchronisation per step",
+           "per_call_sync": {"value": tokens * world / e2e_call_s, "ms_per_step": e2e_call_s * 1e3,
+                             "call": "spear_linear_forward_host per linear (synchronous)"}}
+
+    # --- prefill: Llama-3-8B MLP at M = 2048 (gate, up 4096->14336; down 14336->4096), EC rank 128,
+    # next to the same kernels without the compensator
     prefill = None
     if not args.skip_prefill:
         pspecs = wl.config_linears(3)
         Mp = 2048
-        pl = [spear.from_weights(wl.make_weights(sp, 0), max_tokens=Mp, stream=stream) for sp in pspecs]
+        pw = [wl.make_weights(sp, 0) for sp in pspecs]
         px = {K: torch.randn(Mp, K, device="cuda").to(torch.bfloat16) for K in (4096, 14336)}
         py = {N: torch.empty(Mp, N, device="cuda", dtype=torch.bfloat16) for N in (4096, 14336)}
-        with torch.cuda.stream(stream):
-            for h, sp in zip(pl, pspecs):
-                h.forward_prefill(px[sp.K], py[sp.N], stream=stream)
-        stream.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for h, sp in zip(pl, pspecs):
-                h.forward_prefill(px[sp.K], py[sp.N], stream=stream)
-        tp = time_graphs([g], max(3, args.steps // 4), 2)
         flops = sum(sp.flops(Mp) for sp in pspecs)
-        tflops = flops / (tp / 1e3) / 1e12
-        prefill = {"workload": "llama3-8b MLP, M=2048, INT4 g128, EC r128", "ms": tp, "tflops": tflops,
-                   "frac_bf16_peak": tflops / bf16_peak, "peak_tflops": bf16_peak, "peak_source": peak_src,
-                   "tokens_per_s": Mp / (tp / 1e3)}
-        for h in pl:
-            if h.check() != spear.SPEAR_OK:
-                raise SystemExit("prefill device status error")
+        res = {}
+        for ec in (True, False):
+            pl = [spear.from_weights(w if ec else wl.LinearWeights(wl.LinearSpec(w.spec.name, w.spec.K, w.spec.N,
+                                                                                    w.spec.group_size, 0),
+                                                                     w.q, w.s, w.z, None, None, w.outliers),
+                                     max_tokens=Mp, stream=stream) for w in pw]
+            with torch.cuda.stream(stream):
+                for h, sp in zip(pl, pspecs):
+                    h.forward_prefill(px[sp.K], py[sp.N], stream=stream)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for h, sp in zip(pl, pspecs):
+                    h.forward_prefill(px[sp.K], py[sp.N], stream=stream)
+            tp = time_graphs([g], max(3, min(args.steps // 4, 100)), 3)
+            fl = flops if ec else sum(sp.flops(Mp) - 2 * Mp * sp.rank * (sp.K + sp.N) for sp in pspecs)
+            res[ec] = {"ms": tp, "tflops": fl / (tp / 1e3) / 1e12, "frac_bf16_peak": fl / (tp / 1e3) / 1e12 / bf16_peak,
+                       "tokens_per_s": Mp / (tp / 1e3)}
+            for h in pl:
+                if h.check() != spear.SPEAR_OK:
+                    raise SystemExit("prefill device status error")
+                h.close()
+            del g
+        prefill = {"workload": "llama3-8b MLP, M=2048, INT4 g128, EC r128", **res[True],
+                   "peak_tflops": bf16_peak, "peak_source": peak_src,
+                   "ec_off": {**res[False], "ec_overhead": res[True]["ms"] / res[False]["ms"] - 1.0}}
 
     # --- the other workloads: config 1 and 4 (decode), config 5 (mixed serving step, on request)
     configs = None
     if not args.skip_configs:
-        configs = measure_other_configs(args, stream, time_graphs, dev, hbm_peak, bf16_peak, args.config5)
+        configs = measure_other_configs(args, stream, time_graphs, dev, hbm_peak, bf16_peak, not args.skip_config5)
 
     # --- roofline of the decode kernel (the only kernel in the step)
     launches = len(DECODE_TOKENS) * len(specs)
@@ -726,7 +813,8 @@ def main():
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-configs", action="store_true", help="skip the config 1 and 4 measurements")
-    ap.add_argument("--config5", action="store_true", help="also measure config 5 (32-layer mixed serving step)")
+    ap.add_argument("--skip-config5", action="store_true",
+                    help="skip config 5 (32-layer mixed serving step) and the chunk scheduler's table")
     ap.add_argument("--case", help="run one small named case 5 times and exit (profiling target), "
                                    "e.g. decode:c2/q:1, decode:c4/up:16:noec, prefill:c3/gate:2048")
     args = ap.parse_args()
