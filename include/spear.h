@@ -100,6 +100,26 @@ typedef struct {
 spear_status_t spear_linear_create(const spear_linear_desc_t* desc, cudaStream_t stream,
                                    spear_linear_t* out);
 
+/* Build ONE handle for several linears that read the same input x, such as
+ * the q, k and v projections of an attention block or the gate and up
+ * projections of an MLP (the paper has no counterpart; this is how serving
+ * engines fuse such projections). Each member keeps its own weights, zero
+ * points, compensator (A_i, B_i, alpha_i) and result:
+ *   y[:, row_i : row_i + N_i] = W_i x + alpha_i B_i (gamma(A_i x) (.) A_i x),
+ * row_i = N_0 + ... + N_{i-1}, so y is bf16 [M][N_0 + ... + N_{n-1}] and
+ * every forward of the handle computes all members in one call (one launch
+ * on the decode path: the stacked projection [A_0; ...; A_{n-1}] x and its
+ * gate run once for all members, each output tile then applies its own
+ * member's B_i and alpha_i).
+ *   descs: n descriptors, 1 <= n <= 8 (n == 1 is spear_linear_create). All
+ *   members must have the same K, group_size, rank and gate, N_i a multiple
+ *   of 16, and n * rank <= 256; SPEAR_GATE_MLP is not supported here
+ *   (UNSUPPORTED). max_tokens of the handle is the largest of the members'.
+ * The members' buffers are copied (through temporary device buffers that
+ * create frees before returning); errors as for spear_linear_create. */
+spear_status_t spear_linear_create_grouped(const spear_linear_desc_t* descs, int32_t n, cudaStream_t stream,
+                                           spear_linear_t* out);
+
 /* Decode-phase forward ("SPEAR", section 2.2A: memory-bound, small M; the whole
  * layer, compensator included, runs as one kernel).
  *   x: device bf16 [M][K]; y: device bf16 [M][N] (must not overlap x).
@@ -127,6 +147,19 @@ spear_status_t spear_linear_forward(spear_linear_t h, const void* x, void* y, in
  * asynchronous copies. 1 <= M <= max_tokens. */
 spear_status_t spear_linear_forward_host(spear_linear_t h, const void* x_host, void* y_host,
                                          int32_t M, cudaStream_t stream);
+
+/* End-to-end forward of a batch of calls on HOST buffers with one
+ * synchronisation: for i = 0 .. n-1, in order on `stream`, copies x_host[i]
+ * (bf16 [Ms[i]][K of hs[i]]) into hs[i]'s staging buffer, runs
+ * spear_linear_forward on it and copies the result into y_host[i] (bf16
+ * [Ms[i]][N of hs[i]]); then synchronises `stream` once. A handle may appear
+ * several times (its staging buffers are reused in stream order). Every
+ * argument is checked before anything is enqueued: INVALID_ARG for a null
+ * array or handle, Ms[i] outside 0 .. max_tokens of hs[i], or null buffers
+ * with Ms[i] > 0. Pinned host memory gives asynchronous copies. */
+spear_status_t spear_linear_forward_host_batch(const spear_linear_t* hs, const void* const* x_host,
+                                               void* const* y_host, const int32_t* Ms, int32_t n,
+                                               cudaStream_t stream);
 
 /* Free every device allocation of the handle. cudaFree, which this calls,
  * waits for work already queued on the device, so forwards still in flight

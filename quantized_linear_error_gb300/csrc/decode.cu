@@ -56,7 +56,19 @@ struct DecodeParams {
   const __nv_bfloat16* gw1;  // SPEAR_GATE_MLP: W1 [gh][rank]
   const __nv_bfloat16* gw2;  // SPEAR_GATE_MLP: W2 [rank][gh]
   int gh;
+  // grouped handle: member i owns 16-row tiles [tile_start[i], tile_start[i + 1]),
+  // its up-projection reads u columns [i rank_b, (i + 1) rank_b), scaled by alphas[i]
+  int n_members, rank_b;
+  int tile_start[kMaxGroup + 1];
+  float alphas[kMaxGroup];
 };
+
+// Member of a grouped handle that owns 16-row tile `tile`.
+SPEAR_DEVINL int member_of_tile(const DecodeParams& p, int tile) {
+  int m = 0;
+  while (m + 1 < p.n_members && tile >= p.tile_start[m + 1]) ++m;
+  return m;
+}
 
 // Named barrier of the consumer warps. bar.sync counts whole warps, so each
 // warp reconverges first (lane-0 branches precede both uses).
@@ -326,9 +338,9 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
       if (EC) {
         // B fragments of this CTA's tiles (contiguous, constant since create)
         // into shared memory for the final up-projection.
-        const unsigned bbytes = (unsigned)(Pc * (p.rank / 16) * 512);
+        const unsigned bbytes = (unsigned)(Pc * (p.rank_b / 16) * 512);
         mbar_arrive_expect_tx(bbar, bbytes);
-        bulk_g2s_shared_u32(bbuf_s, p.b_frag + (size_t)tile0 * (p.rank / 16) * 32, bbytes, bbar);
+        bulk_g2s_shared_u32(bbuf_s, p.b_frag + (size_t)tile0 * (p.rank_b / 16) * 32, bbytes, bbar);
       }
       for (int i = prefetch; i < p.n_stages; ++i) {
         const int slot = i % p.NS;
@@ -423,7 +435,7 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float g = p.gate == SPEAR_GATE_ONE ? 1.0f : __fdividef(1.0f, 1.0f + __expf(-zz[e]));
-              const float uval = (m0 + e < p.M) ? p.alpha * zz[e] * g : 0.f;
+              const float uval = (m0 + e < p.M) ? p.alphas[j / p.rank_b] * zz[e] * g : 0.f;
               __nv_bfloat16 hi, lo;
               split_bf16(uval, hi, lo);
               uh[(m0 + e) * us + j] = hi;
@@ -688,10 +700,11 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
     const int tile = tile0 + tl;
     if constexpr (EC) {
       if (ec_ok) {
-        const int nj = p.rank / 16;
+        const int nj = p.rank_b / 16;
         const uint32_t bt = bbuf_s + (uint32_t)(((tl * nj) * 32 + lane) * 16);
-        // this lane's ldmatrix row of u: token 8 n + lane % 8, k half lane / 8 % 2
-        const int uoff = (8 * n + mr) * us + 8 * (mat & 1);
+        // this lane's ldmatrix row of u: token 8 n + lane % 8, k half lane / 8 % 2,
+        // in the tile's member's columns of u
+        const int uoff = (8 * n + mr) * us + 8 * (mat & 1) + member_of_tile(p, tile) * p.rank_b;
 #pragma unroll 2
         for (int j = 0; j < nj; ++j) {
           const uint4 bf = lds128(bt + (uint32_t)j * 512);
@@ -791,12 +804,16 @@ spear_status_t decode_config(const spear_linear_s* h, int M, DecodeLaunch* out) 
   p.gw1 = h->gate_w1;
   p.gw2 = h->gate_w2;
   p.gh = h->gate_hidden;
+  p.n_members = h->n_members;
+  p.rank_b = h->rank_b;
+  for (int i = 0; i <= h->n_members; ++i) p.tile_start[i] = h->row_start[i] / 16;
+  for (int i = 0; i < h->n_members; ++i) p.alphas[i] = h->alphas[i];
 
   const size_t red_bytes = (size_t)P * KW * 32 * 4 * MT * 4;
   const size_t u_bytes = ec ? (size_t)2 * Mp * (h->rank + 8) * 2 : 0;
   const size_t mlp_bytes = h->gate_hidden > 0 ? (size_t)M * (h->rank + h->gate_hidden) * 4 : 0;
   const size_t pc_bytes = h->per_channel ? (size_t)P * 64 : 0;
-  const size_t b_bytes = ec ? (size_t)P * (h->rank / 16) * 512 + 16 : 0;
+  const size_t b_bytes = ec ? (size_t)P * (h->rank_b / 16) * 512 + 16 : 0;
   // barriers, alignment slack, per-channel words, u (hi and lo)
   const size_t fixed = kBarrierBytes + 1024 + pc_bytes + u_bytes + mlp_bytes + b_bytes;
   const size_t budget = kSmemCap > fixed ? kSmemCap - fixed : 0;

@@ -47,10 +47,20 @@
 //   a_pre   bf16  [rank][K]               copy of A
 //   b_pre   bf16  [nt128*128][rank]       copy of B, zero rows past N
 
+constexpr int kMaxGroup = 8;  // linears fused into one grouped handle, at most
+
 struct spear_linear_s {
   int device = 0, sm_count = 0;
   int K = 0, N = 0, G = 0, n_groups = 0, rank = 0, max_tokens = 0;
   float alpha = 1.f;
+  // Grouped handle (spear_linear_create_grouped): n_members linears sharing x,
+  // rows [row_start[i], row_start[i + 1]) of y belong to member i. `rank` is
+  // the stacked rank of all members' A (the projection and gate run over all
+  // of it); member i's up-projection uses u columns [i rank_b, (i + 1) rank_b)
+  // and its own alpha. An ordinary handle is a group of one.
+  int n_members = 1, rank_b = 0;
+  int row_start[kMaxGroup + 1] = {};
+  float alphas[kMaxGroup] = {};
   int gate = 0;
   bool per_channel = false;
 
@@ -166,7 +176,11 @@ spear_status_t spear_launch_decode(spear_linear_s* h, const __nv_bfloat16* x, __
 spear_status_t spear_decode_check_residency(spear_linear_s* h);
 spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,
                                     cudaStream_t stream);
-spear_status_t spear_build_layouts(spear_linear_s* h, const spear_linear_desc_t* d, cudaStream_t stream);
+// Builds every kernel layout from user-layout weights: q, scales, zeros and A
+// from `d` (A with h->rank rows), B from `B_rows` ([N][h->rank_b], the members'
+// B matrices one after the other).
+spear_status_t spear_build_layouts(spear_linear_s* h, const spear_linear_desc_t* d, const void* B_rows,
+                                   cudaStream_t stream);
 spear_status_t spear_launch_dequant(spear_linear_s* h, int path, __nv_bfloat16* out, cudaStream_t stream);
 
 // Raise `kernel`'s dynamic shared-memory limit to 227 KB on the current device,

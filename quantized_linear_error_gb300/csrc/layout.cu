@@ -115,6 +115,29 @@ __global__ void copy_pad_rows(const uint16_t* __restrict__ m, int rows, int rows
     out[i] = (i / cols) < rows ? m[i] : (uint16_t)0;
 }
 
+// Block-diagonal prefill B of a grouped handle: out [rows_pad][n * rb], row r
+// of member i (rows [start[i], start[i + 1])) holds that member's B row in
+// columns [i rb, (i + 1) rb) and zeros elsewhere; rows past N are zero.
+struct RowStarts {
+  int n;
+  int start[kMaxGroup + 1];
+};
+__global__ void expand_block_diag(const uint16_t* __restrict__ b, int N, int rb, RowStarts rs, int rows_pad,
+                                  uint16_t* __restrict__ out) {
+  const int cols = rs.n * rb;
+  const long total = (long)rows_pad * cols;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+    const int row = (int)(i / cols), c = (int)(i % cols);
+    uint16_t v = 0;
+    if (row < N) {
+      int m = 0;
+      while (m + 1 < rs.n && row >= rs.start[m + 1]) ++m;
+      if (c / rb == m) v = b[(size_t)row * rb + (c - m * rb)];
+    }
+    out[i] = v;
+  }
+}
+
 // (q - z) * s with one rounding: the exact difference d = (q - z) * 2^-e comes
 // from the kernels' own unpack (e = 0 for the prefill layout; e = 7 or 3 for
 // the decode layout), d * 2^e is exact, its product with s is exact in fp32
@@ -200,8 +223,9 @@ inline int grid_for(long total, int threads) {
 
 using namespace spear;
 
-spear_status_t spear_build_layouts(spear_linear_s* h, const spear_linear_desc_t* d, cudaStream_t st) {
-  const int K = h->K, N = h->N, r = h->rank;
+spear_status_t spear_build_layouts(spear_linear_s* h, const spear_linear_desc_t* d, const void* B_rows,
+                                   cudaStream_t st) {
+  const int K = h->K, N = h->N, r = h->rank, rb = h->rank_b;
   const uint16_t* s = static_cast<const uint16_t*>(d->scales);
   const int T = 256;
   long n;
@@ -221,15 +245,23 @@ spear_status_t spear_build_layouts(spear_linear_s* h, const spear_linear_desc_t*
   repack_sz<<<grid_for(n, T), T, 0, st>>>(s, d->zeros, h->n_groups, N, h->nt128, 128, h->sz_pre);
   if (r > 0) {
     const uint16_t* A = static_cast<const uint16_t*>(d->A);
-    const uint16_t* B = static_cast<const uint16_t*>(d->B);
+    const uint16_t* B = static_cast<const uint16_t*>(B_rows);
     n = (long)(r / 16) * (K / 16) * 32;
     repack_frag<<<grid_for(n, T), T, 0, st>>>(A, r, K, r / 16, true, h->a_dec);
-    n = (long)h->nt16 * (r / 16) * 32;
-    repack_frag<<<grid_for(n, T), T, 0, st>>>(B, N, r, h->nt16, false, h->b_dec);
+    n = (long)h->nt16 * (rb / 16) * 32;
+    repack_frag<<<grid_for(n, T), T, 0, st>>>(B, N, rb, h->nt16, false, h->b_dec);
     n = (long)r * K;
     copy_pad_rows<<<grid_for(n, T), T, 0, st>>>(A, r, r, K, reinterpret_cast<uint16_t*>(h->a_pre));
     n = (long)h->nt128 * 128 * r;
-    copy_pad_rows<<<grid_for(n, T), T, 0, st>>>(B, N, h->nt128 * 128, r, reinterpret_cast<uint16_t*>(h->b_pre));
+    if (h->n_members == 1) {
+      copy_pad_rows<<<grid_for(n, T), T, 0, st>>>(B, N, h->nt128 * 128, r, reinterpret_cast<uint16_t*>(h->b_pre));
+    } else {
+      RowStarts rs{};
+      rs.n = h->n_members;
+      for (int i = 0; i <= h->n_members; ++i) rs.start[i] = h->row_start[i];
+      expand_block_diag<<<grid_for(n, T), T, 0, st>>>(B, N, rb, rs, h->nt128 * 128,
+                                                      reinterpret_cast<uint16_t*>(h->b_pre));
+    }
   }
   return cudaGetLastError() == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
 }

@@ -64,6 +64,8 @@ struct GemmParams {
   int ld_out;
   float alpha;
   int gate;
+  int rank_b;                // pre-kernel: column c of u' belongs to member c / rank_b (grouped handle)
+  float alphas[kMaxGroup];   // pre-kernel: each member's alpha
   unsigned* status;
   uint64_t wait_ns;
   int skip_arrive;  // test surface: splits other than the leader skip their arrival on part_cnt
@@ -444,9 +446,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (row < p.a_rows) {
             uint32_t pk[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              pk[j] = pack_bf16x2(p.alpha * gate_apply(__uint_as_float(v[2 * j]), p.gate),
-                                  p.alpha * gate_apply(__uint_as_float(v[2 * j + 1]), p.gate));
+            for (int j = 0; j < 8; ++j) {
+              const float al = p.alphas[(c0 + 2 * j) / p.rank_b];  // c0 + 2j and + 1: same member
+              pk[j] = pack_bf16x2(al * gate_apply(__uint_as_float(v[2 * j]), p.gate),
+                                  al * gate_apply(__uint_as_float(v[2 * j + 1]), p.gate));
+            }
             uint4* dst = reinterpret_cast<uint4*>(p.out + (size_t)row * p.ld_out + c0);
             dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
@@ -552,10 +556,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 8; ++j) {
               const int m = a0 + 32 * q + r0 + j;
               if (m < p.a_rows) {
-                const uint2 pk = make_uint2(pack_bf16x2(p.alpha * gate_apply(zv[j].x, p.gate),
-                                                        p.alpha * gate_apply(zv[j].y, p.gate)),
-                                            pack_bf16x2(p.alpha * gate_apply(zv[j].z, p.gate),
-                                                        p.alpha * gate_apply(zv[j].w, p.gate)));
+                const float al = p.alphas[c / p.rank_b];  // columns c .. c + 3: one member
+                const uint2 pk = make_uint2(pack_bf16x2(al * gate_apply(zv[j].x, p.gate),
+                                                        al * gate_apply(zv[j].y, p.gate)),
+                                            pack_bf16x2(al * gate_apply(zv[j].z, p.gate),
+                                                        al * gate_apply(zv[j].w, p.gate)));
                 *reinterpret_cast<uint2*>(p.out + (size_t)m * p.ld_out + c) = pk;
                 *reinterpret_cast<float4*>(p.zacc + (size_t)m * p.ld_out + c) = make_float4(0.f, 0.f, 0.f, 0.f);
               }
@@ -659,6 +664,8 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
     p.ld_out = r;
     p.alpha = h->alpha;
     p.gate = h->gate;
+    p.rank_b = h->rank_b;
+    for (int i = 0; i < h->n_members; ++i) p.alphas[i] = h->alphas[i];
     p.status = &h->sync->status;
     p.wait_ns = h->wait_ns;
     p.a_bytes = kATileBytes;

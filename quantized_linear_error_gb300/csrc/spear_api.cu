@@ -95,15 +95,17 @@ spear_status_t check_io(spear_linear_t h, const void* x, void* y, int32_t M) {
   return SPEAR_OK;
 }
 
-}  // namespace
+// Members of a grouped handle (a group of one for spear_linear_create).
+struct GroupInfo {
+  int n = 1;
+  int rank_b = 0;                      // each member's compensator rank
+  int row_start[kMaxGroup + 1] = {};   // first output row of each member, then N
+  float alphas[kMaxGroup] = {};
+  const void* B_rows = nullptr;        // [N][rank_b]: the members' B, one after the other
+};
 
-extern "C" {
-
-spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t stream, spear_linear_t* out) {
-  if (!out) return SPEAR_ERR_INVALID_ARG;
+spear_status_t create_impl(const spear_linear_desc_t* d, const GroupInfo& g, cudaStream_t stream, spear_linear_t* out) {
   *out = nullptr;
-  spear_status_t v = validate(d);
-  if (v != SPEAR_OK) return v;
 
   spear_linear_s* h = new (std::nothrow) spear_linear_s();
   if (!h) return SPEAR_ERR_OOM;
@@ -119,6 +121,10 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
   h->n_groups = h->K / h->G;
   h->rank = d->rank;
   h->alpha = d->alpha;
+  h->n_members = g.n;
+  h->rank_b = g.rank_b;
+  for (int i = 0; i <= g.n; ++i) h->row_start[i] = g.row_start[i];
+  for (int i = 0; i < g.n; ++i) h->alphas[i] = g.alphas[i];
   h->gate = d->gate;
   // zero-padded to a multiple of 8 hidden units (16-byte rows of W2): the
   // extra units are relu(0) = 0 and meet zero columns of W2
@@ -156,7 +162,7 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
   A(alloc(&h->sz_pre, (size_t)h->nt128 * h->n_groups * 128 * 4));
   if (r > 0) {
     A(alloc(&h->a_dec, (r / 16) * (K / 16) * 32 * 16));
-    A(alloc(&h->b_dec, (size_t)h->nt16 * (r / 16) * 32 * 16));
+    A(alloc(&h->b_dec, (size_t)h->nt16 * (h->rank_b / 16) * 32 * 16));
     A(alloc(&h->a_pre, r * K * 2));
     A(alloc(&h->b_pre, (size_t)h->nt128 * 128 * r * 2));
   }
@@ -185,7 +191,7 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
 
   spear_status_t st = SPEAR_OK;
   if (cudaMemsetAsync(h->ws, 0, ws_bytes, stream) != cudaSuccess) st = SPEAR_ERR_CUDA;
-  if (st == SPEAR_OK) st = spear_build_layouts(h, d, stream);
+  if (st == SPEAR_OK) st = spear_build_layouts(h, d, g.B_rows, stream);
   if (st == SPEAR_OK && h->gate_hidden > 0) {
     const size_t h8 = h->gate_hidden, hu = d->gate_hidden;
     if (cudaMemsetAsync(h->gate_w1, 0, h8 * r * 2, stream) != cudaSuccess ||
@@ -205,6 +211,107 @@ spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t st
   }
   *out = h;
   return SPEAR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+spear_status_t spear_linear_create(const spear_linear_desc_t* d, cudaStream_t stream, spear_linear_t* out) {
+  if (!out) return SPEAR_ERR_INVALID_ARG;
+  *out = nullptr;
+  spear_status_t v = validate(d);
+  if (v != SPEAR_OK) return v;
+  GroupInfo g;
+  g.rank_b = d->rank;
+  g.row_start[1] = d->N;
+  g.alphas[0] = d->alpha;
+  g.B_rows = d->B;
+  return create_impl(d, g, stream, out);
+}
+
+spear_status_t spear_linear_create_grouped(const spear_linear_desc_t* descs, int32_t n, cudaStream_t stream,
+                                           spear_linear_t* out) {
+  if (!out) return SPEAR_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!descs || n < 1 || n > kMaxGroup) return SPEAR_ERR_INVALID_ARG;
+  if (n == 1) return spear_linear_create(descs, stream, out);
+  const spear_linear_desc_t& d0 = descs[0];
+  int n_tot = 0, max_tokens = 0;
+  bool any_zeros = false;
+  for (int32_t i = 0; i < n; ++i) {
+    const spear_linear_desc_t& d = descs[i];
+    spear_status_t v = validate(&d);
+    if (v != SPEAR_OK) return v;
+    if (d.K != d0.K || d.group_size != d0.group_size || d.rank != d0.rank || d.gate != d0.gate || d.N % 16 != 0)
+      return SPEAR_ERR_INVALID_ARG;
+    if (d.gate == SPEAR_GATE_MLP) return SPEAR_ERR_UNSUPPORTED;
+    n_tot += d.N;
+    max_tokens = d.max_tokens > max_tokens ? d.max_tokens : max_tokens;
+    any_zeros = any_zeros || d.zeros != nullptr;
+  }
+  const int r = d0.rank, K = d0.K, ng = d0.group_size == 0 ? 1 : K / d0.group_size;
+  if (n * r > 256) return SPEAR_ERR_INVALID_ARG;
+  // The members' weights side by side in temporary buffers (freed once the
+  // layouts are built; create_impl synchronises the stream before returning).
+  uint8_t *q = nullptr, *z = nullptr;
+  void *s = nullptr, *A = nullptr, *B = nullptr;
+  cudaError_t e = cudaSuccess;
+  auto chk = [&](cudaError_t x) {
+    if (e == cudaSuccess) e = x;
+  };
+  chk(alloc(&q, (size_t)n_tot * K / 2));
+  chk(alloc(reinterpret_cast<uint8_t**>(&s), (size_t)n_tot * ng * 2));
+  if (any_zeros) chk(alloc(&z, (size_t)n_tot * ng));
+  if (r > 0) {
+    chk(alloc(reinterpret_cast<uint8_t**>(&A), (size_t)n * r * K * 2));
+    chk(alloc(reinterpret_cast<uint8_t**>(&B), (size_t)n_tot * r * 2));
+  }
+  GroupInfo g;
+  g.n = n;
+  g.rank_b = r;
+  g.B_rows = B;
+  size_t row = 0;
+  for (int32_t i = 0; i < n && e == cudaSuccess; ++i) {
+    const spear_linear_desc_t& d = descs[i];
+    g.row_start[i] = (int)row;
+    g.alphas[i] = d.alpha;
+    chk(cudaMemcpyAsync(q + row * K / 2, d.qweight, (size_t)d.N * K / 2, cudaMemcpyDeviceToDevice, stream));
+    chk(cudaMemcpyAsync(static_cast<uint8_t*>(s) + row * ng * 2, d.scales, (size_t)d.N * ng * 2,
+                        cudaMemcpyDeviceToDevice, stream));
+    if (any_zeros)
+      chk(d.zeros ? cudaMemcpyAsync(z + row * ng, d.zeros, (size_t)d.N * ng, cudaMemcpyDeviceToDevice, stream)
+                  : cudaMemsetAsync(z + row * ng, 8, (size_t)d.N * ng, stream));  // no zeros: z = 8
+    if (r > 0) {
+      chk(cudaMemcpyAsync(static_cast<uint8_t*>(A) + (size_t)i * r * K * 2, d.A, (size_t)r * K * 2,
+                          cudaMemcpyDeviceToDevice, stream));
+      chk(cudaMemcpyAsync(static_cast<uint8_t*>(B) + row * r * 2, d.B, (size_t)d.N * r * 2,
+                          cudaMemcpyDeviceToDevice, stream));
+    }
+    row += d.N;
+  }
+  g.row_start[n] = n_tot;
+  spear_status_t st = SPEAR_ERR_CUDA;
+  if (e == cudaSuccess) {
+    spear_linear_desc_t d = d0;
+    d.N = n_tot;
+    d.qweight = q;
+    d.scales = s;
+    d.zeros = z;
+    d.rank = n * r;
+    d.A = A;
+    d.B = B;  // validated as present; the layouts take B from g.B_rows
+    d.max_tokens = max_tokens;
+    st = validate(&d);
+    if (st == SPEAR_OK) st = create_impl(&d, g, stream, out);
+  } else {
+    st = e == cudaErrorMemoryAllocation ? SPEAR_ERR_OOM : SPEAR_ERR_CUDA;
+    cudaGetLastError();
+    cudaStreamSynchronize(stream);
+  }
+  for (void* p : {static_cast<void*>(q), s, static_cast<void*>(z), A, B})
+    if (p) cudaFree(p);
+  return st;
 }
 
 spear_status_t spear_linear_forward_decode(spear_linear_t h, const void* x, void* y, int32_t M,
@@ -242,6 +349,31 @@ spear_status_t spear_linear_forward_host(spear_linear_t h, const void* x_host, v
   if (s != SPEAR_OK) return s;
   if (cudaMemcpyAsync(y_host, h->y_stage, yb, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
     return SPEAR_ERR_CUDA;
+  return cudaStreamSynchronize(stream) == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
+}
+
+spear_status_t spear_linear_forward_host_batch(const spear_linear_t* hs, const void* const* x_host,
+                                               void* const* y_host, const int32_t* Ms, int32_t n,
+                                               cudaStream_t stream) {
+  if (n < 0 || (n > 0 && (!hs || !x_host || !y_host || !Ms))) return SPEAR_ERR_INVALID_ARG;
+  if (n == 0) return SPEAR_OK;
+  // every argument is checked before anything is enqueued
+  for (int32_t i = 0; i < n; ++i) {
+    const spear_linear_t h = hs[i];
+    if (!h || Ms[i] < 0 || Ms[i] > h->max_tokens) return SPEAR_ERR_INVALID_ARG;
+    if (Ms[i] > 0 && (!x_host[i] || !y_host[i])) return SPEAR_ERR_INVALID_ARG;
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    const spear_linear_t h = hs[i];
+    const int32_t M = Ms[i];
+    if (M == 0) continue;
+    if (cudaMemcpyAsync(h->x_stage, x_host[i], (size_t)M * h->K * 2, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+      return SPEAR_ERR_CUDA;
+    spear_status_t s = spear_linear_forward(h, h->x_stage, h->y_stage, M, stream);
+    if (s != SPEAR_OK) return s;
+    if (cudaMemcpyAsync(y_host[i], h->y_stage, (size_t)M * h->N * 2, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+      return SPEAR_ERR_CUDA;
+  }
   return cudaStreamSynchronize(stream) == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
 }
 

@@ -56,10 +56,14 @@ def load(path: Path | None = None):
     L = ctypes.CDLL(str(p))
     H = c_void_p  # opaque handle / stream
     L.spear_linear_create.argtypes = [POINTER(spear_linear_desc_t), H, POINTER(c_void_p)]
+    L.spear_linear_create_grouped.argtypes = [POINTER(spear_linear_desc_t), c_int32, H, POINTER(c_void_p)]
+    L.spear_linear_create_grouped.restype = c_int
     L.spear_linear_forward_decode.argtypes = [H, c_void_p, c_void_p, c_int32, H]
     L.spear_linear_forward_prefill.argtypes = [H, c_void_p, c_void_p, c_int32, H]
     L.spear_linear_forward.argtypes = [H, c_void_p, c_void_p, c_int32, H]
     L.spear_linear_forward_host.argtypes = [H, c_void_p, c_void_p, c_int32, H]
+    L.spear_linear_forward_host_batch.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, H]
+    L.spear_linear_forward_host_batch.restype = c_int
     L.spear_linear_destroy.argtypes = [H]
     L.spear_linear_dequantize.argtypes = [H, c_int32, c_void_p, H]
     L.spear_linear_check.argtypes = [H, H]
@@ -129,6 +133,31 @@ class SpearLinear:
         self.h = h
         self.K, self.N, self.rank, self.max_tokens = int(K), int(N), rank, int(max_tokens)
 
+    @classmethod
+    def grouped(cls, members, max_tokens=32, stream=None):
+        """One handle for linears sharing x (spear_linear_create_grouped).
+        ``members``: list of dicts with the keyword arguments of the
+        constructor (K, N, group_size, qweight, scales, zeros, A, B, alpha,
+        gate). y of the handle is [M][sum of the members' N]."""
+        L = load()
+        n = len(members)
+        arr = (spear_linear_desc_t * n)()
+        for i, m in enumerate(members):
+            A = m.get("A")
+            arr[i] = spear_linear_desc_t(int(m["K"]), int(m["N"]), int(m["group_size"]), _ptr(m["qweight"]),
+                                         _ptr(m["scales"]), _ptr(m.get("zeros")), 0 if A is None else int(A.shape[0]),
+                                         _ptr(A), _ptr(m.get("B")), float(m.get("alpha", 1.0)),
+                                         int(m.get("gate", SPEAR_GATE_SIGMOID)), int(max_tokens), 0, None, None)
+        h = c_void_p()
+        _check(L.spear_linear_create_grouped(arr, n, _stream(stream), byref(h)), "spear_linear_create_grouped")
+        self = cls.__new__(cls)
+        self.h = h
+        self.K = int(members[0]["K"])
+        self.N = sum(int(m["N"]) for m in members)
+        self.rank = 0 if members[0].get("A") is None else int(members[0]["A"].shape[0]) * n
+        self.max_tokens = int(max_tokens)
+        return self
+
     def _io(self, fn, x, y, M, stream, what):
         _check(fn(self.h, _ptr(x), _ptr(y), int(M), _stream(stream)), what)
 
@@ -172,6 +201,19 @@ class SpearLinear:
             pass
 
 
+def forward_host_batch(linears, xs_host, ys_host, stream=None) -> None:
+    """spear_linear_forward_host_batch over (SpearLinear, host x, host y)
+    triples: every call's copies and kernels in order on one stream, one
+    synchronisation at the end."""
+    n = len(linears)
+    hs = (c_void_p * n)(*[lin.h.value for lin in linears])
+    xp = (c_void_p * n)(*[x.data_ptr() for x in xs_host])
+    yp = (c_void_p * n)(*[y.data_ptr() for y in ys_host])
+    ms = (c_int32 * n)(*[int(x.shape[0]) for x in xs_host])
+    _check(load().spear_linear_forward_host_batch(hs, xp, yp, ms, n, _stream(stream)),
+           "spear_linear_forward_host_batch")
+
+
 def from_weights(w, device="cuda", max_tokens=32, alpha=None, gate=None, stream=None) -> SpearLinear:
     """Build a :class:`SpearLinear` from ``workload.LinearWeights`` (host numpy)."""
     import numpy as np
@@ -192,6 +234,28 @@ def from_weights(w, device="cuda", max_tokens=32, alpha=None, gate=None, stream=
                       sp.alpha if alpha is None else alpha, sp.gate if gate is None else gate,
                       max_tokens, stream, W1, W2)
     return lin
+
+
+def grouped_from_weights(ws, device="cuda", max_tokens=32, stream=None) -> SpearLinear:
+    """A grouped :class:`SpearLinear` from several ``workload.LinearWeights``
+    sharing K (host numpy); member i's outputs are columns
+    [N_0 + ... + N_{i-1}, + N_i) of y."""
+    import numpy as np
+    import torch
+
+    def dev(a, dt):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).view(dt).to(device)
+
+    members, keep = [], []
+    for w in ws:
+        sp = w.spec
+        m = {"K": sp.K, "N": sp.N, "group_size": sp.group_size, "qweight": dev(w.q, torch.uint8),
+             "scales": dev(w.s.view(np.int16), torch.bfloat16), "zeros": dev(w.z, torch.uint8),
+             "A": dev(w.A.view(np.int16), torch.bfloat16) if sp.rank else None,
+             "B": dev(w.B.view(np.int16), torch.bfloat16) if sp.rank else None,
+             "alpha": sp.alpha, "gate": sp.gate}
+        members.append(m)
+    return SpearLinear.grouped(members, max_tokens=max_tokens, stream=stream)
 
 
 def quantize_rtn(w, group_size=128, stream=None):

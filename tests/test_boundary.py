@@ -51,6 +51,12 @@ def test_null_arguments(L):
     for fn in (L.spear_linear_forward_decode, L.spear_linear_forward_prefill, L.spear_linear_forward):
         assert fn(None, 16, 32, 1, None) == spear.SPEAR_ERR_INVALID_ARG
     assert L.spear_linear_forward_host(None, 16, 32, 1, None) == spear.SPEAR_ERR_INVALID_ARG
+    assert L.spear_linear_forward_host_batch(None, None, None, None, 1, None) == spear.SPEAR_ERR_INVALID_ARG
+    nulls = (ctypes.c_void_p * 1)(None)
+    ms = (ctypes.c_int32 * 1)(1)
+    assert L.spear_linear_forward_host_batch(nulls, nulls, nulls, ms, 1, None) == spear.SPEAR_ERR_INVALID_ARG
+    assert L.spear_linear_forward_host_batch(None, None, None, None, 0, None) == spear.SPEAR_OK
+    assert L.spear_linear_forward_host_batch(None, None, None, None, -1, None) == spear.SPEAR_ERR_INVALID_ARG
     assert L.spear_linear_dequantize(None, 0, 16, None) == spear.SPEAR_ERR_INVALID_ARG
     assert L.spear_linear_check(None, None) == spear.SPEAR_ERR_INVALID_ARG
     assert L.spear_linear_debug_set(None, 0, 0) == spear.SPEAR_ERR_INVALID_ARG
@@ -73,3 +79,26 @@ def test_noalloc_entry_point_rejects_mlp_gate(L):
     """The allocation-free decode has no MLP gate: refused before any device work."""
     d = _desc(**_MLP)
     assert L.spear_linear_forward_decode_noalloc(ctypes.byref(d), 16, 32, 1, None) == spear.SPEAR_ERR_UNSUPPORTED
+
+
+def test_grouped_create_rejects_incompatible_members(L):
+    """Checked before any device work: members must share K, group size, rank
+    and gate, have N a multiple of 16 and a stacked rank <= 256; the MLP gate
+    is not supported for groups; 1..8 members."""
+    base = dict(K=256, N=64, group_size=128, rank=16, A=16, B=16)
+    cases = [([base, {**base, "K": 512}], spear.SPEAR_ERR_INVALID_ARG),
+             ([base, {**base, "rank": 32, "A": 16, "B": 16}], spear.SPEAR_ERR_INVALID_ARG),
+             ([base, {**base, "group_size": 0}], spear.SPEAR_ERR_INVALID_ARG),
+             ([base, {**base, "N": 72}], spear.SPEAR_ERR_INVALID_ARG),
+             ([base, {**base, "gate": 1}], spear.SPEAR_ERR_INVALID_ARG),
+             ([{**base, "rank": 144}, {**base, "rank": 144}], spear.SPEAR_ERR_INVALID_ARG),
+             ([{**base, **_MLP}, {**base, **_MLP}], spear.SPEAR_ERR_UNSUPPORTED),
+             ([base] * 9, spear.SPEAR_ERR_INVALID_ARG)]
+    for members, want in cases:
+        arr = (spear.spear_linear_desc_t * len(members))(*[_desc(**m) for m in members])
+        h = ctypes.c_void_p(1234)
+        assert L.spear_linear_create_grouped(arr, len(members), None, ctypes.byref(h)) == want, members
+        assert h.value is None
+    h = ctypes.c_void_p()
+    assert L.spear_linear_create_grouped(None, 2, None, ctypes.byref(h)) == spear.SPEAR_ERR_INVALID_ARG
+    assert L.spear_linear_create_grouped(None, 0, None, ctypes.byref(h)) == spear.SPEAR_ERR_INVALID_ARG

@@ -110,3 +110,25 @@ def test_host_entry_rejects_more_tokens_than_the_handle_holds(layer):
     with pytest.raises(spear.SpearError) as ei:
         lin.forward_host(xh, yh)
     assert ei.value.status == spear.SPEAR_ERR_INVALID_ARG
+
+
+def test_host_batch_against_oracle():
+    """spear_linear_forward_host_batch: several handles, one of them twice,
+    token counts on both sides of the dispatch boundary, one synchronisation;
+    every result against the oracle."""
+    ws = [wl.make_weights(sp, 33) for sp in SPECS]
+    lins = [spear.from_weights(w, max_tokens=300) for w in ws]
+    plan = [(0, 1), (1, 32), (2, 300), (0, 33), (1, 8)]
+    xs_bits, xs, ys = [], [], []
+    for i, (li, M) in enumerate(plan):
+        xb = wl.make_x(ws[li].spec.K, M, ws[li].outliers, i, "dp/batch")
+        xs_bits.append(xb)
+        xs.append(torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).view(torch.bfloat16).pin_memory())
+        ys.append(torch.full((M, ws[li].spec.N), float("nan"), dtype=torch.bfloat16).pin_memory())
+    spear.forward_host_batch([lins[li] for li, _ in plan], xs, ys)
+    for i, (li, M) in enumerate(plan):
+        e = rel_err(ys[i].double().numpy(), ref.forward_w(ws[li], xs_bits[i]))
+        assert e <= TOL, f"call {i} (linear {li}, M={M}): rel err {e:.3e}"
+    for lin in lins:
+        assert lin.check() == spear.SPEAR_OK
+        lin.close()
