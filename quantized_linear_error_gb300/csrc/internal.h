@@ -25,7 +25,8 @@
 // per (tile, group).
 //
 // The blocks are ordered for the decode kernel's schedule, fixed at create:
-// CTA c owns tiles [c*P, c*P + Pc) and reads K in runs of 256 channels;
+// CTA c owns tiles [c*P, c*P + P) (nt16 is padded to a whole number of
+// CTAs with zero tiles: rows past N, scale 0) and reads K in runs of 256 channels;
 // everything one CTA needs for one run is contiguous,
 //   [W: Pc tiles x kcw/64 k64 blocks][S: Pc tiles x kcw/128 group blocks]
 // (kcw = channels in the run, 256 except maybe the last; S absent for
@@ -64,7 +65,7 @@ struct spear_linear_s {
   int gate = 0;
   bool per_channel = false;
 
-  int nt16 = 0, nt128 = 0;
+  int nt16 = 0, nt128 = 0;  // decode tiles of 16 rows (padded to whole CTAs), prefill tiles of 128
   // decode schedule (see the layout comment)
   int dec_P = 0;
   size_t dec_tile_bytes = 0;  // one tile over all of K: W blocks plus (grouped) scale blocks
@@ -134,16 +135,34 @@ struct DecodeLayout {
 // Tiles of 16 rows per CTA (grid <= SM count); fixed at create.
 inline int decode_tiles_per_cta(int nt16, int sm_count) { return (nt16 + sm_count - 1) / sm_count; }
 
-// Per-call decode schedule: NW consumer warps (16 when M <= 16, else 8), T
-// tiles per warp, KW warps splitting K, KC channels per pipeline stage (a
-// whole number of layout runs).
+// Per-call decode schedule: NW consumer warps, T tiles per warp, KW warps
+// splitting K, KC channels per pipeline stage (a whole number of layout runs).
+// The consumer warps of a CTA form ceil(P / T) row groups of KW warps each;
+// only instantiated (NW, T) pairs may be chosen (decode_mt*.cu). Register
+// budget: the CTA's NW + 5 warps share four 16K-register files, so 21-23 warps
+// get 80 registers per thread, 20 warps 96 and 15 warps 128.
 inline void decode_plan(int P, int K, int M, int* NW, int* T, int* KW, int* KC) {
-  // M > 16: with one or two tiles per CTA, 8 warps already split K four ways
-  // (measured faster than 16); five tiles take 10 warps (two K warps per tile,
-  // and no register spills, which the 16-warp variant has at M > 16); other
-  // tile counts take 16 warps to keep every warp busy.
-  *NW = (M > 16 && P <= 2) ? 8 : (M > 16 && P == 5) ? 10 : 16;
-  *T = P > *NW ? 2 : 1;
+  if (M > 16) {
+    // four token tiles: one or two tiles take 8 warps (K split four ways,
+    // measured faster than 16); five, six or ten tiles take two, two or one
+    // K warps per tile at up to 128 registers (the 16-warp variant spills);
+    // other tile counts keep 16 warps busy
+    *NW = P <= 2 ? 8 : P == 5 ? 10 : P == 6 ? 12 : P == 10 ? 10 : 16;
+    *T = 1;
+  } else {
+    // every consumer warp busy where the tile count allows: 15 = 3 x 5 or
+    // 5 x 3, 18 = 6 x 3 or 9 x 2, and ten tiles as five pairs (T = 2) with
+    // three K warps each
+    switch (P) {
+      case 3: case 5: *NW = 15; *T = 1; break;
+      case 6: case 9: *NW = 18; *T = 1; break;
+      case 10:  // five tile pairs x three K warps (at M <= 8; the M <= 16 variant spills)
+        *NW = M <= 8 ? 15 : 16;
+        *T = M <= 8 ? 2 : 1;
+        break;
+      default: *NW = 16; *T = 1; break;
+    }
+  }
   const int pw = (P + *T - 1) / *T;  // warps along rows
   *KW = *NW / pw;                    // warps along K; 128-channel units go round-robin
   // Two units per K warp per stage: measured faster than smaller stages,

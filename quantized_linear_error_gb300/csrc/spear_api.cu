@@ -130,13 +130,16 @@ spear_status_t create_impl(const spear_linear_desc_t* d, const GroupInfo& g, cud
   // extra units are relu(0) = 0 and meet zero columns of W2
   h->gate_hidden = d->gate == SPEAR_GATE_MLP ? (d->gate_hidden + 7) / 8 * 8 : 0;
   h->max_tokens = d->max_tokens;
-  h->nt16 = (h->N + 15) / 16;
+  const int nt16_rows = (h->N + 15) / 16;  // 16-row tiles holding output rows
   h->nt128 = (h->N + 127) / 128;
-  if ((h->nt16 + h->sm_count - 1) / h->sm_count > kDecodeMaxTilesPerCta) {
+  if ((nt16_rows + h->sm_count - 1) / h->sm_count > kDecodeMaxTilesPerCta) {
     delete h;
     return SPEAR_ERR_UNSUPPORTED;
   }
-  h->dec_P = decode_tiles_per_cta(h->nt16, h->sm_count);
+  h->dec_P = decode_tiles_per_cta(nt16_rows, h->sm_count);
+  // every decode CTA owns exactly dec_P tiles: the layout is padded with
+  // zero tiles (rows past N, scale 0) up to whole CTAs
+  h->nt16 = (nt16_rows + h->dec_P - 1) / h->dec_P * h->dec_P;
   h->dec_tile_bytes = DecodeLayout{h->K, h->nt16, h->dec_P, h->per_channel}.tile_bytes();
 
   const size_t K = h->K, r = h->rank, mt = h->max_tokens;
