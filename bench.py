@@ -4,17 +4,20 @@ Workload (the decode layer set of a Llama-7B-shaped block, 4-bit group-128
 weights, compensator rank 64 on all seven projections): one step runs the
 seven linears q, k, v, o (4096 -> 4096), gate, up (4096 -> 11008) and down
 (11008 -> 4096) through the fused decode kernel at each of M = 1, 8 and 32
-tokens, i.e. 21 forward calls and 41 tokens. Weights rotate over four copies
-(about 460 MB, more than the 129 MB L2) so that every pass streams its
-weights from HBM. Steps are replayed from CUDA graphs; timing uses CUDA
-events on the launch stream.
+tokens, i.e. 21 linears and 41 tokens. q/k/v and gate/up, which read the same
+x, run as grouped handles (one launch each), so a step is 12 launches; the
+same step with one handle per projection (21 launches) is reported next to
+it. Weights rotate over four copies (about 460 MB, more than the 129 MB L2)
+so that every pass streams its weights from HBM. Steps are replayed from CUDA
+graphs; timing uses CUDA events on the launch stream.
 
 Also reported: the same kernels with the compensator disabled (rank 0), the
-end-to-end rate through spear_linear_forward_host (pinned host buffers, copies
-inside the timed region), the prefill path on the Llama-3-8B MLP at M = 2048,
-the roofline of the decode kernel against the measured HBM copy bandwidth, SM
-clocks sampled during the timed region, and the fp64 CPU oracle timed on a
-bounded sample of the same workload.
+end-to-end rate through the batched host-buffer entry point (pinned host
+buffers, copies inside the timed region, one synchronisation per step), the
+prefill path on the Llama-3-8B MLP at M = 2048 with its EC-off twin, configs
+1, 4 and 5 and the chunk scheduler, the roofline of the decode kernel against
+the measured HBM copy bandwidth, SM clocks sampled during the timed region,
+and the fp64 CPU oracle timed on the whole layer set.
 
 Usage: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 """
@@ -37,6 +40,9 @@ ROOT = Path(__file__).resolve().parent
 sys.path.insert(0, str(ROOT))
 
 DECODE_TOKENS = (1, 8, 32)
+# grouped handles of the layer set: q/k/v (linears 0-2) and gate/up (4-5) read
+# the same x; o (3) and down (6) stand alone
+GROUPS = ((0, 3), (3, 4), (4, 6), (6, 7))
 COPIES = 4
 METRIC = "W4+EC linear: decode tokens/s & HBM GB/s (M=1–32); prefill TFLOP/s vs roofline"
 WORKLOAD = "llama7b decode layer set (q,k,v,o 4096x4096; gate,up 4096->11008; down 11008->4096), INT4 g128, EC r64"
@@ -143,16 +149,28 @@ def decode_bytes(specs, ec=True):
     return total
 
 
-def traffic_from_profile(kernel_src: Path, summary: Path):
-    """dram bytes per launch recorded by an ncu capture, if it was taken on the
-    current kernel source (the summary stores the source's SHA-256)."""
+CSRC = ROOT / "quantized_linear_error_gb300" / "csrc"
+DECODE_SOURCES = [CSRC / f for f in ("decode.cu", "decode_kernel.cuh", "decode_mt1.cu", "decode_mt2.cu",
+                                     "decode_mt4.cu", "internal.h", "common.cuh")]
+
+
+def sources_sha256(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        h.update(Path(p).read_bytes())
+    return h.hexdigest()
+
+
+def traffic_from_profile(kernel_srcs, summary: Path):
+    """dram bytes per step recorded by an ncu capture, if it was taken on the
+    current kernel sources (the summary stores their SHA-256)."""
     if not summary.exists():
         return None
     try:
         d = json.loads(summary.read_text())
     except ValueError:
         return None
-    if d.get("kernel_source_sha256") != hashlib.sha256(kernel_src.read_bytes()).hexdigest():
+    if d.get("kernel_source_sha256") != sources_sha256(kernel_srcs):
         return None
     return d.get("dram_bytes_per_step")
 
@@ -560,31 +578,40 @@ def run_ours(args, world, rank, local):
     def dev(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
 
-    # --- handles: COPIES copies of the layer set, with and without the compensator
-    handles = {True: [], False: []}
+    # --- handles: COPIES copies of the layer set, with and without the
+    # compensator, in two arrangements of the same seven projections:
+    # "grouped" (q/k/v and gate/up, which read the same x, as grouped handles:
+    # 4 launches per token count) and "separate" (one handle per projection:
+    # 7 launches per token count)
+    def no_ec(w):
+        return wl.LinearWeights(wl.LinearSpec(w.spec.name, w.spec.K, w.spec.N, w.spec.group_size, 0), w.q, w.s, w.z,
+                                None, None, w.outliers)
+
+    handles = {(kind, ec): [] for kind in ("grouped", "separate") for ec in (True, False)}
     for c in range(COPIES):
-        for sp in specs:
-            w = wl.make_weights(sp, 100 * rank + c)
-            handles[True].append(spear.from_weights(w, max_tokens=32, stream=stream))
-            w0 = wl.LinearWeights(wl.LinearSpec(sp.name, sp.K, sp.N, sp.group_size, 0), w.q, w.s, w.z, None, None,
-                                  w.outliers)
-            handles[False].append(spear.from_weights(w0, max_tokens=32, stream=stream))
+        ws = [wl.make_weights(sp, 100 * rank + c) for sp in specs]
+        for ec in (True, False):
+            wc = ws if ec else [no_ec(w) for w in ws]
+            handles[("separate", ec)].append([spear.from_weights(w, max_tokens=32, stream=stream) for w in wc])
+            handles[("grouped", ec)].append([spear.grouped_from_weights(wc[i:j], max_tokens=32, stream=stream)
+                                             for i, j in GROUPS])
     outl = {sp.K: wl.outlier_channels(sp.K, 0, sp.name) for sp in specs}
     xs = {(M, K): dev(wl.make_x(K, M, outl[K], rank, f"bench/x{K}")) for M in DECODE_TOKENS for K in (4096, 11008)}
-    ys = {(M, N): torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for M in DECODE_TOKENS for N in (4096, 11008)}
+    out_widths = {h.N for hs in handles[("grouped", True)] + handles[("separate", True)] for h in hs}
+    ys = {(M, N): torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for M in DECODE_TOKENS for N in out_widths}
 
-    def capture(ec, copy, ms=DECODE_TOKENS):
+    def capture(kind, ec, copy, ms=DECODE_TOKENS):
         g = torch.cuda.CUDAGraph()
-        hs = handles[ec][copy * 7:(copy + 1) * 7]
+        hs = handles[(kind, ec)][copy]
         with torch.cuda.stream(stream):
             for M in ms:  # warm (configures the kernels outside capture)
-                for h, sp in zip(hs, specs):
-                    h.forward_decode(xs[(M, sp.K)], ys[(M, sp.N)], stream=stream)
+                for h in hs:
+                    h.forward_decode(xs[(M, h.K)], ys[(M, h.N)], stream=stream)
         stream.synchronize()
         with torch.cuda.graph(g, stream=stream):
             for M in ms:
-                for h, sp in zip(hs, specs):
-                    h.forward_decode(xs[(M, sp.K)], ys[(M, sp.N)], stream=stream)
+                for h in hs:
+                    h.forward_decode(xs[(M, h.K)], ys[(M, h.N)], stream=stream)
         return g
 
     def time_graphs(graphs, steps, warmup):
@@ -604,30 +631,33 @@ def run_ours(args, world, rank, local):
         barrier(world)
         return e0.elapsed_time(e1) / steps  # ms per step
 
-    graphs_ec = [capture(True, c) for c in range(COPIES)]
-    graphs_noec = [capture(False, c) for c in range(COPIES)]
-
+    graphs = {key: [capture(*key, c) for c in range(COPIES)] for key in handles}
     with ClockSampler(local) as clk:
-        ms_step = time_graphs(graphs_ec, args.steps, args.warmup)
+        ms_step = time_graphs(graphs[("grouped", True)], args.steps, args.warmup)
     clocks = clk.summary()
     ms_step = max_over_ranks(ms_step, world)
-    ms_noec = max_over_ranks(time_graphs(graphs_noec, args.steps, args.warmup), world)
-    for h in handles[True] + handles[False]:
-        st = h.check()
-        if st != spear.SPEAR_OK:
-            raise SystemExit(f"device status {spear.status_string(st)}")
+    ms_other = {key: max_over_ranks(time_graphs(graphs[key], args.steps, args.warmup), world)
+                for key in handles if key != ("grouped", True)}
+    ms_noec = ms_other[("grouped", False)]
+    del graphs
+    for hs in sum(handles.values(), []):
+        for h in hs:
+            st = h.check()
+            if st != spear.SPEAR_OK:
+                raise SystemExit(f"device status {spear.status_string(st)}")
 
     tokens = sum(DECODE_TOKENS)
     value = tokens * world / (ms_step / 1e3)
     bytes_step = decode_bytes(specs, True)
-    per_m = {}
-    for M in DECODE_TOKENS:
-        gm = [capture(True, c, (M,)) for c in range(COPIES)]
-        t = time_graphs(gm, max(4, args.steps // 2), 2)
-        b = sum(sp.algorithmic_bytes(M) for sp in specs)
-        per_m[str(M)] = {"tokens_per_s": M / (t / 1e3), "us_per_layer_set": t * 1e3, "hbm_gbs": b / (t / 1e3) / 1e9,
-                         "frac_hbm": b / (t / 1e3) / 1e9 / hbm_peak}
-        del gm
+    per_m, per_m_sep = {}, {}
+    for kind, dst in (("grouped", per_m), ("separate", per_m_sep)):
+        for M in DECODE_TOKENS:
+            gm = [capture(kind, True, c, (M,)) for c in range(COPIES)]
+            t = time_graphs(gm, max(4, args.steps // 2), 3)
+            b = sum(sp.algorithmic_bytes(M) for sp in specs)
+            dst[str(M)] = {"tokens_per_s": M / (t / 1e3), "us_per_layer_set": t * 1e3, "hbm_gbs": b / (t / 1e3) / 1e9,
+                           "frac_hbm": b / (t / 1e3) / 1e9 / hbm_peak}
+            del gm
 
     # --- end to end through the host-buffer entry points: the step's 21 calls
     # with their copies from and to pinned host memory, one synchronisation
@@ -635,24 +665,24 @@ def run_ours(args, world, rank, local):
     # synchronous spear_linear_forward_host per call
     hx = {k: v.cpu().pin_memory() for k, v in xs.items()}
     hy = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in ys.items()}
-    h2d = sum(M * sp.K * 2 for M in DECODE_TOKENS for sp in specs)
-    d2h = sum(M * sp.N * 2 for M in DECODE_TOKENS for sp in specs)
+    # the step's inputs: one x per grouped call (q/k/v read one x, gate/up one x)
+    h2d = sum(M * h.K * 2 for M in DECODE_TOKENS for h in handles[("grouped", True)][0])
+    d2h = sum(M * h.N * 2 for M in DECODE_TOKENS for h in handles[("grouped", True)][0])
 
     def e2e_batch(i):
-        hs = handles[True][(i % COPIES) * 7:(i % COPIES + 1) * 7]
+        hs = handles[("grouped", True)][i % COPIES]
         lins, xl, yl = [], [], []
         for M in DECODE_TOKENS:
-            for h, sp in zip(hs, specs):
+            for h in hs:
                 lins.append(h)
-                xl.append(hx[(M, sp.K)])
-                yl.append(hy[(M, sp.N)])
+                xl.append(hx[(M, h.K)])
+                yl.append(hy[(M, h.N)])
         spear.forward_host_batch(lins, xl, yl, stream=stream)
 
     def e2e_per_call(i):
-        hs = handles[True][(i % COPIES) * 7:(i % COPIES + 1) * 7]
         for M in DECODE_TOKENS:
-            for h, sp in zip(hs, specs):
-                h.forward_host(hx[(M, sp.K)], hy[(M, sp.N)], stream=stream)
+            for h in handles[("grouped", True)][i % COPIES]:
+                h.forward_host(hx[(M, h.K)], hy[(M, h.N)], stream=stream)
 
     def time_host(fn):
         for i in range(args.warmup):
@@ -667,8 +697,8 @@ def run_ours(args, world, rank, local):
     e2e_call_s = time_host(e2e_per_call)
     e2e = {"value": tokens * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "ms_per_step": e2e_s * 1e3,
-           "call": "spear_linear_forward_host_batch: the step's 21 calls with their H2D/D2H copies (pinned host "
-                   "x/y), one synchronisation per step",
+           "call": "spear_linear_forward_host_batch: the step's 12 grouped calls with their H2D/D2H copies "
+                   "(pinned host x/y), one synchronisation per step",
            "per_call_sync": {"value": tokens * world / e2e_call_s, "ms_per_step": e2e_call_s * 1e3,
                              "call": "spear_linear_forward_host per linear (synchronous)"}}
 
@@ -715,13 +745,12 @@ def run_ours(args, world, rank, local):
         configs = measure_other_configs(args, stream, time_graphs, dev, hbm_peak, bf16_peak, not args.skip_config5)
 
     # --- roofline of the decode kernel (the only kernel in the step)
-    launches = len(DECODE_TOKENS) * len(specs)
+    launches = len(DECODE_TOKENS) * len(GROUPS)
     achieved = bytes_step / (ms_step / 1e3) / 1e9
-    traffic = traffic_from_profile(ROOT / "quantized_linear_error_gb300" / "csrc" / "decode.cu",
-                                   ROOT / "profiles" / "decode_kernel_traffic.json")
+    traffic = traffic_from_profile(DECODE_SOURCES, ROOT / "profiles" / "decode_kernel_traffic.json")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                 "traffic": None if traffic is None else traffic / launches,
-                "kernel": "decode_kernel (all 21 launches of a step)",
+                "kernel": f"decode_kernel (all {launches} launches of a step)",
                 "algorithmic_bytes_per_launch": bytes_step / launches, "peak_source": peak_src}
 
     cpu = None
@@ -732,41 +761,53 @@ def run_ours(args, world, rank, local):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
             "config": {"workload": WORKLOAD, "tokens_per_step": list(DECODE_TOKENS), "linears_per_step": 21,
+                       "launches_per_step": launches,
+                       "arrangement": "q/k/v and gate/up (which read the same x) as grouped handles: 4 decode "
+                                      "launches per token count; o and down alone",
                        "l2": f"{COPIES} rotating weight copies (~{COPIES * 115} MB) > 129 MB L2",
                        "graphs": "each step replayed from a CUDA graph", "parallelism": "replicas"},
             "hbm_gbs": achieved, "per_batch": per_m,
             "ec_off": {"ms_per_step": ms_noec, "tokens_per_s": tokens * world / (ms_noec / 1e3),
                        "hbm_gbs": decode_bytes(specs, False) / (ms_noec / 1e3) / 1e9,
                        "ec_overhead": ms_step / ms_noec - 1.0},
+            "separate_handles": {
+                "arrangement": "one handle per projection: 7 decode launches per token count, 21 per step",
+                "ms_per_step": ms_other[("separate", True)],
+                "tokens_per_s": tokens * world / (ms_other[("separate", True)] / 1e3),
+                "frac_hbm": bytes_step / (ms_other[("separate", True)] / 1e3) / 1e9 / hbm_peak,
+                "per_batch": per_m_sep,
+                "ec_off_ms_per_step": ms_other[("separate", False)]},
             "prefill": prefill, "configs": configs, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches * args.steps, "clocks": clocks}
     if rank == 0:
         print(json.dumps(line), flush=True)
-    for h in handles[True] + handles[False]:
-        h.close()
+    for hs in sum(handles.values(), []):
+        for h in hs:
+            h.close()
 
 
 def run_step_case():
-    """One warm-up pass, then one pass of the decode step's 21 launches (the
-    seven config-2 linears with the compensator at M = 1, 8, 32), without
-    graphs: a profiler skips the first 21 decode launches and captures the
-    next 21, i.e. exactly one step."""
+    """One warm-up pass, then one pass of the decode step's 12 launches (the
+    seven config-2 linears with the compensator as the four grouped handles of
+    the timed step, at M = 1, 8, 32), without graphs: a profiler skips the
+    first 12 decode launches and captures the next 12, i.e. exactly one step."""
     import torch
 
     from quantized_linear_error_gb300 import build, spear
     from quantized_linear_error_gb300 import workload as wl
     build.build()
     specs = wl.config_linears(2)
-    hs = [spear.from_weights(wl.make_weights(sp, 0), max_tokens=32) for sp in specs]
+    ws = [wl.make_weights(sp, 0) for sp in specs]
+    hs = [spear.grouped_from_weights(ws[i:j], max_tokens=32) for i, j in GROUPS]
     gen = torch.Generator().manual_seed(0)
     xs = {(M, K): torch.randn((M, K), generator=gen).to(torch.bfloat16).cuda()
           for M in DECODE_TOKENS for K in (4096, 11008)}
-    ys = {(M, N): torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-          for M in DECODE_TOKENS for N in (4096, 11008)}
+    ys = {(M, h.N): torch.empty((M, h.N), dtype=torch.bfloat16, device="cuda")
+          for M in DECODE_TOKENS for h in hs}
     for _ in range(2):
         for M in DECODE_TOKENS:
-            for h, sp in zip(hs, specs):
-                h.forward_decode(xs[(M, sp.K)], ys[(M, sp.N)])
+            for h in hs:
+                h.forward_decode(xs[(M, h.K)], ys[(M, h.N)])
     torch.cuda.synchronize()
     for h in hs:
         if h.check() != spear.SPEAR_OK:

@@ -7,9 +7,6 @@ namespace dec {
 
 DecodeKernelRef kernel_ref_mt2(int NW, int T, bool pc, bool ec) {
   if (NW == 16 && T == 1) return kernel_t<16, 2, 1>(pc, ec);
-  if (NW == 15 && T == 1) return kernel_t<15, 2, 1>(pc, ec);
-  if (NW == 18 && T == 1) return kernel_t<18, 2, 1>(pc, ec);
-  if (NW == 15 && T == 2) return kernel_t<15, 2, 2>(pc, ec);
   return DecodeKernelRef{};
 }
 
