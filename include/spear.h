@@ -137,6 +137,26 @@ spear_status_t spear_linear_forward_decode(spear_linear_t h, const void* x, void
 spear_status_t spear_linear_forward_prefill(spear_linear_t h, const void* x, void* y, int32_t M,
                                             cudaStream_t stream);
 
+/* Prefill with the compensator on a concurrent stream ("SPEAR", section 2.2A:
+ * in the prefill phase the compensator runs as a separate kernel overlapped
+ * with the low-bit GEMM). The same y as spear_linear_forward_prefill, computed
+ * as three launches: the compensator pre-kernel (u' = bf16(alpha gamma(Ax) (.)
+ * Ax)) on ec_stream, forked from `stream` by an event; the main contraction
+ * W x on `stream` into an fp32 buffer of the handle; after an event join, a
+ * K-tail launch that adds alpha B u' to it and rounds to bf16 once. Both
+ * streams are left joined (ec_stream's work precedes `stream`'s later work),
+ * so the call can be captured into one CUDA graph. Requires
+ * spear_linear_enable_concurrent_ec on handles with a compensator (a handle
+ * without one takes the plain prefill path); ec_stream != stream.
+ * Errors: INVALID_ARG, CUDA. */
+spear_status_t spear_linear_forward_prefill_concurrent(spear_linear_t h, const void* x, void* y, int32_t M,
+                                                       cudaStream_t stream, cudaStream_t ec_stream);
+
+/* Allocates what spear_linear_forward_prefill_concurrent needs: an fp32
+ * buffer of max_tokens x N and two events (once; later calls return OK). This
+ * is the only allocation outside create. Errors: INVALID_ARG, OOM, CUDA. */
+spear_status_t spear_linear_enable_concurrent_ec(spear_linear_t h);
+
 /* Phase dispatch ("SPEAR", section 2.2A): decode path for M <= 32, prefill otherwise. */
 spear_status_t spear_linear_forward(spear_linear_t h, const void* x, void* y, int32_t M,
                                     cudaStream_t stream);

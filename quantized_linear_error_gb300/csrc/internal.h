@@ -93,6 +93,10 @@ struct spear_linear_s {
   __nv_bfloat16* gate_w1 = nullptr;  // SPEAR_GATE_MLP: W1 [h8][rank], rows h.. zero
   __nv_bfloat16* gate_w2 = nullptr;  // SPEAR_GATE_MLP: W2 [rank][h8], columns h.. zero
   size_t ws_bytes = 0;               // workspace size (zeroed at create and by a TIMEOUT check)
+  // compensator on a concurrent stream (spear_linear_enable_concurrent_ec):
+  // fp32 main result [max_tokens][N] and the fork / join events
+  float* y32 = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   __nv_bfloat16* x_stage = nullptr;  // host-path staging [max_tokens][K]
   __nv_bfloat16* y_stage = nullptr;  // host-path staging [max_tokens][N]
 
@@ -195,6 +199,8 @@ spear_status_t spear_launch_decode(spear_linear_s* h, const __nv_bfloat16* x, __
 spear_status_t spear_decode_check_residency(spear_linear_s* h);
 spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,
                                     cudaStream_t stream);
+spear_status_t spear_launch_prefill_concurrent(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,
+                                               cudaStream_t stream, cudaStream_t ec_stream);
 // Builds every kernel layout from user-layout weights: q, scales, zeros and A
 // from `d` (A with h->rank rows), B from `B_rows` ([N][h->rank_b], the members'
 // B matrices one after the other).

@@ -86,6 +86,11 @@ struct GemmParams {
   int kps;
   float* part;
   unsigned* part_cnt;
+  // main kernel, compensator on a concurrent stream: the main contraction
+  // writes its fp32 result to y32_out [M][N] instead of y; the K-tail launch
+  // (no W blocks) adds y32_in [M][N] to its accumulator before the rounding
+  float* y32_out;
+  const float* y32_in;
 };
 
 SPEAR_DEVINL void fail(const GemmParams& p) { atomicOr(p.status, kStatusTimeoutPipe); }
@@ -414,7 +419,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                          (size_t)c0 * 128 + 32 * q + lane;
 #pragma unroll
             for (int j = 0; j < 16; ++j) __stcg(dst + j * 128, __uint_as_float(v[j]));
+          } else if (p.y32_out != nullptr) {
+            // fp32 result for the separate compensator K-tail: lane = row n
+            // (consecutive lanes, consecutive addresses), columns = tokens
+            if (row < p.a_rows)
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (b0 + c0 + j < p.b_rows)
+                  __stcg(p.y32_out + (size_t)(b0 + c0 + j) * p.ld_out + row, __uint_as_float(v[j]));
           } else if (row < p.a_rows) {
+            if (p.y32_in != nullptr) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (b0 + c0 + j < p.b_rows)
+                  v[j] = __float_as_uint(__uint_as_float(v[j]) +
+                                         __ldcg(p.y32_in + (size_t)(b0 + c0 + j) * p.ld_out + row));
+            }
             if (leader) {
               // add the other splits' partials, in split order, from shared
               // memory (shared-space loads, all 16 of a split in flight at once)
@@ -467,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (EPI == 0 && !(split && !leader)) {
+    if (EPI == 0 && !(split && !leader) && p.y32_out == nullptr) {
       // 16-byte stores of the staged tile: token m, rows a0 + 8 c8 .. + 7
       // (the barrier is unconditional: every epilogue warp reaches it)
       epilogue_bar();
@@ -628,15 +648,16 @@ static int prefill_tn(int M) {
   return tn < 16 ? 16 : tn;
 }
 
-spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,
-                                    cudaStream_t stream) {
-  const int K = h->K, N = h->N, r = h->rank;
+// Compensator pre-kernel: u' [M][rank] = bf16(alpha gamma(A x) (.) A x).
+// Sets *pre_ctas to the CTAs it runs on.
+static spear_status_t launch_pre(spear_linear_s* h, const __nv_bfloat16* x, int M, cudaStream_t stream,
+                                 int* pre_ctas) {
+  const int K = h->K, r = h->rank;
   CUtensorMap none;
   memset(&none, 0, sizeof none);
   cudaError_t e;
-  int pre_ctas = 0;  // CTAs of the compensator pre-kernel
-
-  if (r > 0) {
+  *pre_ctas = 0;
+  {
     // ---- compensator projection and gate: u' [M][r]
     CUtensorMap mx, ma;
     if (!encode_2d_bf16(&mx, x, K, M, (uint64_t)K * 2, 64, 128) ||
@@ -684,11 +705,23 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
     }
     p.tmem_cols = tmem_cols_for(r);
     const size_t smem = kBarrierBytes + 1024 + (size_t)p.NS * p.stage_bytes;
-    pre_ctas = mt * splits;
+    *pre_ctas = mt * splits;
     e = launch<false, 2>(p, dim3(mt, splits), smem, stream, mx, ma, none, none);
     if (e != cudaSuccess) return SPEAR_ERR_CUDA;
   }
+  return SPEAR_OK;
+}
 
+// Main kernel. mode 0: W x plus the compensator K-tail, bf16 y; mode 1: W x
+// only, fp32 result into h->y32; mode 2: the K-tail only, added to h->y32,
+// bf16 y.
+static spear_status_t launch_main(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,
+                                  cudaStream_t stream, int pre_ctas, int mode) {
+  const int K = h->K, N = h->N;
+  const int r = mode == 1 ? 0 : h->rank;
+  CUtensorMap none;
+  memset(&none, 0, sizeof none);
+  cudaError_t e;
   // ---- main contraction with the compensator K-tail
   const int TN = prefill_tn(M);
   CUtensorMap mx, mut;
@@ -706,7 +739,7 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
   // split that runs the K-tail waits for them (measured slower than no split).
   int ks = 1;
   const int avail = h->sm_count - pre_ctas;
-  if (h->part && r == 0 && tiles < avail) {
+  if (h->part && r == 0 && mode == 0 && tiles < avail) {
     ks = std::min(std::min(4, avail / tiles), kbt / 8);
     if (ks < 1) ks = 1;
   }
@@ -715,8 +748,11 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
   p.part = h->part;
   p.part_cnt = h->part_cnt;
   p.skip_arrive = h->skip_arrive;
-  p.kblocks = kbt;
-  p.kb_total = kbt;
+  p.kblocks = mode == 2 ? 0 : kbt;
+  p.kb_total = mode == 2 ? 0 : kbt;
+  if (mode == 2) p.kps = 0;
+  p.y32_out = mode == 1 ? h->y32 : nullptr;
+  p.y32_in = mode == 2 ? h->y32 : nullptr;
   p.splits = 1;
   p.tail_blocks = (r + 63) / 64;
   p.TN = TN;
@@ -752,4 +788,32 @@ spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, _
   const size_t smem = kBarrierBytes + 1024 + (size_t)p.NS * p.stage_bytes;
   e = launch<true, 0>(p, dim3(h->nt128, ntt, ks), smem, stream, none, mx, none, mut);
   return e == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
+}
+
+spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,
+                                    cudaStream_t stream) {
+  int pre_ctas = 0;
+  if (h->rank > 0) {
+    spear_status_t st = launch_pre(h, x, M, stream, &pre_ctas);
+    if (st != SPEAR_OK) return st;
+  }
+  return launch_main(h, x, y, M, stream, pre_ctas, 0);
+}
+
+// The compensator on a concurrent stream (the pages' semi-fused prefill): the
+// pre-kernel runs on ec_stream next to the main contraction on `stream`, which
+// writes fp32; after the join, the K-tail launch adds alpha B u' and rounds.
+spear_status_t spear_launch_prefill_concurrent(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,
+                                               cudaStream_t stream, cudaStream_t ec_stream) {
+  if (h->rank == 0) return spear_launch_prefill(h, x, y, M, stream);
+  if (cudaEventRecord(h->ev_fork, stream) != cudaSuccess || cudaStreamWaitEvent(ec_stream, h->ev_fork, 0) != cudaSuccess)
+    return SPEAR_ERR_CUDA;
+  int pre_ctas = 0;
+  spear_status_t st = launch_pre(h, x, M, ec_stream, &pre_ctas);
+  if (st != SPEAR_OK) return st;
+  st = launch_main(h, x, y, M, stream, 0, 1);
+  if (st != SPEAR_OK) return st;
+  if (cudaEventRecord(h->ev_join, ec_stream) != cudaSuccess || cudaStreamWaitEvent(stream, h->ev_join, 0) != cudaSuccess)
+    return SPEAR_ERR_CUDA;
+  return launch_main(h, x, y, M, stream, 0, 2);
 }

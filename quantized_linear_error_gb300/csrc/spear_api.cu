@@ -59,10 +59,12 @@ cudaError_t alloc(T** p, size_t bytes) {
 }
 
 void free_all(spear_linear_s* h) {
-  void* ptrs[] = {h->wq_dec, h->sz_dec, h->a_dec,   h->b_dec,   h->wq_pre,  h->sz_pre, h->a_pre,
-                  h->b_pre,  h->ws,     h->x_stage, h->y_stage, h->gate_w1, h->gate_w2};
+  void* ptrs[] = {h->wq_dec, h->sz_dec,  h->a_dec,   h->b_dec,   h->wq_pre,  h->sz_pre, h->a_pre,
+                  h->b_pre,  h->ws,      h->x_stage, h->y_stage, h->gate_w1, h->gate_w2, h->y32};
   for (void* p : ptrs)
     if (p) cudaFree(p);
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
 }
 
 spear_status_t validate(const spear_linear_desc_t* d) {
@@ -333,6 +335,37 @@ spear_status_t spear_linear_forward_prefill(spear_linear_t h, const void* x, voi
   if (v != SPEAR_OK || M == 0) return v;
   return spear_launch_prefill(h, static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), M,
                               stream);
+}
+
+spear_status_t spear_linear_enable_concurrent_ec(spear_linear_t h) {
+  if (!h) return SPEAR_ERR_INVALID_ARG;
+  if (h->y32) return SPEAR_OK;
+  if (h->rank == 0) return SPEAR_OK;  // nothing runs beside the main contraction
+  float* y32 = nullptr;
+  cudaEvent_t a = nullptr, b = nullptr;
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&y32), (size_t)h->max_tokens * h->N * 4);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&a, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&b, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    if (y32) cudaFree(y32);
+    if (a) cudaEventDestroy(a);
+    if (b) cudaEventDestroy(b);
+    return e == cudaErrorMemoryAllocation ? SPEAR_ERR_OOM : SPEAR_ERR_CUDA;
+  }
+  h->y32 = y32;
+  h->ev_fork = a;
+  h->ev_join = b;
+  return SPEAR_OK;
+}
+
+spear_status_t spear_linear_forward_prefill_concurrent(spear_linear_t h, const void* x, void* y, int32_t M,
+                                                       cudaStream_t stream, cudaStream_t ec_stream) {
+  spear_status_t v = check_io(h, x, y, M);
+  if (v != SPEAR_OK || M == 0) return v;
+  if (h->rank > 0 && (!h->y32 || ec_stream == stream)) return SPEAR_ERR_INVALID_ARG;
+  return spear_launch_prefill_concurrent(h, static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y),
+                                         M, stream, ec_stream);
 }
 
 spear_status_t spear_linear_forward(spear_linear_t h, const void* x, void* y, int32_t M, cudaStream_t stream) {

@@ -61,6 +61,10 @@ def load(path: Path | None = None):
     L.spear_linear_forward_decode.argtypes = [H, c_void_p, c_void_p, c_int32, H]
     L.spear_linear_forward_prefill.argtypes = [H, c_void_p, c_void_p, c_int32, H]
     L.spear_linear_forward.argtypes = [H, c_void_p, c_void_p, c_int32, H]
+    L.spear_linear_forward_prefill_concurrent.argtypes = [H, c_void_p, c_void_p, c_int32, H, H]
+    L.spear_linear_forward_prefill_concurrent.restype = c_int
+    L.spear_linear_enable_concurrent_ec.argtypes = [H]
+    L.spear_linear_enable_concurrent_ec.restype = c_int
     L.spear_linear_forward_host.argtypes = [H, c_void_p, c_void_p, c_int32, H]
     L.spear_linear_forward_host_batch.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, H]
     L.spear_linear_forward_host_batch.restype = c_int
@@ -167,6 +171,16 @@ class SpearLinear:
 
     def forward_prefill(self, x, y, stream=None):
         self._io(load().spear_linear_forward_prefill, x, y, x.shape[0], stream, "spear_linear_forward_prefill")
+        return y
+
+    def enable_concurrent_ec(self) -> None:
+        _check(load().spear_linear_enable_concurrent_ec(self.h), "spear_linear_enable_concurrent_ec")
+
+    def forward_prefill_concurrent(self, x, y, stream=None, ec_stream=None):
+        """Prefill with the compensator pre-kernel on ec_stream (a torch stream)."""
+        _check(load().spear_linear_forward_prefill_concurrent(self.h, _ptr(x), _ptr(y), int(x.shape[0]),
+                                                              _stream(stream), _stream(ec_stream)),
+               "spear_linear_forward_prefill_concurrent")
         return y
 
     def forward(self, x, y, stream=None):

@@ -61,6 +61,8 @@ def test_null_arguments(L):
     assert L.spear_linear_check(None, None) == spear.SPEAR_ERR_INVALID_ARG
     assert L.spear_linear_debug_set(None, 0, 0) == spear.SPEAR_ERR_INVALID_ARG
     assert L.spear_linear_destroy(None) == spear.SPEAR_OK
+    assert L.spear_linear_enable_concurrent_ec(None) == spear.SPEAR_ERR_INVALID_ARG
+    assert L.spear_linear_forward_prefill_concurrent(None, 16, 32, 1, None, None) == spear.SPEAR_ERR_INVALID_ARG
 
 
 _MLP = dict(gate=spear.SPEAR_GATE_MLP, rank=16, A=16, B=16, gate_hidden=8, gate_w1=16, gate_w2=32)

@@ -109,3 +109,96 @@ def test_split_wait_times_out_and_recovers():
     lin.debug_set(0, False)
     _check(w, M, lin=lin)
     assert lin.check() == spear.SPEAR_OK
+
+
+# ---------------------------------------------------------------- compensator on a concurrent stream
+def _concurrent(w, M, lin=None, seed=0, graph=False):
+    import torch
+
+    from .helpers import dev_bf16, host_f64
+    sp = w.spec
+    lin = lin or spear.from_weights(w, max_tokens=M)
+    lin.enable_concurrent_ec()
+    xb = wl.make_x(sp.K, M, w.outliers, seed, sp.name)
+    x = dev_bf16(xb)
+    y = torch.full((M, sp.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    s_main, s_ec = torch.cuda.Stream(), torch.cuda.Stream()
+    if graph:
+        lin.forward_prefill_concurrent(x, y, stream=s_main, ec_stream=s_ec)  # warm
+        s_main.synchronize()
+        y.fill_(float("nan"))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s_main):
+            lin.forward_prefill_concurrent(x, y, stream=s_main, ec_stream=s_ec)
+        g.replay()
+    else:
+        lin.forward_prefill_concurrent(x, y, stream=s_main, ec_stream=s_ec)
+    torch.cuda.synchronize()
+    assert lin.check() == spear.SPEAR_OK
+    return host_f64(y), ref.forward_w(w, xb)
+
+
+@pytest.mark.parametrize("M", [33, 300])
+@pytest.mark.parametrize("sp", [SMALL[0], SMALL[1], SMALL[3], SMALL[4]], ids=lambda s: s.name)
+def test_concurrent_compensator_matches_oracle(sp, M):
+    y, yr = _concurrent(wl.make_weights(sp, 16), M)
+    assert rel_err(y, yr) <= TOL
+
+
+@pytest.mark.parametrize("variant", ["ec_only", "alpha30", "gate_one"])
+def test_concurrent_compensator_dominant(variant):
+    w = wl.make_weights(SMALL[3], 17)
+    w = {"ec_only": codes_equal_zeros(w), "alpha30": with_spec(w, alpha=30.0),
+         "gate_one": with_spec(codes_equal_zeros(w), gate=wl.GATE_ONE)}[variant]
+    y, yr = _concurrent(w, 130)
+    assert rel_err(y, yr) <= TOL
+
+
+def test_concurrent_compensator_in_a_graph_and_next_to_the_fused_path():
+    """Captured into one CUDA graph (fork and join by events) and replayed;
+    the result agrees with the fused K-tail path far inside the tolerance
+    (the same u' and the same rounding; only the order of the fp32 sums
+    differs)."""
+    w = wl.make_weights(SMALL[3], 18)
+    lin = spear.from_weights(w, max_tokens=300)
+    y, yr = _concurrent(w, 300, lin=lin, graph=True)
+    assert rel_err(y, yr) <= TOL
+    yf = run(lin, wl.make_x(w.spec.K, 300, w.outliers, 0, w.spec.name), "prefill")
+    assert rel_err(y, yf) <= 2e-3
+
+
+def test_concurrent_compensator_grouped_and_plain_handles():
+    from .test_gpu_grouped import _members
+    ws = _members(46)
+    lin = spear.grouped_from_weights(ws, max_tokens=200)
+    lin.enable_concurrent_ec()
+    import torch
+
+    from .helpers import dev_bf16, host_f64
+    xb = wl.make_x(ws[0].spec.K, 200, ws[0].outliers, 0, "conc/grp")
+    y = torch.empty((200, lin.N), dtype=torch.bfloat16, device="cuda")
+    lin.forward_prefill_concurrent(dev_bf16(xb), y, stream=torch.cuda.Stream(), ec_stream=torch.cuda.Stream())
+    torch.cuda.synchronize()
+    yh, c0 = host_f64(y), 0
+    for w in ws:
+        assert rel_err(yh[:, c0:c0 + w.spec.N], ref.forward_w(w, xb)) <= TOL
+        c0 += w.spec.N
+    # a handle without a compensator takes the plain path (nothing to enable)
+    nw = wl.make_weights(SMALL[2], 19)
+    yp, yr = _concurrent(nw, 100)
+    assert rel_err(yp, yr) <= TOL
+
+
+def test_concurrent_compensator_argument_errors():
+    import torch
+    w = wl.make_weights(SMALL[0], 20)
+    lin = spear.from_weights(w, max_tokens=64)
+    x = torch.zeros((40, w.spec.K), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((40, w.spec.N), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    with pytest.raises(spear.SpearError):  # not enabled
+        lin.forward_prefill_concurrent(x, y, stream=s, ec_stream=torch.cuda.Stream())
+    lin.enable_concurrent_ec()
+    lin.enable_concurrent_ec()  # idempotent
+    with pytest.raises(spear.SpearError):  # the same stream twice
+        lin.forward_prefill_concurrent(x, y, stream=s, ec_stream=s)
