@@ -28,12 +28,9 @@ def nvcc() -> str:
     return cand
 
 
-def flags(debug: bool = False) -> list[str]:
-    f = [ARCH, "-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", f"-I{INCLUDE}", f"-I{CSRC}",
-         "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]
-    if debug:
-        f += ["-DSPEAR_DEBUG=1"]
-    return f
+def flags() -> list[str]:
+    return [ARCH, "-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", f"-I{INCLUDE}", f"-I{CSRC}",
+            "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]
 
 
 def _sources() -> list[Path]:
