@@ -276,6 +276,98 @@ SPEAR_DEVINL void decode_frag_unpack(uint32_t w, uint32_t c_lo, uint32_t c_hi, u
   a[3] = bf16x2_fma(w8 & 0x00F000F0u, k2p126, c_hi);
 }
 
+SPEAR_DEVINL uint32_t pack_bf16x2(float lo, float hi);
+
+// Copy a bf16 [rows][cols] matrix (cols a multiple of 8, 16-byte aligned rows)
+// into shared memory with row stride cols + 8 (16-byte chunks, all loads of a
+// thread's share in flight before any store): the MLP gate's weights.
+SPEAR_DEVINL void stage_rows_padded(__nv_bfloat16* dst, const __nv_bfloat16* src, int rows, int cols, int tid,
+                                    int nthreads) {
+  const int c8 = cols / 8, n = rows * c8;
+  for (int i0 = 0; i0 < n; i0 += 4 * nthreads) {
+    uint4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = i0 + k * nthreads + tid;
+      v[k] = i < n ? __ldg(reinterpret_cast<const uint4*>(src) + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = i0 + k * nthreads + tid;
+      if (i < n) *reinterpret_cast<uint4*>(dst + (i / c8) * (cols + 8) + (i % c8) * 8) = v[k];
+    }
+  }
+}
+
+// Bottleneck-MLP gate logits of one block of 16 tokens by warp MMA (bf16
+// operands, fp32 accumulation), for the gate gamma(z) = sigmoid(W2 relu(W1 z)):
+//   t = relu(z W1^T) (16 x gh),   g = t W2^T (16 x r),
+// rows t0 .. t0 + 15 of z (fp32, shared memory, row stride zst floats; rows
+// past the valid tokens must hold zeros). z enters the first product as bf16
+// hi + lo (two MMAs per step), t the second as bf16. W1 is [gh][r] (row stride
+// w1s elements), W2 [r][gh] (row stride w2s), bf16, in shared or global
+// memory, with gh a multiple of 16 and r of 16 (gh <= 64). The C fragment of a
+// 16 x 8 tile of t is the A fragment of the second product, so t never leaves
+// registers. For each 8-column tile j8 of g in [j8_0, j8_1), out(row, col,
+// g[row][col], g[row][col + 1]) is called for this lane's two pairs: rows
+// t0 + lane / 4 and + 8, columns 8 j8 + 2 (lane % 4) and + 1.
+template <class Out>
+SPEAR_DEVINL void mlp_gate_logits(const float* z, int zst, int t0, int r, int gh, const __nv_bfloat16* W1, int w1s,
+                                  const __nv_bfloat16* W2, int w2s, int lane, int j8_0, int j8_1, Out out) {
+  const int g = lane >> 2, tq = lane & 3;
+  const int nh8 = gh / 8;  // 8-unit tiles of the hidden layer, even
+  float acc1[8][4];
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc1[c][e] = 0.f;
+  for (int k16 = 0; k16 < r / 16; ++k16) {
+    const float* z0 = z + (t0 + g) * zst + k16 * 16 + 2 * tq;
+    const float* z1 = z0 + 8 * zst;
+    const float2 v[4] = {*reinterpret_cast<const float2*>(z0), *reinterpret_cast<const float2*>(z1),
+                         *reinterpret_cast<const float2*>(z0 + 8), *reinterpret_cast<const float2*>(z1 + 8)};
+    uint32_t ah[4], al[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      ah[i] = pack_bf16x2(v[i].x, v[i].y);
+      al[i] = pack_bf16x2(v[i].x - __uint_as_float(ah[i] << 16), v[i].y - __uint_as_float(ah[i] & 0xFFFF0000u));
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      if (c < nh8) {
+        const __nv_bfloat16* w = W1 + (size_t)(c * 8 + g) * w1s + k16 * 16 + 2 * tq;
+        const uint32_t b0 = *reinterpret_cast<const unsigned int*>(w);
+        const uint32_t b1 = *reinterpret_cast<const unsigned int*>(w + 8);
+        mma_bf16_16816(acc1[c], ah, b0, b1);
+        mma_bf16_16816(acc1[c], al, b0, b1);
+      }
+    }
+  }
+  uint32_t ta[4][4];  // relu(t) as A fragments, one per 16 hidden units
+#pragma unroll
+  for (int kh = 0; kh < 4; ++kh) {
+    if (2 * kh < nh8) {
+      ta[kh][0] = pack_bf16x2(fmaxf(acc1[2 * kh][0], 0.f), fmaxf(acc1[2 * kh][1], 0.f));
+      ta[kh][1] = pack_bf16x2(fmaxf(acc1[2 * kh][2], 0.f), fmaxf(acc1[2 * kh][3], 0.f));
+      ta[kh][2] = pack_bf16x2(fmaxf(acc1[2 * kh + 1][0], 0.f), fmaxf(acc1[2 * kh + 1][1], 0.f));
+      ta[kh][3] = pack_bf16x2(fmaxf(acc1[2 * kh + 1][2], 0.f), fmaxf(acc1[2 * kh + 1][3], 0.f));
+    }
+  }
+  for (int j8 = j8_0; j8 < j8_1; ++j8) {
+    float c2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kh = 0; kh < 4; ++kh) {
+      if (2 * kh < nh8) {
+        const __nv_bfloat16* w = W2 + (size_t)(j8 * 8 + g) * w2s + kh * 16 + 2 * tq;
+        mma_bf16_16816(c2, ta[kh], *reinterpret_cast<const unsigned int*>(w),
+                       *reinterpret_cast<const unsigned int*>(w + 8));
+      }
+    }
+    out(t0 + g, j8 * 8 + 2 * tq, c2[0], c2[1]);
+    out(t0 + g + 8, j8 * 8 + 2 * tq, c2[2], c2[3]);
+  }
+}
+
 SPEAR_DEVINL uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

@@ -92,7 +92,11 @@ spear_status_t decode_config(const spear_linear_s* h, int M, DecodeLaunch* out) 
 
   const size_t red_bytes = (size_t)P * KW * 32 * 4 * MT * 4;
   const size_t u_bytes = ec ? (size_t)2 * Mp * (h->rank + 8) * 2 : 0;
-  const size_t mlp_bytes = h->gate_hidden > 0 ? (size_t)M * (h->rank + h->gate_hidden) * 4 : 0;
+  // MLP gate: z^T [M16][rank + 8] fp32, W1 [gh][rank + 8] and W2 [rank][gh + 8] bf16
+  const size_t mlp_bytes =
+      h->gate_hidden > 0 ? (size_t)(Mp < 16 ? 16 : Mp) * (h->rank + 8) * 4 +
+                               ((size_t)h->gate_hidden * (h->rank + 8) + (size_t)h->rank * (h->gate_hidden + 8)) * 2
+                         : 0;
   const size_t pc_bytes = h->per_channel ? (size_t)P * 64 : 0;
   const size_t b_bytes = ec ? (size_t)P * (h->rank_b / 16) * 512 + 16 : 0;
   // barriers, alignment slack, per-channel words, u (hi and lo)

@@ -119,60 +119,70 @@ SPEAR_DEVINL void ec_prefetch(const DecodeParams& p, int ew, int lane) {
 
 // Bottleneck-MLP gate ("SPEAR", section 2.1A: gamma is a bottleneck MLP):
 // u = alpha * sigmoid(W2 relu(W1 z)) (.) z per token, by the four compensator
-// warps on z staged in shared memory (zs [M][rank], hidden ts [M][gh], gh a
-// multiple of 8); u is written split into bf16 hi + lo like the elementwise
-// gates (zero for tokens M..Mp-1, and everywhere if z never arrived).
-SPEAR_DEVINL float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-SPEAR_DEVINL float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// sum_k w[k] v[k] over n = 8 * n8 bf16 weights (16-byte rows) and fp32 values.
-SPEAR_DEVINL float dot_bf16_f32(const uint4* w, const float4* v, int n8) {
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll 4
-  for (int k = 0; k < n8; ++k) {
-    const uint4 wv = __ldg(w + k);
-    const float4 v0 = v[2 * k], v1 = v[2 * k + 1];
-    a0 = fmaf(bf_lo(wv.x), v0.x, a0);
-    a1 = fmaf(bf_hi(wv.x), v0.y, a1);
-    a2 = fmaf(bf_lo(wv.y), v0.z, a2);
-    a3 = fmaf(bf_hi(wv.y), v0.w, a3);
-    a0 = fmaf(bf_lo(wv.z), v1.x, a0);
-    a1 = fmaf(bf_hi(wv.z), v1.y, a1);
-    a2 = fmaf(bf_lo(wv.w), v1.z, a2);
-    a3 = fmaf(bf_hi(wv.w), v1.w, a3);
-  }
-  return (a0 + a1) + (a2 + a3);
+// warps: z is staged transposed in shared memory (zs [M16][rank + 8], token
+// rows M .. M16 - 1 zero, M16 = Mp rounded up to 16) next to W1 and W2 (copied
+// there before the grid-dependency wait, rows padded by 8), the two products
+// run on warp MMAs (mlp_gate_logits), each warp taking one 16-token block and
+// half of the rank columns; u is written split into bf16 hi + lo like the elementwise
+// gates (zero for tokens M .. Mp - 1, and everywhere if z never arrived).
+// One (16-token block, half of the rank columns) item of the MLP gate. Not
+// inlined: its fragments would otherwise raise the register allocation of the
+// whole kernel, consumer loop included.
+template <int Mp>
+__device__ __noinline__ void ec_u_mlp_item(const float* zs, int zst, int tb, int half, int r, int gh, int M,
+                                           float alpha, bool arrived, const __nv_bfloat16* w1s,
+                                           const __nv_bfloat16* w2s, int lane, __nv_bfloat16* uh,
+                                           __nv_bfloat16* ul, int us) {
+  const int nj8 = r / 8;
+  mlp_gate_logits(zs, zst, 16 * tb, r, gh, w1s, r + 8, w2s, gh + 8, lane, half * nj8 / 2, (half + 1) * nj8 / 2,
+                  [&](int m, int j, float g0, float g1) {
+                    if (m >= Mp) return;
+                    const bool live = arrived && m < M;
+                    const float u0 = live ? alpha * zs[m * zst + j] * __fdividef(1.0f, 1.0f + __expf(-g0)) : 0.f;
+                    const float u1 = live ? alpha * zs[m * zst + j + 1] * __fdividef(1.0f, 1.0f + __expf(-g1)) : 0.f;
+                    __nv_bfloat16 h0, l0, h1, l1;
+                    split_bf16(u0, h0, l0);
+                    split_bf16(u1, h1, l1);
+                    uh[m * us + j] = h0;
+                    uh[m * us + j + 1] = h1;
+                    ul[m * us + j] = l0;
+                    ul[m * us + j + 1] = l1;
+                  });
 }
 
 template <int Mp>
-SPEAR_DEVINL void ec_u_mlp(const DecodeParams& p, const float* z, bool arrived, int tid, float* zs, float* ts,
+SPEAR_DEVINL void ec_u_mlp(const DecodeParams& p, const float* z, bool arrived, int ew, int lane, float* zs,
                            __nv_bfloat16* uh, __nv_bfloat16* ul, int us) {
-  constexpr int kThr = kEcWarps * 32;
-  const int r = p.rank, hh = p.gh, M = p.M;
-  for (int i = tid; i < M * r; i += kThr) {
-    const int m = i / r, j = i - m * r;
-    zs[i] = arrived ? __ldcg(z + j * 32 + m) : 0.f;
-  }
-  ec_bar();
-  for (int i = tid; i < M * hh; i += kThr) {
-    const int m = i / hh, c = i - m * hh;
-    ts[i] = fmaxf(dot_bf16_f32(reinterpret_cast<const uint4*>(p.gw1 + (size_t)c * r),
-                               reinterpret_cast<const float4*>(zs + m * r), r / 8), 0.f);
-  }
-  ec_bar();
-  for (int i = tid; i < Mp * r; i += kThr) {
-    const int m = i / r, j = i - m * r;
-    float uval = 0.f;
-    if (arrived && m < M) {
-      const float g = dot_bf16_f32(reinterpret_cast<const uint4*>(p.gw2 + (size_t)j * hh),
-                                   reinterpret_cast<const float4*>(ts + m * hh), hh / 8);
-      uval = p.alpha * zs[m * r + j] * (1.0f / (1.0f + expf(-g)));
+  constexpr int M16 = Mp < 16 ? 16 : Mp;
+  const int r = p.rank, M = p.M, zst = r + 8;
+  // z [rank][32] -> zs [token][rank]: four tokens per float4, eight loads of a
+  // thread in flight before any store (one L2 round trip for M16 <= 32, r <= 256)
+  const int nv = r * (M16 / 4);
+  for (int base = ew * 32 + lane; base < nv; base += 8 * kEcWarps * 32) {
+    float4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int idx = base + k * kEcWarps * 32;
+      const int j = idx / (M16 / 4), m0 = (idx % (M16 / 4)) * 4;
+      v[k] = (arrived && idx < nv && m0 < M) ? __ldcg(reinterpret_cast<const float4*>(z + j * 32 + m0))
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    __nv_bfloat16 hi, lo;
-    split_bf16(uval, hi, lo);
-    uh[m * us + j] = hi;
-    ul[m * us + j] = lo;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int idx = base + k * kEcWarps * 32;
+      if (idx < nv) {
+        const int j = idx / (M16 / 4), m0 = (idx % (M16 / 4)) * 4;
+        const float e[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) zs[(m0 + q) * zst + j] = m0 + q < M ? e[q] : 0.f;
+      }
+    }
   }
+  ec_bar();
+  for (int item = ew; item < (M16 / 16) * 2; item += kEcWarps)
+    ec_u_mlp_item<Mp>(zs, zst, item >> 1, item & 1, r, p.gh, M, p.alpha, arrived,
+                      reinterpret_cast<const __nv_bfloat16*>(zs + M16 * zst),
+                      reinterpret_cast<const __nv_bfloat16*>(zs + M16 * zst) + p.gh * zst, lane, uh, ul, us);
 }
 
 // z += A[:, this CTA's share] x, via warp MMA with A rows as the M side.
@@ -233,10 +243,12 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
   const int us = p.rank + 8;  // bf16 elements per token row of u
   __nv_bfloat16* uh = reinterpret_cast<__nv_bfloat16*>(szpc + (PC ? p.P * 16 : 0));
   __nv_bfloat16* ul = uh + Mp * us;
-  float* zs_mlp = reinterpret_cast<float*>(ul + Mp * us);  // MLP gate: z [M][rank], then hidden [M][gh]
+  float* zs_mlp = reinterpret_cast<float*>(ul + Mp * us);  // MLP gate: z^T [M16][rank + 8]
+  constexpr int M16 = Mp < 16 ? 16 : Mp;
   // B fragments of this CTA's tiles [Pc][rank / 16][32] uint4 (16-byte aligned)
   const uint32_t bbuf_s =
-      (smem_u32(zs_mlp + (p.gh > 0 ? p.M * (p.rank + p.gh) : 0)) + 15u) & ~15u;
+      (smem_u32(zs_mlp + (p.gh > 0 ? M16 * (p.rank + 8) : 0)) +
+       (p.gh > 0 ? (uint32_t)(p.gh * (p.rank + 8) + p.rank * (p.gh + 8)) * 2u : 0u) + 15u) & ~15u;
 
   const uint32_t stages_s = smem_u32(stages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -339,6 +351,14 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
       const int ew = warp - NW - 1;
       volatile int* ec_flag = reinterpret_cast<volatile int*>(smem + 512);
       ec_prefetch(p, ew, lane);
+      if (p.gate == SPEAR_GATE_MLP) {
+        // the MLP gate's weights (constant since create) into shared memory,
+        // after z^T: W1 [gh][rank + 8], then W2 [rank][gh + 8]
+        constexpr int M16 = Mp < 16 ? 16 : Mp;
+        __nv_bfloat16* w1s = reinterpret_cast<__nv_bfloat16*>(zs_mlp + M16 * (p.rank + 8));
+        stage_rows_padded(w1s, p.gw1, p.gh, p.rank, ew * 32 + lane, kEcWarps * 32);
+        stage_rows_padded(w1s + p.gh * (p.rank + 8), p.gw2, p.rank, p.gh, ew * 32 + lane, kEcWarps * 32);
+      }
       asm volatile("griddepcontrol.wait;" ::: "memory");
       // Calls alternate between two z buffers. `epoch` (calls completed so
       // far) is read by every CTA before its arrival and advanced by the last
@@ -385,7 +405,7 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
       ec_bar();
       const bool arrived = *ec_flag != 0;
       if (p.gate == SPEAR_GATE_MLP) {
-        ec_u_mlp<Mp>(p, zc, arrived, ew * 32 + lane, zs_mlp, zs_mlp + p.M * p.rank, uh, ul, us);
+        ec_u_mlp<Mp>(p, zc, arrived, ew, lane, zs_mlp, uh, ul, us);
       } else {
         // u = alpha * gamma(z) * z for 4 tokens per float4 of z ([rank][32] fp32).
         // Kept compact (fast exp and division for the sigmoid, ~1e-6

@@ -76,6 +76,7 @@ struct GemmParams {
   const __nv_bfloat16* gw1;  // pre-kernel, SPEAR_GATE_MLP: W1 [gh][rank]
   const __nv_bfloat16* gw2;  // pre-kernel, SPEAR_GATE_MLP: W2 [rank][gh]
   int gh;
+  int mlp_stage_w;  // pre-kernel, SPEAR_GATE_MLP: W1 and W2 staged in shared memory (they fit)
   int rank;
   float* zacc;          // pre-kernel: fp32 [M][rank] partial sums of z (zero between calls)
   unsigned* tile_done;  // pre-kernel: per 128-token tile, splits finished
@@ -522,37 +523,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       epilogue_bar();
       if (last_split && p.gate == SPEAR_GATE_MLP) {
         // Bottleneck-MLP gate: warp q stages z rows a0 + 32 q .. + 31 in the
-        // (now idle) stage memory, rows padded by 4 floats so that 8 lanes'
-        // float4 reads of one column hit 8 distinct 16-byte bank groups; then
-        // lane l evaluates token row 32 q + l:
-        // t = relu(W1 z), u' = bf16(alpha sigmoid(W2 t) (.) z).
-        const int zst = p.TN + 4, tst = p.gh + 4;
+        // (now idle) stage memory (rows padded by 8 floats: conflict-free
+        // fragment reads), then evaluates the gate for its two 16-token blocks
+        // on warp MMAs (mlp_gate_logits): u' = bf16(alpha sigmoid(W2 relu(W1 z)) (.) z).
+        const int zst = p.TN + 8;
         float* zt = reinterpret_cast<float*>(stages);
-        float* tt = zt + 128 * zst;
         for (int rr = 0; rr < 32; ++rr) {
           const int m = a0 + 32 * q + rr;
           for (int c = lane; c < p.TN; c += 32)
             zt[(32 * q + rr) * zst + c] = m < p.a_rows ? __ldcg(p.zacc + (size_t)m * p.ld_out + c) : 0.f;
         }
-        __syncwarp();
-        const int lr = 32 * q + lane, m = a0 + lr;
-        const float4* zr = reinterpret_cast<const float4*>(zt + lr * zst);
-        float* tr = tt + lr * tst;
-        for (int i = 0; i < p.gh; ++i)
-          tr[i] = fmaxf(dot_bf16_f32(reinterpret_cast<const uint4*>(p.gw1 + (size_t)i * p.TN), zr, p.TN / 8), 0.f);
-        if (m < p.a_rows) {
-          const float* zs = zt + lr * zst;
-          for (int j = 0; j < p.TN; j += 2) {
-            float g[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e)
-              g[e] = dot_bf16_f32(reinterpret_cast<const uint4*>(p.gw2 + (size_t)(j + e) * p.gh),
-                                  reinterpret_cast<const float4*>(tr), p.gh / 8);
-            *reinterpret_cast<uint32_t*>(p.out + (size_t)m * p.ld_out + j) =
-                pack_bf16x2(p.alpha * zs[j] * (1.0f / (1.0f + expf(-g[0]))),
-                            p.alpha * zs[j + 1] * (1.0f / (1.0f + expf(-g[1]))));
-          }
+        // W1 [gh][rank + 8] and W2 [rank][gh + 8] after the 128 z rows when
+        // they fit the stage area, else read from global memory
+        const __nv_bfloat16* w1 = p.gw1;
+        const __nv_bfloat16* w2 = p.gw2;
+        int w1s = p.TN, w2s = p.gh;
+        if (p.mlp_stage_w) {
+          __nv_bfloat16* s1 = reinterpret_cast<__nv_bfloat16*>(zt + 128 * zst);
+          __nv_bfloat16* s2 = s1 + p.gh * (p.TN + 8);
+          stage_rows_padded(s1, p.gw1, p.gh, p.TN, threadIdx.x - 64, 128);
+          stage_rows_padded(s2, p.gw2, p.TN, p.gh, threadIdx.x - 64, 128);
+          w1 = s1;
+          w2 = s2;
+          w1s = p.TN + 8;
+          w2s = p.gh + 8;
         }
+        epilogue_bar();
+        for (int tb = 0; tb < 2; ++tb)
+          mlp_gate_logits(zt, zst, 32 * q + 16 * tb, p.TN, p.gh, w1, w1s, w2, w2s, lane, 0, p.TN / 8,
+                          [&](int lr, int j, float g0, float g1) {
+                            const int m = a0 + lr;
+                            if (m >= p.a_rows) return;
+                            const float* zr = zt + lr * zst;
+                            *reinterpret_cast<uint32_t*>(p.out + (size_t)m * p.ld_out + j) =
+                                pack_bf16x2(p.alpha * zr[j] * (1.0f / (1.0f + expf(-g0))),
+                                            p.alpha * zr[j + 1] * (1.0f / (1.0f + expf(-g1))));
+                          });
         __syncwarp();
         for (int rr = 0; rr < 32; ++rr) {
           const int mm = a0 + 32 * q + rr;
@@ -698,8 +704,14 @@ static spear_status_t launch_pre(spear_linear_s* h, const __nv_bfloat16* x, int 
     p.gw2 = h->gate_w2;
     p.gh = h->gate_hidden;
     if (h->gate_hidden > 0) {
-      // the MLP gate stages 128 z rows and 128 hidden rows in the stage area
-      const size_t need = (size_t)128 * (r + 4) * 4 + (size_t)128 * (h->gate_hidden + 4) * 4;
+      // the MLP gate stages 128 z rows in the stage area, and W1 and W2 after
+      // them if that still fits
+      const size_t need_z = (size_t)128 * (r + 8) * 4;
+      const size_t need_w = need_z + ((size_t)h->gate_hidden * (r + 8) + (size_t)r * (h->gate_hidden + 8)) * 2;
+      const size_t cap = 227 * 1024 - kBarrierBytes - 1024;
+      const int ns_w = (int)((need_w + p.stage_bytes - 1) / p.stage_bytes);
+      p.mlp_stage_w = ns_w <= 8 && (size_t)ns_w * p.stage_bytes <= cap;
+      const size_t need = p.mlp_stage_w ? need_w : need_z;
       while ((size_t)p.NS * p.stage_bytes < need) ++p.NS;
       if (p.NS > 8 || kBarrierBytes + 1024 + (size_t)p.NS * p.stage_bytes > 227 * 1024) return SPEAR_ERR_UNSUPPORTED;
     }

@@ -128,9 +128,9 @@ spear_status_t create_impl(const spear_linear_desc_t* d, const GroupInfo& g, cud
   for (int i = 0; i <= g.n; ++i) h->row_start[i] = g.row_start[i];
   for (int i = 0; i < g.n; ++i) h->alphas[i] = g.alphas[i];
   h->gate = d->gate;
-  // zero-padded to a multiple of 8 hidden units (16-byte rows of W2): the
-  // extra units are relu(0) = 0 and meet zero columns of W2
-  h->gate_hidden = d->gate == SPEAR_GATE_MLP ? (d->gate_hidden + 7) / 8 * 8 : 0;
+  // zero-padded to a multiple of 16 hidden units (one MMA k step): the extra
+  // units are relu(0) = 0 and meet zero columns of W2
+  h->gate_hidden = d->gate == SPEAR_GATE_MLP ? (d->gate_hidden + 15) / 16 * 16 : 0;
   h->max_tokens = d->max_tokens;
   const int nt16_rows = (h->N + 15) / 16;  // 16-row tiles holding output rows
   h->nt128 = (h->N + 127) / 128;
