@@ -854,7 +854,8 @@ def run_step_case():
 def run_case(case: str, reps: int = 5):
     """Run one named linear `reps` times and exit (a target for profilers):
     <decode|prefill>:<linear>:<M>[:noec], <linear> a workload linear name such
-    as c2/q, c2/gate, c3/gate, c4/up; or decode-step (see run_step_case)."""
+    as c2/q, c2/gate, c3/gate, c4/up, c5/L0/q, or a grouped linear of the
+    decode layer set, c2/qkv or c2/gateup; or decode-step (see run_step_case)."""
     import torch
 
     from quantized_linear_error_gb300 import build, spear
@@ -864,14 +865,17 @@ def run_case(case: str, reps: int = 5):
     parts = case.split(":")
     path, name, M = parts[0], parts[1], int(parts[2])
     ec = not (len(parts) > 3 and parts[3] == "noec")
-    sp = next(s for c in (1, 2, 3, 4) for s in wl.config_linears(c) if s.name == name)
+    groups = {"c2/qkv": ("c2/q", "c2/k", "c2/v"), "c2/gateup": ("c2/gate", "c2/up")}
+    names = groups.get(name, (name,))
+    specs = [next(s for c in (1, 2, 3, 4, 5) for s in wl.config_linears(c) if s.name == n) for n in names]
     if not ec:
-        sp = wl.LinearSpec(sp.name, sp.K, sp.N, sp.group_size, 0)
+        specs = [wl.LinearSpec(sp.name, sp.K, sp.N, sp.group_size, 0) for sp in specs]
     build.build()
-    w = wl.make_weights(sp, 0)
-    lin = spear.from_weights(w, max_tokens=max(M, 32))
-    x = torch.from_numpy(wl.make_x(sp.K, M, w.outliers, 0, sp.name).view("int16")).view(torch.bfloat16).cuda()
-    y = torch.empty((M, sp.N), dtype=torch.bfloat16, device="cuda")
+    ws = [wl.make_weights(sp, 0) for sp in specs]
+    lin = (spear.grouped_from_weights(ws, max_tokens=max(M, 32)) if len(ws) > 1
+           else spear.from_weights(ws[0], max_tokens=max(M, 32)))
+    x = torch.from_numpy(wl.make_x(lin.K, M, ws[0].outliers, 0, name).view("int16")).view(torch.bfloat16).cuda()
+    y = torch.empty((M, lin.N), dtype=torch.bfloat16, device="cuda")
     for _ in range(reps):
         getattr(lin, f"forward_{path}")(x, y)
     torch.cuda.synchronize()
