@@ -204,10 +204,10 @@ spear_status_t spear_linear_check(spear_linear_t h, cudaStream_t stream);
  * arrival another CTA waits for, so that the wait must run out:
  *  - decode: the "compensator projection done" arrival (the kernel then leaves
  *    the compensator out of y and latches TIMEOUT);
- *  - prefill, when the main kernel splits K (a handle without compensator and
- *    too few tiles to fill the SMs): the splits' "partial tile stored"
- *    arrival (the split that adds the partials then gives up, writes nothing
- *    for its tile and latches TIMEOUT).
+ *  - prefill, when the main kernel's stream-K schedule splits a tile over
+ *    several CTAs (a handle sized for more than 32 tokens): the "partial tile
+ *    stored" flag of the CTAs that run a tile's later K blocks (the tile's
+ *    owner then gives up, writes nothing for its tile and latches TIMEOUT).
  * The prefill pre-kernel -> main kernel dependency is a stream (programmatic
  * launch) dependency that the hardware resolves; it has no arrival to skip. */
 spear_status_t spear_linear_debug_set(spear_linear_t h, int64_t wait_ns, int32_t skip_arrive);

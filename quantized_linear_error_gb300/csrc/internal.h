@@ -84,11 +84,13 @@ struct spear_linear_s {
   spear::SyncWords* sync = nullptr;
   float* z_dec = nullptr;
   float* z_mma = nullptr;            // warp-MMA decode: z [2][256][32] fp32, alternating by call
-  float* part = nullptr;             // prefill split over K: fp32 partial tiles, at most [sm_count][256][128]
-  unsigned* part_cnt = nullptr;      // prefill split over K: [sm_count] splits finished per tile
-  float* z_pre = nullptr;            // [max_tokens][rank] fp32 (prefill projection)
+  float* part = nullptr;             // prefill stream-K schedule: one fp32 partial tile per CTA, [sm_count][256][128]
+  unsigned* part_cnt = nullptr;      // prefill stream-K schedule: [sm_count] flags, 1 = that CTA's partial is stored
+  float* z_pre = nullptr;            // [ceil(max_tokens / 128) * 128][rank] fp32 (prefill projection; rows past M zero)
   __nv_bfloat16* u_pre = nullptr;    // [max_tokens][rank] bf16 (prefill gated, alpha-scaled)
-  unsigned* pre_done = nullptr;      // [ceil(max_tokens / 128)] split counters of the pre-kernel
+  unsigned* pre_done = nullptr;      // [ceil(max_tokens / 128)] K splits of the projection finished per token tile
+  unsigned* u_ready = nullptr;       // [ceil(max_tokens / 128)] 1 = that token tile's u' is written (prefill)
+  unsigned* pf_done = nullptr;       // prefill main kernel: CTAs finished (the last clears u_ready)
   int gate_hidden = 0;               // SPEAR_GATE_MLP: hidden width h8 = h rounded up to 8
   __nv_bfloat16* gate_w1 = nullptr;  // SPEAR_GATE_MLP: W1 [h8][rank], rows h.. zero
   __nv_bfloat16* gate_w2 = nullptr;  // SPEAR_GATE_MLP: W2 [rank][h8], columns h.. zero

@@ -146,11 +146,15 @@ spear_status_t create_impl(const spear_linear_desc_t* d, const GroupInfo& g, cud
 
   const size_t K = h->K, r = h->rank, mt = h->max_tokens;
   const size_t pre_tiles = (mt + 127) / 128;
-  const size_t ws_base = sizeof(spear::SyncWords) + kZDecFloats * 4 + mt * r * 4 + mt * r * 2 + pre_tiles * 4;
+  // prefill compensator: z [pre_tiles * 128][rank] fp32 (rows past the tokens
+  // stay zero), u' [max_tokens][rank] bf16, per 128-token tile a split
+  // counter and a "u' ready" flag, and the count of finished CTAs
+  const size_t ws_base =
+      sizeof(spear::SyncWords) + kZDecFloats * 4 + pre_tiles * 128 * r * 4 + mt * r * 2 + pre_tiles * 8 + 4;
   const size_t z_mma_off = (ws_base + 127) / 128 * 128;
-  // Prefill splits K when its tiles fill less than one wave: at most sm_count
-  // (split, tile) pairs of 128 rows x 256 tokens in fp32, for handles sized
-  // for more than decode token counts.
+  // Prefill's stream-K schedule: one fp32 partial tile of 128 rows x 256
+  // tokens and one flag per CTA (at most sm_count), for handles sized for
+  // more than decode token counts.
   const bool want_part = mt > (size_t)kDecodeMaxTokens;
   const size_t part_off = z_mma_off + 2 * kZDecFloats * 4;
   const size_t part_floats = want_part ? (size_t)h->sm_count * 128 * 256 : 0;
@@ -191,8 +195,10 @@ spear_status_t create_impl(const spear_linear_desc_t* d, const GroupInfo& g, cud
   h->part = want_part ? reinterpret_cast<float*>(w + part_off) : nullptr;
   h->part_cnt = reinterpret_cast<unsigned*>(w + cnt_off);
   h->z_pre = h->z_dec + kZDecFloats;
-  h->u_pre = reinterpret_cast<__nv_bfloat16*>(h->z_pre + mt * r);
+  h->u_pre = reinterpret_cast<__nv_bfloat16*>(h->z_pre + pre_tiles * 128 * r);
   h->pre_done = reinterpret_cast<unsigned*>(h->u_pre + mt * r);
+  h->u_ready = h->pre_done + pre_tiles;
+  h->pf_done = h->u_ready + pre_tiles;
 
   spear_status_t st = SPEAR_OK;
   if (cudaMemsetAsync(h->ws, 0, ws_bytes, stream) != cudaSuccess) st = SPEAR_ERR_CUDA;

@@ -63,8 +63,8 @@ def test_forward_host(layer, M, pinned):
 
 def test_host_and_device_paths_agree_on_the_prefill_side(layer):
     """Above the boundary both calls run the same prefill kernels on the same
-    handle. Without a compensator they are deterministic (split partials are
-    added in split order), so the host entry point's result is the device
+    handle. Without a compensator they are deterministic (partial tiles are
+    added in CTA order), so the host entry point's result is the device
     entry point's bit for bit; with one, the pre-kernel sums z over its K
     splits with atomics in arbitrary order, so u' may differ by one bf16 ulp
     and y agrees to well inside the tolerance."""

@@ -65,3 +65,15 @@ def test_llama7b_q_projection_sampled_rows(M):
 def test_prefill_llama7b_q_projection_sampled_rows():
     sp = wl.LinearSpec("m/c2q", 4096, 4096, 128, 64, gate=MLP, gate_hidden=16)
     _check(wl.make_weights(sp, 0), 320, "prefill", rows=sample_rows(sp.N, 96))
+
+
+@pytest.mark.parametrize("dominant", [False, True])
+def test_prefill_gate_in_the_main_kernel_prologue(dominant):
+    """4096 -> 11008 at 640 tokens: the projection runs as the main kernel's
+    prologue, and the MLP gate is evaluated there on z staged in shared
+    memory (W_q = 0 in the dominant case, so the gate decides the result)."""
+    sp = wl.LinearSpec("m/c5gate", 4096, 11008, 128, 64, gate=MLP, gate_hidden=16)
+    w = wl.make_weights(sp, 3)
+    if dominant:
+        w = codes_equal_zeros(w)
+    _check(w, 640, "prefill", rows=sample_rows(sp.N, 96, 1))

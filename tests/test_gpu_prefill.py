@@ -72,27 +72,47 @@ def test_config5_linears(idx, M):
     _check(nw, M, rows)
 
 
+@pytest.mark.parametrize("variant", ["plain", "ec_only", "gate_one", "alpha30"])
+@pytest.mark.parametrize("K,N,M", [(4096, 4096, 1088), (4096, 11008, 640)])
+def test_compensator_prologue_in_the_main_kernel(K, N, M, variant):
+    """Shapes where the projection runs as the persistent kernel's prologue
+    (one 128-token item over all of K, gated in tensor memory, u' written
+    by one bulk copy; the owners' K-tail loads wait for the tile's flag),
+    also with W_q = 0 so that the compensator is the whole result."""
+    sp = wl.LinearSpec(f"pro/{K}x{N}", K, N, 128, 64)
+    w = wl.make_weights(sp, 19)
+    w = {"plain": w, "ec_only": codes_equal_zeros(w), "gate_one": with_spec(codes_equal_zeros(w), gate=wl.GATE_ONE),
+         "alpha30": with_spec(w, alpha=30.0)}[variant]
+    rows = sample_rows(N, 96, 3)
+    lin = spear.from_weights(w, max_tokens=M)
+    y1 = _check(w, M, rows, lin=lin)
+    y2 = _check(w, M, rows, lin=lin)  # the "u' ready" flags are cleared for the next call
+    # every sum is in a fixed order (the projection is not split over K): bit for bit
+    np.testing.assert_array_equal(y1, y2)
+
+
 @pytest.mark.parametrize("M", [17, 100, 300])
 @pytest.mark.parametrize("group_size,rank", [(128, 64), (0, 32), (128, 0)])
 def test_split_over_k(M, group_size, rank):
-    """Few row tiles: without a compensator the main kernel splits K (up to
-    four splits) and the last split adds the others' fp32 partials in split
-    order; with one it does not split. Both give the oracle's result."""
+    """Few row tiles: the stream-K schedule splits every tile's K range over
+    two to four CTAs, and each tile's owner adds the others' fp32 partials in
+    CTA order (with a compensator the owner also runs the K-tail). Both give
+    the oracle's result."""
     sp = wl.LinearSpec(f"split/g{group_size}/r{rank}", 4096, 1024, group_size, rank)
     w = wl.make_weights(sp, 14)
     lin = spear.from_weights(w, max_tokens=512)
     y1 = _check(w, M, lin=lin)
     y2 = _check(w, M, lin=lin)  # counters and partials are reused by the next call
     if rank == 0:
-        # the partials are added in split order: repeated calls agree bit for bit
+        # the partials are added in CTA order: repeated calls agree bit for bit
         # (with a compensator, the pre-kernel's atomic split-K sum of z does not)
         np.testing.assert_array_equal(y1, y2)
 
 
 def test_split_wait_times_out_and_recovers():
-    """The K splits skip their "partial tile stored" arrival: the split that
-    adds the partials waits out its 4 x 2 ms limit, writes nothing for its
-    tile and latches TIMEOUT; check() reports it and resets the workspace, and
+    """The CTAs that run a tile's later K blocks skip their "partial tile
+    stored" flag: the tile's owner waits out its 4 x 2 ms limit, writes
+    nothing for its tile and latches TIMEOUT; check() reports it and resets the workspace, and
     the next call on the same handle is correct again. Nothing traps or hangs."""
     import torch
 
@@ -156,15 +176,16 @@ def test_concurrent_compensator_dominant(variant):
 
 def test_concurrent_compensator_in_a_graph_and_next_to_the_fused_path():
     """Captured into one CUDA graph (fork and join by events) and replayed;
-    the result agrees with the fused K-tail path far inside the tolerance
-    (the same u' and the same rounding; only the order of the fp32 sums
-    differs)."""
+    the result agrees with the fused path far inside the tolerance. The two
+    forms split the projection z = A x over K differently, so a u' element
+    (rounded to bf16 once) may differ by one bf16 ulp (2^-8 relative) between
+    them, and y by a few 1e-3 of its largest value."""
     w = wl.make_weights(SMALL[3], 18)
     lin = spear.from_weights(w, max_tokens=300)
     y, yr = _concurrent(w, 300, lin=lin, graph=True)
     assert rel_err(y, yr) <= TOL
     yf = run(lin, wl.make_x(w.spec.K, 300, w.outliers, 0, w.spec.name), "prefill")
-    assert rel_err(y, yf) <= 2e-3
+    assert rel_err(y, yf) <= 5e-3
 
 
 def test_concurrent_compensator_grouped_and_plain_handles():
