@@ -42,9 +42,10 @@
 // Rows are grouped in tiles of 128; for a tile and a block of 64 channels the
 // 4 KB block holds, per row, eight u32 words; word c packs channels
 // 8c .. 8c+7 with nibble order (0, 2, 4, 6, 1, 3, 5, 7) so that
-// (w >> 4j) & 0x000F000F yields channels (2j, 2j+1) as a bf16 pair.
-//   wq_pre  u32   [nt128][K/64][128][8]
-//   sz_pre  u32   [nt128][n_groups][128] same encoding as sz_dec
+// (w >> 4j) & 0x000F000F yields channels (2j, 2j+1) as a bf16 pair. The
+// block's 128 scale/zero words (same encoding as sz_dec, of the group that
+// holds the block) follow it, so one bulk copy brings a block's input.
+//   wq_pre  u32   [nt128][K/64][1024 + 128]
 //   a_pre   bf16  [rank][K]               copy of A
 //   b_pre   bf16  [nt128*128][rank]       copy of B, zero rows past N
 
@@ -74,7 +75,6 @@ struct spear_linear_s {
   uint4* a_dec = nullptr;
   uint4* b_dec = nullptr;
   uint32_t* wq_pre = nullptr;
-  uint32_t* sz_pre = nullptr;
   __nv_bfloat16* a_pre = nullptr;
   __nv_bfloat16* b_pre = nullptr;
 
@@ -107,6 +107,7 @@ struct spear_linear_s {
 };
 
 constexpr int kDecodeMaxTokens = 32;
+constexpr int kPrefillBlockWords = 1024 + 128;  // prefill layout: a block's code words, then its scale/zero words
 constexpr int kMaxGateHidden = 64;  // widest hidden layer of the MLP gate
 
 constexpr int kDecodeRun = 256;  // channels per layout run

@@ -53,6 +53,8 @@ __global__ void repack_sz_decode(const uint16_t* __restrict__ s, const uint8_t* 
   }
 }
 
+// Prefill layout: per (row tile, 64-channel block) 1024 code words, then the
+// block's 128 scale/zero words (kPrefillBlockWords in all).
 __global__ void repack_w_prefill(const uint8_t* __restrict__ q, int K, int N, int nt128, uint32_t* __restrict__ out) {
   const int kb64 = K / 64;
   const long total = (long)nt128 * kb64 * 128 * 8;
@@ -69,7 +71,23 @@ __global__ void repack_w_prefill(const uint8_t* __restrict__ q, int K, int N, in
       w |= user_code(q, K, N, row, k + 2 * j) << (4 * j);
       w |= user_code(q, K, N, row, k + 2 * j + 1) << (16 + 4 * j);
     }
-    out[i] = w;
+    out[((long)tile * kb64 + kb) * kPrefillBlockWords + (i % 1024)] = w;
+  }
+}
+
+// The scale/zero words of the prefill blocks: block (tile, kb), row rl holds
+// the word of the group of channels kb * 64 (the same word in both blocks of
+// a 128-channel group, and in every block of a per-channel row).
+__global__ void repack_sz_prefill(const uint16_t* __restrict__ s, const uint8_t* __restrict__ z, int K, int G,
+                                  int n_groups, int N, int nt128, uint32_t* __restrict__ out) {
+  const int kb64 = K / 64;
+  const long total = (long)nt128 * kb64 * 128;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+    const int rl = i % 128;
+    const int kb = (i / 128) % kb64;
+    const int tile = i / (128L * kb64);
+    out[((long)tile * kb64 + kb) * kPrefillBlockWords + 1024 + rl] =
+        user_sz(s, z, n_groups, N, tile * 128 + rl, (kb * 64) / G);
   }
 }
 
@@ -187,8 +205,8 @@ __global__ void dequant_from_decode(const uint8_t* __restrict__ wq, const uint32
   }
 }
 
-__global__ void dequant_from_prefill(const uint32_t* __restrict__ wq, const uint32_t* __restrict__ sz, int K,
-                                     int N, int nt128, int G, int n_groups, __nv_bfloat16* __restrict__ out) {
+__global__ void dequant_from_prefill(const uint32_t* __restrict__ wq, int K, int N, int nt128,
+                                     __nv_bfloat16* __restrict__ out) {
   const int kb64 = K / 64;
   const long total = (long)nt128 * kb64 * 1024;
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
@@ -199,10 +217,11 @@ __global__ void dequant_from_prefill(const uint32_t* __restrict__ wq, const uint
     const int row = tile * 128 + rl;
     if (row >= N) continue;
     const int k = kb * 64 + c * 8;
-    const uint32_t szw = sz[((size_t)tile * n_groups + k / G) * 128 + rl];
+    const uint32_t* blk = wq + ((size_t)tile * kb64 + kb) * kPrefillBlockWords;
+    const uint32_t szw = blk[1024 + rl];
     const uint32_t zz = biased_zero_x2(szw >> 16);
     const float s = bf16_bits_to_float(szw & 0xFFFF);
-    const uint32_t w = wq[i];
+    const uint32_t w = blk[i % 1024];
     __align__(16) __nv_bfloat16 v[8];
     for (int j = 0; j < 4; ++j) {
       const uint32_t d = bf16x2_sub(int4_pair_to_bf16x2_biased(w >> (4 * j)), zz);
@@ -241,8 +260,8 @@ spear_status_t spear_build_layouts(spear_linear_s* h, const spear_linear_desc_t*
   }
   n = (long)h->nt128 * (K / 64) * 1024;
   repack_w_prefill<<<grid_for(n, T), T, 0, st>>>(d->qweight, K, N, h->nt128, h->wq_pre);
-  n = (long)h->nt128 * h->n_groups * 128;
-  repack_sz<<<grid_for(n, T), T, 0, st>>>(s, d->zeros, h->n_groups, N, h->nt128, 128, h->sz_pre);
+  n = (long)h->nt128 * (K / 64) * 128;
+  repack_sz_prefill<<<grid_for(n, T), T, 0, st>>>(s, d->zeros, K, h->G, h->n_groups, N, h->nt128, h->wq_pre);
   if (r > 0) {
     const uint16_t* A = static_cast<const uint16_t*>(d->A);
     const uint16_t* B = static_cast<const uint16_t*>(B_rows);
@@ -274,8 +293,7 @@ spear_status_t spear_launch_dequant(spear_linear_s* h, int path, __nv_bfloat16* 
     dequant_from_decode<<<grid_for(n, T), T, 0, st>>>(h->wq_dec, h->sz_dec, h->K, h->N, L, out);
   } else {
     long n = (long)h->nt128 * (h->K / 64) * 1024;
-    dequant_from_prefill<<<grid_for(n, T), T, 0, st>>>(h->wq_pre, h->sz_pre, h->K, h->N, h->nt128, h->G,
-                                                       h->n_groups, out);
+    dequant_from_prefill<<<grid_for(n, T), T, 0, st>>>(h->wq_pre, h->K, h->N, h->nt128, out);
   }
   return cudaGetLastError() == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
 }

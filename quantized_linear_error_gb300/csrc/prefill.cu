@@ -66,12 +66,15 @@ namespace {
 constexpr int kThreads = 192;
 constexpr int kATileBytes = 128 * 128;           // 128 rows x 64 bf16
 constexpr int kRawWBytes = 128 * 8 * 4;          // 128 rows x 64 codes, packed
-constexpr int kRawBytes = kRawWBytes + 128 * 4;  // plus one scale/zero word per row
+constexpr int kRawBytes = kRawWBytes + 128 * 4;  // plus one scale/zero word per row (one prefill-layout block)
+static_assert(kRawBytes == kPrefillBlockWords * 4, "a stage's raw input is one prefill-layout block");
 constexpr int kBarrierBytes = 1024;
-constexpr int kMaxStages = 6;
+constexpr int kMaxStages = 6;       // pre-kernel
+constexpr int kMaxMainStages = 16;  // main kernel (barrier arrays of 16)
 constexpr uint32_t kHintNs = 100;  // suspend-time hint of the pipeline waits
-constexpr uint32_t kTmemA = 256;   // main kernel: A operand of stage s at column 256 + 32 s (after the accumulator)
-static_assert(kTmemA + 32 * kMaxStages <= 512, "the A slots of every stage fit in tensor memory");
+// Main kernel: the accumulator takes columns 0 .. TN - 1 of the 512 TMEM
+// columns and stage s's A operand columns tmem_a + 32 s (tmem_a = TN rounded
+// up to 32), so small token tiles leave room for more stages.
 constexpr int kSlotFloats = 256 * 128;  // one partial tile: [256 columns][128 rows] fp32
 // Dynamic shared memory of at least this much keeps a second CTA of either
 // kernel off the SM (each allocates tensor memory for the whole launch).
@@ -113,15 +116,14 @@ struct MainParams {
   uint32_t units;  // all tiles' units
   int TN;          // tokens per tile = MMA N (multiple of 16, <= 256)
   int N, M;
-  const uint32_t* wq;  // prefill-layout packed W
-  const uint32_t* sz;  // prefill-layout scale/zero words
-  int n_groups, G;
+  const uint32_t* wq;  // prefill-layout blocks: packed W, then the block's scale/zero words
   __nv_bfloat16* out;  // y [M][N]
   unsigned* status;
   uint64_t wait_ns;
   int skip_arrive;  // test surface: contributors skip raising their flag
   int late_wait;    // u' comes from the pre-kernel launched just before: only the K-tail loads wait for it
   int NS;
+  uint32_t tmem_a;  // first TMEM column of the stages' A slots (after the accumulator)
   uint32_t b_bytes, stage_bytes;
   const __nv_bfloat16* bt;  // compensator B rows [nt128 * 128][rank] (the K-tail's A operand)
   int rank;
@@ -202,6 +204,21 @@ SPEAR_DEVINL bool warp_wait(uint64_t* bar, unsigned parity, uint64_t limit_ns, u
   const bool ok =
       hint_ns ? mbar_wait_bounded_hint(bar, parity, limit_ns, hint_ns) : mbar_wait_bounded(bar, parity, limit_ns);
   return __all_sync(0xffffffffu, ok);
+}
+
+// Non-blocking test of an mbarrier phase (the producer's stage is usually
+// free long before it is reused: a blocking try_wait cost it ~200 cycles per
+// block even then).
+SPEAR_DEVINL bool mbar_test_wait(uint64_t* bar, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 
 // Spin (bounded) until *flag is nonzero; acquire.
@@ -515,12 +532,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the stage have completed. acc_full completes one phase per prologue item
   // and per segment; part_bar one per pass over the owner's partials.
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* raw_full = full + 8;
-  uint64_t* empty = full + 16;
-  uint64_t* acc_full = full + 24;
-  uint64_t* part_bar = full + 32;
-  uint64_t* pro_done = full + 33;  // a prologue item's epilogue is done: the stage memory is free
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 384);
+  uint64_t* raw_full = full + kMaxMainStages;
+  uint64_t* empty = full + 2 * kMaxMainStages;
+  uint64_t* acc_full = full + 3 * kMaxMainStages;
+  uint64_t* part_bar = acc_full + 1;
+  uint64_t* pro_done = acc_full + 2;  // a prologue item's epilogue is done: the stage memory is free
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 448);
   volatile int& epi_bad = *reinterpret_cast<volatile int*>(smem + 512);  // an epilogue warp gave up
   uint8_t* stages = smem + kBarrierBytes;
   const uint32_t stages_s = smem_u32(stages);
@@ -575,7 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         for (int i = 0; i < p.kbt; ++i, ++it) {
-          if (it >= p.NS && !mbar_wait_bounded_hint(&empty[s], ph ^ 1u, p.wait_ns, kHintNs)) {
+          if (it >= p.NS && !mbar_test_wait(&empty[s], ph ^ 1u) &&
+              !mbar_wait_bounded_hint(&empty[s], ph ^ 1u, p.wait_ns, kHintNs)) {
             fail(p.status);
             bad = true;
             break;
@@ -601,7 +619,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rt = g.tile % p.nt128, b0 = (g.tile / p.nt128) * p.TN;
         if (g.ntail > 0) prefetch_l2(p.bt + (size_t)rt * 128 * p.rank, 128u * p.rank * 2u);
         for (int i = 0; i < g.nw + g.ntail; ++i, ++it) {
-          if (it >= p.NS && !mbar_wait_bounded_hint(&empty[s], ph ^ 1u, p.wait_ns, kHintNs)) {
+          if (it >= p.NS && !mbar_test_wait(&empty[s], ph ^ 1u) &&
+              !mbar_wait_bounded_hint(&empty[s], ph ^ 1u, p.wait_ns, kHintNs)) {
             fail(p.status);
             bad = true;
             break;
@@ -611,8 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (i < g.nw) {
             const int kb = g.wb0 + i;
             mbar_arrive_expect_tx(&raw_full[s], kRawBytes);
-            bulk_g2s(raw, p.wq + ((size_t)rt * p.kbt + kb) * 1024, kRawWBytes, &raw_full[s]);
-            bulk_g2s(raw + kRawWBytes, p.sz + ((size_t)rt * p.n_groups + (kb * 64) / p.G) * 128, 512, &raw_full[s]);
+            bulk_g2s(raw, p.wq + ((size_t)rt * p.kbt + kb) * kPrefillBlockWords, kRawBytes, &raw_full[s]);
             mbar_arrive_expect_tx(&full[s], p.b_bytes);
             tma_load_2d(B, &mapX, kb * 64, b0, &full[s]);
           } else {
@@ -689,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // A from tensor memory: 8 columns (16 channels) per k16 step
 #pragma unroll
           for (int k16 = 0; k16 < 4; ++k16)
-            umma_ts_bf16(tmem_d, tmem_d + kTmemA + 32 * s + 8 * k16, sw128_kmajor_desc(b_s + 32 * k16), idesc,
+            umma_ts_bf16(tmem_d, tmem_d + p.tmem_a + 32 * s + 8 * k16, sw128_kmajor_desc(b_s + 32 * k16), idesc,
                          (i | k16) != 0);
           umma_commit(&empty[s]);
           b_s += p.stage_bytes;
@@ -852,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(&full[pending]);
         }
         tc_fence_after_sync();
-        tmem_st_x32(lane_base + kTmemA + 32 * s, v);
+        tmem_st_x32(lane_base + p.tmem_a + 32 * s, v);
         pending = s;
         raw_sa += p.stage_bytes;
         if (++s == p.NS) {
@@ -1011,10 +1029,10 @@ cudaError_t launch(Kernel k, std::atomic<uint64_t>& configured, const Params& p,
 }
 
 // Stages that fit next to the barriers.
-int stages_for(uint32_t stage_bytes) {
+int stages_for(uint32_t stage_bytes, int max_stages = kMaxStages) {
   const size_t budget = 227 * 1024 - kBarrierBytes - 1024;
   int ns = (int)(budget / stage_bytes);
-  return ns > kMaxStages ? kMaxStages : ns;
+  return ns > max_stages ? max_stages : ns;
 }
 
 uint32_t host_range_start(const MainParams& p, uint32_t c, uint32_t G) { return range_start_of(p, c, G); }
@@ -1139,9 +1157,6 @@ static spear_status_t launch_main(spear_linear_s* h, const __nv_bfloat16* x, __n
   p.N = N;
   p.M = M;
   p.wq = h->wq_pre;
-  p.sz = h->sz_pre;
-  p.n_groups = h->n_groups;
-  p.G = h->G;
   p.out = y;
   p.status = &h->sync->status;
   p.wait_ns = h->wait_ns;
@@ -1160,7 +1175,8 @@ static spear_status_t launch_main(spear_linear_s* h, const __nv_bfloat16* x, __n
   uint32_t stage = (p.b_bytes + kRawBytes + 1023) / 1024 * 1024;
   if (prologue) stage = std::max<uint32_t>(stage, kATileBytes + (uint32_t)(r * 128 + 1023) / 1024 * 1024);
   p.stage_bytes = stage;
-  p.NS = stages_for(p.stage_bytes);
+  p.tmem_a = (uint32_t)(TN + 31) / 32 * 32;
+  p.NS = stages_for(p.stage_bytes, std::min<int>(kMaxMainStages, (int)(512 - p.tmem_a) / 32));
   // CTAs: one per tile for the K-tail-only launch and for handles without a
   // partial workspace (sized for decode token counts). Otherwise every SM,
   // with at least max(8, tail + 2, kpt / 3) units each (so that every range

@@ -59,7 +59,7 @@ cudaError_t alloc(T** p, size_t bytes) {
 }
 
 void free_all(spear_linear_s* h) {
-  void* ptrs[] = {h->wq_dec, h->sz_dec,  h->a_dec,   h->b_dec,   h->wq_pre,  h->sz_pre, h->a_pre,
+  void* ptrs[] = {h->wq_dec, h->sz_dec,  h->a_dec,   h->b_dec,   h->wq_pre,  h->a_pre,
                   h->b_pre,  h->ws,      h->x_stage, h->y_stage, h->gate_w1, h->gate_w2, h->y32};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -167,8 +167,7 @@ spear_status_t create_impl(const spear_linear_desc_t* d, const GroupInfo& g, cud
   };
   A(alloc(&h->wq_dec, (size_t)h->nt16 * h->dec_tile_bytes));
   if (h->per_channel) A(alloc(&h->sz_dec, (size_t)h->nt16 * 16 * 4));
-  A(alloc(&h->wq_pre, (size_t)h->nt128 * (K / 64) * 1024 * 4));
-  A(alloc(&h->sz_pre, (size_t)h->nt128 * h->n_groups * 128 * 4));
+  A(alloc(&h->wq_pre, (size_t)h->nt128 * (K / 64) * kPrefillBlockWords * 4));
   if (r > 0) {
     A(alloc(&h->a_dec, (r / 16) * (K / 16) * 32 * 16));
     A(alloc(&h->b_dec, (size_t)h->nt16 * (h->rank_b / 16) * 32 * 16));
