@@ -46,8 +46,9 @@
 // that runs it on a concurrent stream: there the main kernel writes its fp32
 // sum, and a K-tail-only launch of it adds alpha B u' after the join.
 //
-// Warp roles: warp 0 issues TMA (one thread) and owns the TMEM allocation,
-// warp 1 issues tcgen05.mma (one thread), warps 2-5 dequantise and run the
+// Warp roles: warp 0 owns the TMEM allocation and issues copies (one thread:
+// in the main kernel the packed W; there warp 6 issues the x copies), warp 1
+// issues tcgen05.mma (one thread), warps 2-5 dequantise and run the
 // epilogues (warp w reads TMEM lanes 32 (w % 4) .. + 31). Every mbarrier and
 // flag wait is bounded; a timeout latches the handle's status word and the
 // CTA runs through its remaining barriers without touching data. The MMA
@@ -63,7 +64,8 @@
 namespace spear {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;      // pre-kernel: TMA, MMA, four epilogue warps
+constexpr int kMainThreads = 224;  // main kernel: W producer, MMA, four dequantising warps, x producer
 constexpr int kATileBytes = 128 * 128;           // 128 rows x 64 bf16
 constexpr int kRawWBytes = 128 * 8 * 4;          // 128 rows x 64 codes, packed
 constexpr int kRawBytes = kRawWBytes + 128 * 4;  // plus one scale/zero word per row (one prefill-layout block)
@@ -513,10 +515,117 @@ SPEAR_DEVINL void store_out(const MainParams& p, int row, int b0, int c0, float 
   }
 }
 
+// ------------------------------------------------------------------ main kernel: producers
+// The stages are filled by two threads in different warps, stepping the same
+// sequence of K blocks: the W producer (X = false) brings each block's packed
+// W and scale/zero words (raw_full[s]; a plain arrival for prologue and
+// K-tail blocks), the x producer (X = true) the B operand (full[s]: x, u' or,
+// in the prologue, x and the compensator's A). One thread issuing both was
+// the pace-setter of the whole kernel (~700 cycles per block against 512 of
+// MMA at 256 tokens). Both wait for a stage's MMAs (empty[s]) before
+// refilling it, and for each prologue item's epilogue (pro_done), which uses
+// the stage memory, before the next item or the main contraction.
+template <bool X>
+SPEAR_DEVINL void produce(const MainParams& p, const CUtensorMap* mapX, const CUtensorMap* mapU,
+                          const CUtensorMap* mapXp, const CUtensorMap* mapA, uint8_t* stages, uint64_t* full,
+                          uint64_t* raw_full, uint64_t* empty, uint64_t* pro_done, uint32_t ub, uint32_t ue) {
+  const uint32_t pro_a_bytes = kATileBytes;  // prologue stage: x tile, then the A tile
+  int s = 0;
+  unsigned ph = 0;
+  bool waited = !X || !p.late_wait;
+  int it = 0;
+  bool bad = false;
+  int k = 0;
+  for (int item = blockIdx.x; item < p.pro_items && !bad; item += gridDim.x, ++k) {
+    if (k > 0 && !mbar_wait_bounded(pro_done, (unsigned)((k - 1) & 1), 8 * p.wait_ns)) {
+      fail(p.status);
+      bad = true;
+      break;
+    }
+    for (int i = 0; i < p.kbt; ++i, ++it) {
+      if (it >= p.NS && !mbar_test_wait(&empty[s], ph ^ 1u) &&
+          !mbar_wait_bounded_hint(&empty[s], ph ^ 1u, p.wait_ns, kHintNs)) {
+        fail(p.status);
+        bad = true;
+        break;
+      }
+      if (X) {
+        uint8_t* st = stages + (size_t)s * p.stage_bytes;
+        mbar_arrive_expect_tx(&full[s], pro_a_bytes + (uint32_t)p.rank * 128u);
+        tma_load_2d(st, mapXp, i * 64, item * 128, &full[s]);
+        tma_load_2d(st + pro_a_bytes, mapA, i * 64, 0, &full[s]);
+      } else {
+        mbar_arrive(&raw_full[s]);
+      }
+      if (++s == p.NS) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+  }
+  if (!bad && k > 0 && !mbar_wait_bounded(pro_done, (unsigned)((k - 1) & 1), 8 * p.wait_ns)) {
+    fail(p.status);
+    bad = true;
+  }
+  for (uint32_t u = ub; u < ue && !bad;) {
+    const Segment g = segment_at(p, u, ue);
+    u += g.len;
+    const int rt = g.tile % p.nt128, b0 = (g.tile / p.nt128) * p.TN;
+    if (!X && g.ntail > 0) prefetch_l2(p.bt + (size_t)rt * 128 * p.rank, 128u * p.rank * 2u);
+    const uint32_t* wsrc = p.wq + ((size_t)rt * p.kbt + g.wb0) * kPrefillBlockWords;
+    for (int i = 0; i < g.nw + g.ntail; ++i, ++it) {
+      if (it >= p.NS && !mbar_test_wait(&empty[s], ph ^ 1u) &&
+          !mbar_wait_bounded_hint(&empty[s], ph ^ 1u, p.wait_ns, kHintNs)) {
+        fail(p.status);
+        bad = true;
+        break;
+      }
+      uint8_t* B = stages + (size_t)s * p.stage_bytes;
+      if (i < g.nw) {
+        if (X) {
+          mbar_arrive_expect_tx(&full[s], p.b_bytes);
+          tma_load_2d(B, mapX, (g.wb0 + i) * 64, b0, &full[s]);
+        } else {
+          mbar_arrive_expect_tx(&raw_full[s], kRawBytes);
+          bulk_g2s(B + p.b_bytes, wsrc, kRawBytes, &raw_full[s]);
+          wsrc += kPrefillBlockWords;
+        }
+      } else if (X) {
+        // K-tail block: B = u' of this tile's tokens, once the prologue has
+        // written it (or the pre-kernel's grid has completed)
+        if (i == g.nw && p.pro_items > 0) {
+          const int t_end = min(b0 + p.TN, p.M);
+          for (int ti = b0 / 128; ti * 128 < t_end && !bad; ++ti)
+            if (!wait_flag(&p.u_ready[ti], 4 * p.wait_ns)) bad = true;
+          if (bad) {
+            fail(p.status);
+            break;
+          }
+          fence_proxy_async_global();
+        }
+        if (!waited) {
+          asm volatile("griddepcontrol.wait;" ::: "memory");
+          waited = true;
+        }
+        mbar_arrive_expect_tx(&full[s], p.b_bytes);
+        tma_load_2d(B, mapU, (i - g.nw) * 64, b0, &full[s]);
+      } else {
+        // K-tail block: the dequantisers read A rows (the compensator's B)
+        // from global memory and may fill the stage's A slot from now on
+        mbar_arrive(&raw_full[s]);
+      }
+      if (++s == p.NS) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ main kernel
 // mapX: x tokens (box 64 x TN); mapU: u' (box 64 x TN); mapXp: x tokens for
 // the prologue (box 64 x 128); mapA: the compensator's A (box 64 x rank).
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kMainThreads, 1)
     main_kernel(const MainParams p, const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapU,
                 const __grid_constant__ CUtensorMap mapXp, const __grid_constant__ CUtensorMap mapA) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -575,93 +684,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0) {
-    // ---------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      int s = 0;
-      unsigned ph = 0;
-      bool waited = !p.late_wait;
-      int it = 0;
-      bool bad = false;
-      // prologue items, each after the previous one's epilogue has released
-      // the stage memory (pro_done completes one phase per item)
-      int k = 0;
-      for (int item = blockIdx.x; item < p.pro_items && !bad; item += gridDim.x, ++k) {
-        if (k > 0 && !mbar_wait_bounded(pro_done, (unsigned)((k - 1) & 1), 8 * p.wait_ns)) {
-          fail(p.status);
-          bad = true;
-          break;
-        }
-        for (int i = 0; i < p.kbt; ++i, ++it) {
-          if (it >= p.NS && !mbar_test_wait(&empty[s], ph ^ 1u) &&
-              !mbar_wait_bounded_hint(&empty[s], ph ^ 1u, p.wait_ns, kHintNs)) {
-            fail(p.status);
-            bad = true;
-            break;
-          }
-          uint8_t* st = stages + (size_t)s * p.stage_bytes;
-          mbar_arrive(&raw_full[s]);
-          mbar_arrive_expect_tx(&full[s], pro_a_bytes + (uint32_t)p.rank * 128u);
-          tma_load_2d(st, &mapXp, i * 64, item * 128, &full[s]);
-          tma_load_2d(st + pro_a_bytes, &mapA, i * 64, 0, &full[s]);
-          if (++s == p.NS) {
-            s = 0;
-            ph ^= 1u;
-          }
-        }
-      }
-      if (!bad && k > 0 && !mbar_wait_bounded(pro_done, (unsigned)((k - 1) & 1), 8 * p.wait_ns)) {
-        fail(p.status);
-        bad = true;
-      }
-      for (uint32_t u = ub; u < ue && !bad;) {
-        const Segment g = segment_at(p, u, ue);
-        u += g.len;
-        const int rt = g.tile % p.nt128, b0 = (g.tile / p.nt128) * p.TN;
-        if (g.ntail > 0) prefetch_l2(p.bt + (size_t)rt * 128 * p.rank, 128u * p.rank * 2u);
-        for (int i = 0; i < g.nw + g.ntail; ++i, ++it) {
-          if (it >= p.NS && !mbar_test_wait(&empty[s], ph ^ 1u) &&
-              !mbar_wait_bounded_hint(&empty[s], ph ^ 1u, p.wait_ns, kHintNs)) {
-            fail(p.status);
-            bad = true;
-            break;
-          }
-          uint8_t* B = stages + (size_t)s * p.stage_bytes;
-          uint8_t* raw = B + p.b_bytes;
-          if (i < g.nw) {
-            const int kb = g.wb0 + i;
-            mbar_arrive_expect_tx(&raw_full[s], kRawBytes);
-            bulk_g2s(raw, p.wq + ((size_t)rt * p.kbt + kb) * kPrefillBlockWords, kRawBytes, &raw_full[s]);
-            mbar_arrive_expect_tx(&full[s], p.b_bytes);
-            tma_load_2d(B, &mapX, kb * 64, b0, &full[s]);
-          } else {
-            // K-tail block: A rows come from global memory (the dequantisers
-            // may fill the stage's A slot from now on), B = u' of this tile's
-            // tokens, once the prologue has written it
-            mbar_arrive(&raw_full[s]);
-            if (i == g.nw && p.pro_items > 0) {
-              const int t_end = min(b0 + p.TN, p.M);
-              for (int ti = b0 / 128; ti * 128 < t_end && !bad; ++ti)
-                if (!wait_flag(&p.u_ready[ti], 4 * p.wait_ns)) bad = true;
-              if (bad) {
-                fail(p.status);
-                break;
-              }
-              fence_proxy_async_global();
-            }
-            if (!waited) {
-              asm volatile("griddepcontrol.wait;" ::: "memory");
-              waited = true;
-            }
-            mbar_arrive_expect_tx(&full[s], p.b_bytes);
-            tma_load_2d(B, &mapU, (i - g.nw) * 64, b0, &full[s]);
-          }
-          if (++s == p.NS) {
-            s = 0;
-            ph ^= 1u;
-          }
-        }
-      }
-    }
+    // ---------------------------------------------------------- W producer
+    if (lane == 0)
+      produce<false>(p, &mapX, &mapU, &mapXp, &mapA, stages, full, raw_full, empty, pro_done, ub, ue);
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -720,17 +745,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!bad) umma_commit(acc_full);  // this segment's sum is complete once its MMAs have finished
       }
     }
+  } else if (warp == 6) {
+    // ---------------------------------------------------------- x producer
+    if (lane == 0)
+      produce<true>(p, &mapX, &mapU, &mapXp, &mapA, stages, full, raw_full, empty, pro_done, ub, ue);
   } else {
     // ---------------------------------------------------------- dequantisers + epilogues
     // One thread per row: warp w owns tensor-memory lanes 32 (w % 4) .. + 31,
     // i.e. rows r = 32 (w % 4) + lane of the tile. Per K block a thread reads
     // its row's 8 packed words and scale/zero word, makes 32 bf16 pairs (pair
     // c = channels 2c, 2c + 1) and stores them as the 32 columns of the
-    // stage's A slot. The store of block i is still in flight while block
-    // i + 1 is converted; block i counts towards full[s] once its store has
-    // completed. An epilogue reads the accumulator before these warps arrive
-    // for the next segment's first block, so the MMA thread cannot overwrite
-    // it early. Every warp runs every item and segment and every epilogue
+    // stage's A slot. An epilogue reads the accumulator before these warps
+    // arrive for the next segment's first block, so the MMA thread cannot
+    // overwrite it early. Every warp runs every item and segment and every epilogue
     // barrier; after a failed wait it only skips the data.
     const int q = warp & 3;
     const int r = 32 * q + lane;
@@ -831,7 +858,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Segment g = segment_at(p, u, ue);
       u += g.len;
       const int rt = g.tile % p.nt128, a0 = rt * 128, b0 = (g.tile / p.nt128) * p.TN;
-      int pending = -1;  // stage whose A store is in flight
       for (int i = 0; ok && i < g.nw + g.ntail; ++i) {
         uint32_t v[32];
         if (i < g.nw) {
@@ -863,27 +889,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = warp_wait(&raw_full[s], ph, p.wait_ns, kHintNs);
           if (!ok) break;
         }
-        if (pending >= 0) {
-          tmem_st_wait();
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&full[pending]);
-        }
+        // the block counts towards full[s] once its store has completed
+        // (deferring that until the next block was converted, to overlap the
+        // store, made the MMA wait for the next block's input)
         tc_fence_after_sync();
         tmem_st_x32(lane_base + p.tmem_a + 32 * s, v);
-        pending = s;
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
         raw_sa += p.stage_bytes;
         if (++s == p.NS) {
           s = 0;
           ph ^= 1u;
           raw_sa = stages_s + p.b_bytes;
         }
-      }
-      if (pending >= 0) {
-        tmem_st_wait();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full[pending]);
       }
       if (!ok && lane == 0) fail(p.status);
 
@@ -1011,13 +1031,13 @@ uint32_t tmem_cols_for(int n) {
 }
 
 template <typename Kernel, typename Params, typename... Maps>
-cudaError_t launch(Kernel k, std::atomic<uint64_t>& configured, const Params& p, dim3 grid, size_t smem,
+cudaError_t launch(Kernel k, int threads, std::atomic<uint64_t>& configured, const Params& p, dim3 grid, size_t smem,
                    cudaStream_t st, const Maps&... maps) {
   cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(k), configured);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -1119,7 +1139,7 @@ static spear_status_t launch_pre(spear_linear_s* h, const __nv_bfloat16* x, int 
   p.ga = gate_args(h, M);
   const size_t smem = std::max(kBarrierBytes + 1024 + (size_t)p.NS * p.stage_bytes, kOneCtaPerSmBytes);
   *pre_ctas = mt * splits;
-  const cudaError_t e = launch(pre_kernel, configured, p, dim3(mt, splits), smem, stream, mx, ma);
+  const cudaError_t e = launch(pre_kernel, kThreads, configured, p, dim3(mt, splits), smem, stream, mx, ma);
   return e == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
 }
 
@@ -1211,7 +1231,7 @@ static spear_status_t launch_main(spear_linear_s* h, const __nv_bfloat16* x, __n
     const size_t need = (size_t)128 * r * 2 + (h->gate == SPEAR_GATE_MLP ? (size_t)128 * (r + 8) * 4 : 0);
     smem = std::max(smem, kBarrierBytes + 1024 + need);
   }
-  const cudaError_t e = launch(main_kernel, configured, p, dim3(G), smem, stream, mx, mu, mxp, ma);
+  const cudaError_t e = launch(main_kernel, kMainThreads, configured, p, dim3(G), smem, stream, mx, mu, mxp, ma);
   return e == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
 }
 
