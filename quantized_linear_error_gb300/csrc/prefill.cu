@@ -49,7 +49,8 @@
 // Warp roles: warp 0 owns the TMEM allocation and issues copies (one thread:
 // in the main kernel the packed W; there warp 6 issues the x copies), warp 1
 // issues tcgen05.mma (one thread), warps 2-5 dequantise and run the
-// epilogues (warp w reads TMEM lanes 32 (w % 4) .. + 31). Every mbarrier and
+// epilogues (warp w reads TMEM lanes 32 (w % 4) .. + 31); in the main kernel
+// warps 7-10 dequantise the other half of each block's channels. Every mbarrier and
 // flag wait is bounded; a timeout latches the handle's status word and the
 // CTA runs through its remaining barriers without touching data. The MMA
 // thread's loop is on the critical path, so it waits on one barrier per
@@ -65,7 +66,7 @@ namespace spear {
 namespace {
 
 constexpr int kThreads = 192;      // pre-kernel: TMA, MMA, four epilogue warps
-constexpr int kMainThreads = 224;  // main kernel: W producer, MMA, four dequantising warps, x producer
+constexpr int kMainThreads = 352;  // main kernel: W producer, MMA, 4 dequantising + epilogue warps, x producer, 4 dequantising warps
 constexpr int kATileBytes = 128 * 128;           // 128 rows x 64 bf16
 constexpr int kRawWBytes = 128 * 8 * 4;          // 128 rows x 64 codes, packed
 constexpr int kRawBytes = kRawWBytes + 128 * 4;  // plus one scale/zero word per row (one prefill-layout block)
@@ -179,6 +180,46 @@ SPEAR_DEVINL void bulk_s2g(void* dst, const void* src, unsigned bytes) {
 SPEAR_DEVINL void bulk_commit_wait_all() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// 32 lanes x 32-bit, 16 consecutive columns per thread, registers -> TMEM.
+SPEAR_DEVINL void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// One half of a K block's A operand for row r: channels 32 h .. 32 h + 31
+// of the block as 16 bf16 pairs (TMEM columns 16 h .. 16 h + 15 of the
+// stage's A slot), from the stage's raw input (words 4 h .. 4 h + 3 of the
+// row, then the row's scale/zero word).
+SPEAR_DEVINL void dequant_half(uint32_t raw_sa, int r, int h, uint32_t (&v)[16]) {
+  const uint4 w = lds128(raw_sa + (uint32_t)(r * 32 + 16 * h));
+  const uint32_t szw = lds32(raw_sa + kRawWBytes + r * 4);
+  const uint32_t zz = biased_zero_x2(szw >> 16);
+  const uint32_t sc = (szw & 0xFFFFu) | (szw << 16);
+  const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      v[4 * c + j] = bf16x2_mul(bf16x2_sub(int4_pair_to_bf16x2_biased(words[c] >> (4 * j)), zz), sc);
+}
+
+// The same half of a K-tail block: row a0 + r of the compensator's B,
+// columns 64 t + 32 h .. + 31 (zero past rank).
+SPEAR_DEVINL void tail_half(const __nv_bfloat16* bt, int rank, int row, int t, int h, uint32_t (&v)[16]) {
+  const uint4* src = reinterpret_cast<const uint4*>(bt + (size_t)row * rank + t * 64 + 32 * h);
+#pragma unroll
+  for (int c8 = 0; c8 < 4; ++c8) {
+    const uint4 w = t * 64 + 32 * h + c8 * 8 < rank ? __ldg(src + c8) : make_uint4(0u, 0u, 0u, 0u);
+    v[4 * c8] = w.x;
+    v[4 * c8 + 1] = w.y;
+    v[4 * c8 + 2] = w.z;
+    v[4 * c8 + 3] = w.w;
+  }
 }
 
 // 32 lanes x 32-bit, 32 consecutive columns per thread.
@@ -657,7 +698,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
-      mbar_init(&full[s], 5);  // the producer's expect_tx and the four dequantising warps
+      mbar_init(&full[s], 9);  // the x producer's expect_tx and the eight dequantising warps
       mbar_init(&raw_full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -729,11 +770,16 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             break;
           }
           tc_fence_after_sync();
-          // A from tensor memory: 8 columns (16 channels) per k16 step
-#pragma unroll
-          for (int k16 = 0; k16 < 4; ++k16)
-            umma_ts_bf16(tmem_d, tmem_d + p.tmem_a + 32 * s + 8 * k16, sw128_kmajor_desc(b_s + 32 * k16), idesc,
-                         (i | k16) != 0);
+          // A from tensor memory: 8 columns (16 channels) per k16 step; B's
+          // descriptor built once per stage, the k16 step added to its
+          // address field (a 32-byte step is 2 in units of 16 bytes; the
+          // field holds every shared-memory address, so nothing carries)
+          const uint64_t bdesc = sw128_kmajor_desc(b_s);
+          const uint32_t a_t = tmem_d + p.tmem_a + 32 * s;
+          umma_ts_bf16(tmem_d, a_t, bdesc, idesc, i != 0);
+          umma_ts_bf16(tmem_d, a_t + 8, bdesc + 2, idesc, 1u);
+          umma_ts_bf16(tmem_d, a_t + 16, bdesc + 4, idesc, 1u);
+          umma_ts_bf16(tmem_d, a_t + 24, bdesc + 6, idesc, 1u);
           umma_commit(&empty[s]);
           b_s += p.stage_bytes;
           if (++s == p.NS) {
@@ -749,13 +795,71 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     // ---------------------------------------------------------- x producer
     if (lane == 0)
       produce<true>(p, &mapX, &mapU, &mapXp, &mapA, stages, full, raw_full, empty, pro_done, ub, ue);
+  } else if (warp >= 7) {
+    // ---------------------------------------------------------- second-half dequantisers
+    // Warps 7-10 convert channels 32 .. 63 of every K block (TMEM columns
+    // 16 .. 31 of the stage's A slot) while warps 2-5 convert 0 .. 31: one
+    // warp per lane quarter took ~370 cycles a block. They run no epilogue:
+    // the MMA thread needs every dequantiser's arrival for a stage, and warps
+    // 2-5 arrive for a segment's first block only after its epilogue.
+    const int q = warp & 3;
+    const int r = 32 * q + lane;
+    const uint32_t lane_base = tmem_d + ((uint32_t)(32 * q) << 16);
+    int s = 0;
+    unsigned ph = 0;
+    uint32_t raw_sa = stages_s + p.b_bytes;
+    bool ok = true;
+    for (int item = blockIdx.x; item < p.pro_items; item += gridDim.x) {
+      for (int i = 0; ok && i < p.kbt; ++i) {
+        ok = warp_wait(&raw_full[s], ph, p.wait_ns, kHintNs);
+        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
+        raw_sa += p.stage_bytes;
+        if (++s == p.NS) {
+          s = 0;
+          ph ^= 1u;
+          raw_sa = stages_s + p.b_bytes;
+        }
+      }
+    }
+    for (uint32_t u = ub; ok && u < ue;) {
+      const Segment g = segment_at(p, u, ue);
+      u += g.len;
+      const int a0 = (g.tile % p.nt128) * 128;
+      for (int i = 0; ok && i < g.nw + g.ntail; ++i) {
+        uint32_t v[16];
+        if (i < g.nw) {
+          ok = warp_wait(&raw_full[s], ph, p.wait_ns, kHintNs);
+          if (!ok) break;
+          dequant_half(raw_sa, r, 1, v);
+        } else {
+          tail_half(p.bt, p.rank, a0 + r, i - g.nw, 1, v);
+          ok = warp_wait(&raw_full[s], ph, p.wait_ns, kHintNs);
+          if (!ok) break;
+        }
+        tc_fence_after_sync();
+        tmem_st_x16(lane_base + p.tmem_a + 32 * s + 16, v);
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
+        raw_sa += p.stage_bytes;
+        if (++s == p.NS) {
+          s = 0;
+          ph ^= 1u;
+          raw_sa = stages_s + p.b_bytes;
+        }
+      }
+    }
+    if (!ok && lane == 0) fail(p.status);
   } else {
     // ---------------------------------------------------------- dequantisers + epilogues
     // One thread per row: warp w owns tensor-memory lanes 32 (w % 4) .. + 31,
     // i.e. rows r = 32 (w % 4) + lane of the tile. Per K block a thread reads
-    // its row's 8 packed words and scale/zero word, makes 32 bf16 pairs (pair
-    // c = channels 2c, 2c + 1) and stores them as the 32 columns of the
-    // stage's A slot. An epilogue reads the accumulator before these warps
+    // the first 4 of its row's 8 packed words and its scale/zero word, makes
+    // 16 bf16 pairs (pair c = channels 2c, 2c + 1) and stores them as
+    // columns 0 .. 15 of the stage's A slot (warps 7-10 do channels 32 .. 63). An epilogue reads the accumulator before these warps
     // arrive for the next segment's first block, so the MMA thread cannot
     // overwrite it early. Every warp runs every item and segment and every epilogue
     // barrier; after a failed wait it only skips the data.
@@ -859,33 +963,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       u += g.len;
       const int rt = g.tile % p.nt128, a0 = rt * 128, b0 = (g.tile / p.nt128) * p.TN;
       for (int i = 0; ok && i < g.nw + g.ntail; ++i) {
-        uint32_t v[32];
+        uint32_t v[16];
         if (i < g.nw) {
           ok = warp_wait(&raw_full[s], ph, p.wait_ns, kHintNs);
           if (!ok) break;
-          const uint4 w0 = lds128(raw_sa + (uint32_t)(r * 32));
-          const uint4 w1 = lds128(raw_sa + (uint32_t)(r * 32 + 16));
-          const uint32_t szw = lds32(raw_sa + kRawWBytes + r * 4);
-          const uint32_t zz = biased_zero_x2(szw >> 16);
-          const uint32_t sc = (szw & 0xFFFFu) | (szw << 16);
-          const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              v[4 * c + j] = bf16x2_mul(bf16x2_sub(int4_pair_to_bf16x2_biased(words[c] >> (4 * j)), zz), sc);
+          dequant_half(raw_sa, r, 0, v);
         } else {
-          // row a0 + r of the compensator's B, columns 64 t .. + 63 (zero past rank)
-          const int t = i - g.nw;
-          const uint4* src = reinterpret_cast<const uint4*>(p.bt + (size_t)(a0 + r) * p.rank + t * 64);
-#pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8) {
-            const uint4 w = t * 64 + c8 * 8 < p.rank ? __ldg(src + c8) : make_uint4(0u, 0u, 0u, 0u);
-            v[4 * c8] = w.x;
-            v[4 * c8 + 1] = w.y;
-            v[4 * c8 + 2] = w.z;
-            v[4 * c8 + 3] = w.w;
-          }
+          tail_half(p.bt, p.rank, a0 + r, i - g.nw, 0, v);
           ok = warp_wait(&raw_full[s], ph, p.wait_ns, kHintNs);
           if (!ok) break;
         }
@@ -893,7 +977,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         // (deferring that until the next block was converted, to overlap the
         // store, made the MMA wait for the next block's input)
         tc_fence_after_sync();
-        tmem_st_x32(lane_base + p.tmem_a + 32 * s, v);
+        tmem_st_x16(lane_base + p.tmem_a + 32 * s, v);
         tmem_st_wait();
         tc_fence_before_sync();
         __syncwarp();
