@@ -573,7 +573,11 @@ SPEAR_DEVINL void produce(const MainParams& p, const CUtensorMap* mapX, const CU
   const uint32_t pro_a_bytes = kATileBytes;  // prologue stage: x tile, then the A tile
   int s = 0;
   unsigned ph = 0;
-  bool waited = !X || !p.late_wait;
+  bool waited = !X;
+  if (X && !p.late_wait) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    waited = true;
+  }
   int it = 0;
   bool bad = false;
   int k = 0;
@@ -717,11 +721,15 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_d = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-  // Grid dependencies: x (and for the K-tail-only launch y32 and u') come
-  // from preceding grids. After a separate pre-kernel, which waited for x's
-  // producer before it let this grid launch, x can be read at once and only
-  // u' waits (the producer, before its first K-tail load).
-  if (!p.late_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Grid dependencies: only the x producer reads what preceding grids write
+  // (x, u', and for the K-tail-only launch y32, which the epilogue reads
+  // after MMAs that waited for the x producer's copies); every write of this
+  // grid follows such an MMA too. So only the x producer waits for the
+  // preceding grid, at its start, and the W producer and the dequantisers
+  // fill the first stages' A operands meanwhile. After a separate
+  // pre-kernel, which waited for x's producer before it let this grid
+  // launch, x can be read at once and the x producer waits only before its
+  // first u' load.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0) {
