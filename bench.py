@@ -769,8 +769,9 @@ def run_ours(args, world, rank, local):
             h.close()
         del g
         prefill = {"workload": "llama3-8b MLP, M=2048, INT4 g128, EC r128", **res[True],
-                   "design": "compensator pre-kernel overlapped by programmatic launch, up-projection as a K-tail "
-                             "of the main contraction's accumulator",
+                   "design": "one persistent stream-K kernel per projection: the compensator projection as "
+                             "prologue items (one per 128 tokens), the up-projection as a K-tail of the main "
+                             "contraction's accumulator",
                    "peak_tflops": bf16_peak, "peak_source": peak_src,
                    "ec_off": {**res[False], "ec_overhead": res[True]["ms"] / res[False]["ms"] - 1.0},
                    "concurrent_ec": conc}

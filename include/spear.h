@@ -212,6 +212,32 @@ spear_status_t spear_linear_check(spear_linear_t h, cudaStream_t stream);
  * launch) dependency that the hardware resolves; it has no arrival to skip. */
 spear_status_t spear_linear_debug_set(spear_linear_t h, int64_t wait_ns, int32_t skip_arrive);
 
+/* Test surface: the launch plan spear_linear_forward_prefill uses for a layer
+ * of this shape ("SPEAR", section 3.3: the compensator's projection fused
+ * ahead of the weight contraction, its output GEMM as the K-tail), computed
+ * by the same host code as the launch, with no device work and no GPU.
+ *   N, K, rank: the layer (K a multiple of 64, 0 <= rank <= 256);
+ *   mlp_gate: nonzero for SPEAR_GATE_MLP; M >= 1 tokens;
+ *   sm_count: SMs of the device the handle lives on;
+ *   with_workspace: nonzero when the handle was created with max_tokens > 32
+ *     (it then holds the stream-K partial-tile workspace).
+ * info (14 int32 entries, caller-owned): mode (0: the projection runs in
+ * the main kernel's prologue or rank = 0; 3: a split-K pre-kernel first),
+ * G (main-kernel CTAs), TN (tokens per tile), kpt (units per tile), tail
+ * (K-tail units per tile, ceil(rank / 64)), units (tiles x kpt), pro_items
+ * (prologue items, one per 128 tokens; 0 in mode 3), pro_d (units each item
+ * weighs in the split), NS (pipeline stages), stage_bytes, smem (dynamic
+ * shared memory per CTA), pre_ctas (the pre-kernel's CTAs, mode 3),
+ * tmem_a (first TMEM column of the dequantised-W slots), max_contrib (the
+ * most partial tiles any owner adds).
+ * starts (optional, caller-owned, starts_cap >= G + 1 entries): CTA c runs
+ * units [starts[c], starts[c + 1]); starts[G] = units.
+ * Errors: INVALID_ARG (bad shape, null info, starts_cap too small),
+ * UNSUPPORTED (more than 2^31 units). */
+spear_status_t spear_prefill_schedule(int32_t N, int32_t K, int32_t rank, int32_t mlp_gate, int32_t M,
+                                      int32_t sm_count, int32_t with_workspace, int32_t* info, uint32_t* starts,
+                                      int32_t starts_cap);
+
 /* Decode forward that allocates nothing (the paper has no counterpart; this is
  * a deployment convenience). For callers that cannot call cudaMalloc at all,
  * for instance a process whose device memory is entirely reserved up front by

@@ -1201,6 +1201,16 @@ static int prefill_tn(int M) {
   return tn < 16 ? 16 : tn;
 }
 
+// K splits of the pre-kernel: about 32 CTAs of at least 8 K blocks each.
+static int pre_splits(int K, int M) {
+  const int kbt = K / 64, mt = (M + 127) / 128;
+  int splits = (32 + mt - 1) / mt;
+  if (splits > kbt / 8) splits = kbt / 8;
+  if (splits < 1) splits = 1;
+  const int kblocks = (kbt + splits - 1) / splits;
+  return (kbt + kblocks - 1) / kblocks;
+}
+
 // The compensator projection on its own: u' [M][rank] = bf16(alpha gamma(A x) (.) A x).
 static spear_status_t launch_pre(spear_linear_s* h, const __nv_bfloat16* x, int M, cudaStream_t stream,
                                  int* pre_ctas) {
@@ -1212,10 +1222,7 @@ static spear_status_t launch_pre(spear_linear_s* h, const __nv_bfloat16* x, int 
     return SPEAR_ERR_CUDA;
   PreParams p{};
   const int kbt = K / 64, mt = (M + 127) / 128;
-  // About 32 CTAs of at least 8 K blocks each
-  int splits = (32 + mt - 1) / mt;
-  if (splits > kbt / 8) splits = kbt / 8;
-  if (splits < 1) splits = 1;
+  int splits = pre_splits(K, M);
   p.kblocks = (kbt + splits - 1) / splits;
   splits = (kbt + p.kblocks - 1) / p.kblocks;
   p.kb_total = kbt;
@@ -1233,6 +1240,70 @@ static spear_status_t launch_pre(spear_linear_s* h, const __nv_bfloat16* x, int 
   *pre_ctas = mt * splits;
   const cudaError_t e = launch(pre_kernel, kThreads, configured, p, dim3(mt, splits), smem, stream, mx, ma);
   return e == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
+}
+
+// The main kernel's launch plan (host only): the schedule fields of p, the
+// grid G and the dynamic shared memory. mode as for launch_main; r the rank
+// the launch uses (0 for mode 1); pre_ctas the SMs a preceding pre-kernel
+// holds; has_part whether the handle has the stream-K partial workspace.
+static spear_status_t plan_main(MainParams& p, int& G, size_t& smem, int K, int N, int nt128, int r, bool mlp_gate,
+                                int M, int mode, int sm_count, int pre_ctas, bool has_part) {
+  const int TN = prefill_tn(M);
+  const bool prologue = mode == 0 && r > 0;
+  p.kbt = mode == 2 ? 0 : K / 64;
+  p.tail = (r + 63) / 64;
+  p.kpt = p.kbt + p.tail;
+  p.nt128 = nt128;
+  const int tiles = nt128 * ((M + TN - 1) / TN);
+  const uint64_t units = (uint64_t)tiles * p.kpt;
+  if (units >= (1ull << 31)) return SPEAR_ERR_UNSUPPORTED;
+  p.units = (uint32_t)units;
+  p.TN = TN;
+  p.N = N;
+  p.M = M;
+  p.late_wait = mode == 3 && r > 0;
+  p.rank = r;
+  p.b_bytes = (uint32_t)(TN * 128 + 1023) / 1024 * 1024;
+  uint32_t stage = (p.b_bytes + kRawBytes + 1023) / 1024 * 1024;
+  if (prologue) stage = std::max<uint32_t>(stage, kATileBytes + (uint32_t)(r * 128 + 1023) / 1024 * 1024);
+  p.stage_bytes = stage;
+  p.tmem_a = (uint32_t)(TN + 31) / 32 * 32;
+  p.NS = stages_for(p.stage_bytes, std::min<int>(kMaxMainStages, (int)(512 - p.tmem_a) / 32));
+  // CTAs: one per tile for the K-tail-only launch and for handles without a
+  // partial workspace (sized for decode token counts). Otherwise every SM,
+  // with at least max(8, tail + 2, kpt / 3) units each (so that every range
+  // is non-empty and an owner adds few partials), and fewer where an owner's
+  // partials would not fit its stage memory 32 columns at a time.
+  const bool stream_k = has_part && p.kbt > 0;
+  const uint64_t area = (uint64_t)p.NS * p.stage_bytes;
+  G = tiles;
+  if (stream_k) {
+    const uint64_t lmin = std::max<uint64_t>({8, (uint64_t)p.tail + 2, (uint64_t)(p.kpt + 2) / 3});
+    G = (int)std::min<uint64_t>((uint64_t)std::max(1, sm_count - pre_ctas), units / lmin);
+    if (G < 1) G = 1;
+  }
+  for (;;) {
+    if (prologue) {
+      // One item per 128-token tile. Its weight in main-contraction units:
+      // its loads against a unit's (measured: CTAs with an item then finish
+      // with the others; half of that left them 7 us late).
+      p.pro_items = (M + 127) / 128;
+      const uint32_t pro_bytes = kATileBytes + (uint32_t)r * 128u, unit_bytes = p.b_bytes + kRawBytes;
+      p.pro_d = stream_k ? (int)((uint64_t)p.kbt * pro_bytes / unit_bytes) + 2 : 0;
+      if (stream_k && !ranges_nonempty(p, (uint32_t)G)) p.pro_d = 0;
+    }
+    if (!stream_k || G == 1 ||
+        (ranges_nonempty(p, (uint32_t)G) && (uint64_t)max_contributors(p, (uint32_t)G) * 32 * 512 <= area))
+      break;
+    --G;
+  }
+  smem = std::max(kBarrierBytes + 1024 + (size_t)p.NS * p.stage_bytes, kOneCtaPerSmBytes);
+  if (prologue) {
+    // an item's u' rows [128][rank] bf16 (the MLP gate: after z rows [128][rank + 8] fp32)
+    const size_t need = (size_t)128 * r * 2 + (mlp_gate ? (size_t)128 * (r + 8) * 4 : 0);
+    smem = std::max(smem, kBarrierBytes + 1024 + need);
+  }
+  return SPEAR_OK;
 }
 
 // Main kernel. mode 0: compensator prologue, W x and the K-tail, bf16 y;
@@ -1257,25 +1328,17 @@ static spear_status_t launch_main(spear_linear_s* h, const __nv_bfloat16* x, __n
                    !encode_2d_bf16(&ma, h->a_pre, K, r, (uint64_t)K * 2, 64, r)))
     return SPEAR_ERR_CUDA;
   MainParams p{};
-  p.kbt = mode == 2 ? 0 : K / 64;
-  p.tail = (r + 63) / 64;
-  p.kpt = p.kbt + p.tail;
-  p.nt128 = h->nt128;
-  const int tiles = h->nt128 * ((M + TN - 1) / TN);
-  const uint64_t units = (uint64_t)tiles * p.kpt;
-  if (units >= (1ull << 31)) return SPEAR_ERR_UNSUPPORTED;
-  p.units = (uint32_t)units;
-  p.TN = TN;
-  p.N = N;
-  p.M = M;
+  int G = 0;
+  size_t smem = 0;
+  const spear_status_t ps = plan_main(p, G, smem, K, N, h->nt128, r, h->gate == SPEAR_GATE_MLP, M, mode, h->sm_count,
+                                      pre_ctas, h->part != nullptr);
+  if (ps != SPEAR_OK) return ps;
   p.wq = h->wq_pre;
   p.out = y;
   p.status = &h->sync->status;
   p.wait_ns = h->wait_ns;
   p.skip_arrive = h->skip_arrive;
-  p.late_wait = mode == 3 && r > 0;
   p.bt = h->b_pre;
-  p.rank = r;
   p.part = h->part;
   p.part_flag = h->part_cnt;
   p.u_ready = h->u_ready;
@@ -1283,46 +1346,6 @@ static spear_status_t launch_main(spear_linear_s* h, const __nv_bfloat16* x, __n
   p.ga = gate_args(h, M);
   p.y32_out = mode == 1 ? h->y32 : nullptr;
   p.y32_in = mode == 2 ? h->y32 : nullptr;
-  p.b_bytes = (uint32_t)(TN * 128 + 1023) / 1024 * 1024;
-  uint32_t stage = (p.b_bytes + kRawBytes + 1023) / 1024 * 1024;
-  if (prologue) stage = std::max<uint32_t>(stage, kATileBytes + (uint32_t)(r * 128 + 1023) / 1024 * 1024);
-  p.stage_bytes = stage;
-  p.tmem_a = (uint32_t)(TN + 31) / 32 * 32;
-  p.NS = stages_for(p.stage_bytes, std::min<int>(kMaxMainStages, (int)(512 - p.tmem_a) / 32));
-  // CTAs: one per tile for the K-tail-only launch and for handles without a
-  // partial workspace (sized for decode token counts). Otherwise every SM,
-  // with at least max(8, tail + 2, kpt / 3) units each (so that every range
-  // is non-empty and an owner adds few partials), and fewer where an owner's
-  // partials would not fit its stage memory 32 columns at a time.
-  const bool stream_k = h->part != nullptr && p.kbt > 0;
-  const uint64_t area = (uint64_t)p.NS * p.stage_bytes;
-  int G = tiles;
-  if (stream_k) {
-    const uint64_t lmin = std::max<uint64_t>({8, (uint64_t)p.tail + 2, (uint64_t)(p.kpt + 2) / 3});
-    G = (int)std::min<uint64_t>((uint64_t)std::max(1, h->sm_count - pre_ctas), units / lmin);
-    if (G < 1) G = 1;
-  }
-  for (;;) {
-    if (prologue) {
-      // One item per 128-token tile. Its weight in main-contraction units:
-      // its loads against a unit's (measured: CTAs with an item then finish
-      // with the others; half of that left them 7 us late).
-      p.pro_items = (M + 127) / 128;
-      const uint32_t pro_bytes = kATileBytes + (uint32_t)r * 128u, unit_bytes = p.b_bytes + kRawBytes;
-      p.pro_d = stream_k ? (int)((uint64_t)p.kbt * pro_bytes / unit_bytes) + 2 : 0;
-      if (stream_k && !ranges_nonempty(p, (uint32_t)G)) p.pro_d = 0;
-    }
-    if (!stream_k || G == 1 ||
-        (ranges_nonempty(p, (uint32_t)G) && (uint64_t)max_contributors(p, (uint32_t)G) * 32 * 512 <= area))
-      break;
-    --G;
-  }
-  size_t smem = std::max(kBarrierBytes + 1024 + (size_t)p.NS * p.stage_bytes, kOneCtaPerSmBytes);
-  if (prologue) {
-    // an item's u' rows [128][rank] bf16 (the MLP gate: after z rows [128][rank + 8] fp32)
-    const size_t need = (size_t)128 * r * 2 + (h->gate == SPEAR_GATE_MLP ? (size_t)128 * (r + 8) * 4 : 0);
-    smem = std::max(smem, kBarrierBytes + 1024 + need);
-  }
   const cudaError_t e = launch(main_kernel, kMainThreads, configured, p, dim3(G), smem, stream, mx, mu, mxp, ma);
   return e == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
 }
@@ -1333,19 +1356,19 @@ static spear_status_t launch_main(spear_linear_s* h, const __nv_bfloat16* x, __n
 // contraction, and a separate split-K pre-kernel runs first. (Measured on
 // the mixed step's shapes: at 576 tokens the 4096 x 4096 and 11008 -> 4096
 // projections ran 30% faster with the pre-kernel, 4096 -> 11008 20% slower.)
-static bool prologue_pays(const spear_linear_s* h, int M) {
-  if (h->part == nullptr) return false;
-  const int TN = prefill_tn(M), kbt = h->K / 64;
-  const uint64_t tiles = (uint64_t)h->nt128 * ((M + TN - 1) / TN);
-  const uint64_t share = tiles * (kbt + (h->rank + 63) / 64) / (uint64_t)h->sm_count;
+static bool prologue_pays(int K, int nt128, int rank, int M, int sm_count, bool has_part) {
+  if (!has_part) return false;
+  const int TN = prefill_tn(M), kbt = K / 64;
+  const uint64_t tiles = (uint64_t)nt128 * ((M + TN - 1) / TN);
+  const uint64_t share = tiles * (kbt + (rank + 63) / 64) / (uint64_t)sm_count;
   const uint64_t unit_bytes = (uint64_t)(TN * 128 + 1023) / 1024 * 1024 + kRawBytes;
-  const uint64_t pro_d = (uint64_t)kbt * (kATileBytes + (uint64_t)h->rank * 128) / unit_bytes + 2;
+  const uint64_t pro_d = (uint64_t)kbt * (kATileBytes + (uint64_t)rank * 128) / unit_bytes + 2;
   return 4 * pro_d <= 3 * share;
 }
 
 spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,
                                     cudaStream_t stream) {
-  if (h->rank > 0 && !prologue_pays(h, M)) {
+  if (h->rank > 0 && !prologue_pays(h->K, h->nt128, h->rank, M, h->sm_count, h->part != nullptr)) {
     int pre_ctas = 0;
     const spear_status_t st = launch_pre(h, x, M, stream, &pre_ctas);
     if (st != SPEAR_OK) return st;
@@ -1371,4 +1394,33 @@ spear_status_t spear_launch_prefill_concurrent(spear_linear_s* h, const __nv_bfl
   if (cudaEventRecord(h->ev_join, ec_stream) != cudaSuccess || cudaStreamWaitEvent(stream, h->ev_join, 0) != cudaSuccess)
     return SPEAR_ERR_CUDA;
   return launch_main(h, x, y, M, stream, 2, 0);
+}
+
+// Test surface: the prefill launch plan of a handle of this shape, computed
+// by the same host code as the launch (no device work).
+spear_status_t spear_prefill_schedule(int32_t N, int32_t K, int32_t rank, int32_t mlp_gate, int32_t M, int32_t sm_count,
+                                      int32_t with_workspace, int32_t* info, uint32_t* starts, int32_t starts_cap) {
+  if (N <= 0 || K <= 0 || K % 64 != 0 || rank < 0 || rank > 256 || M < 1 || sm_count < 1 || !info)
+    return SPEAR_ERR_INVALID_ARG;
+  const int nt128 = (N + 127) / 128;
+  const bool has_part = with_workspace != 0;
+  int mode = 0, pre_ctas = 0;
+  if (rank > 0 && !prologue_pays(K, nt128, rank, M, sm_count, has_part)) {
+    mode = 3;
+    pre_ctas = ((M + 127) / 128) * pre_splits(K, M);
+  }
+  MainParams p{};
+  int G = 0;
+  size_t smem = 0;
+  const spear_status_t st = plan_main(p, G, smem, K, N, nt128, rank, mlp_gate != 0, M, mode, sm_count, pre_ctas, has_part);
+  if (st != SPEAR_OK) return st;
+  const int32_t v[14] = {mode, G, p.TN, p.kpt, p.tail, (int32_t)p.units, p.pro_items, p.pro_d, p.NS,
+                         (int32_t)p.stage_bytes, (int32_t)smem, pre_ctas, (int32_t)p.tmem_a,
+                         max_contributors(p, (uint32_t)G)};
+  for (int i = 0; i < 14; ++i) info[i] = v[i];
+  if (starts) {
+    if (starts_cap < G + 1) return SPEAR_ERR_INVALID_ARG;
+    for (int c = 0; c <= G; ++c) starts[c] = host_range_start(p, (uint32_t)c, (uint32_t)G);
+  }
+  return SPEAR_OK;
 }

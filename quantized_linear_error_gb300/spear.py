@@ -84,6 +84,8 @@ def load(path: Path | None = None):
     L.spear_sched_destroy.restype = c_int
     L.spear_quantize_rtn.argtypes = [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, H]
     L.spear_quantize_rtn.restype = c_int
+    L.spear_prefill_schedule.argtypes = [c_int32] * 7 + [c_void_p, c_void_p, c_int32]
+    L.spear_prefill_schedule.restype = c_int
     L.spear_status_string.argtypes = [c_int]
     L.spear_status_string.restype = c_char_p
     for name in ("spear_linear_create", "spear_linear_forward_decode", "spear_linear_forward_prefill",
@@ -286,6 +288,27 @@ def quantize_rtn(w, group_size=128, stream=None):
     _check(load().spear_quantize_rtn(_ptr(w), int(N), int(K), int(group_size), _ptr(q), _ptr(s), _ptr(z),
                                      _stream(stream)), "spear_quantize_rtn")
     return q, s, z
+
+
+PREFILL_SCHEDULE_FIELDS = ("mode", "G", "TN", "kpt", "tail", "units", "pro_items", "pro_d", "NS",
+                           "stage_bytes", "smem", "pre_ctas", "tmem_a", "max_contrib")
+
+
+def prefill_schedule(N: int, K: int, rank: int, M: int, sm_count: int, mlp_gate: bool = False,
+                     with_workspace: bool = True) -> dict:
+    """The prefill launch plan for a layer of this shape (host only, no GPU):
+    the fields of ``PREFILL_SCHEDULE_FIELDS`` plus ``starts``, the first unit
+    of each main-kernel CTA's range (G + 1 entries)."""
+    L = load()
+    info = (ctypes.c_int32 * len(PREFILL_SCHEDULE_FIELDS))()
+    _check(L.spear_prefill_schedule(N, K, rank, int(mlp_gate), M, sm_count, int(with_workspace), info, None, 0),
+           "spear_prefill_schedule")
+    out = dict(zip(PREFILL_SCHEDULE_FIELDS, list(info)))
+    starts = (ctypes.c_uint32 * (out["G"] + 1))()
+    _check(L.spear_prefill_schedule(N, K, rank, int(mlp_gate), M, sm_count, int(with_workspace), info, starts,
+                                    out["G"] + 1), "spear_prefill_schedule")
+    out["starts"] = list(starts)
+    return out
 
 
 class ChunkScheduler:
