@@ -897,11 +897,13 @@ def main():
     ap.add_argument("--skip-configs", action="store_true", help="skip the config 1 and 4 measurements")
     ap.add_argument("--skip-config5", action="store_true",
                     help="skip config 5 (32-layer mixed serving step) and the chunk scheduler's table")
-    ap.add_argument("--case", help="run one small named case 5 times and exit (profiling target), "
+    ap.add_argument("--case", help="run one small named case --reps times and exit (profiling target), "
                                    "e.g. decode:c2/q:1, decode:c4/up:16:noec, prefill:c3/gate:2048")
+    ap.add_argument("--reps", type=int, default=5, help="launches of --case (a profiler can skip the first ones "
+                                                        "to capture a warm launch)")
     args = ap.parse_args()
     if args.case:
-        run_case(args.case)
+        run_case(args.case, args.reps)
         return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -217,7 +217,8 @@ spear_status_t spear_linear_debug_set(spear_linear_t h, int64_t wait_ns, int32_t
  * ahead of the weight contraction, its output GEMM as the K-tail), computed
  * by the same host code as the launch, with no device work and no GPU.
  *   N, K, rank: the layer (K a multiple of 64, 0 <= rank <= 256);
- *   mlp_gate: nonzero for SPEAR_GATE_MLP; M >= 1 tokens;
+ *   gate_hidden: the hidden width of SPEAR_GATE_MLP (16, 32, 48 or 64), 0 for
+ *     the elementwise gates; M >= 1 tokens;
  *   sm_count: SMs of the device the handle lives on;
  *   with_workspace: nonzero when the handle was created with max_tokens > 32
  *     (it then holds the stream-K partial-tile workspace).
@@ -234,7 +235,7 @@ spear_status_t spear_linear_debug_set(spear_linear_t h, int64_t wait_ns, int32_t
  * units [starts[c], starts[c + 1]); starts[G] = units.
  * Errors: INVALID_ARG (bad shape, null info, starts_cap too small),
  * UNSUPPORTED (more than 2^31 units). */
-spear_status_t spear_prefill_schedule(int32_t N, int32_t K, int32_t rank, int32_t mlp_gate, int32_t M,
+spear_status_t spear_prefill_schedule(int32_t N, int32_t K, int32_t rank, int32_t gate_hidden, int32_t M,
                                       int32_t sm_count, int32_t with_workspace, int32_t* info, uint32_t* starts,
                                       int32_t starts_cap);
 

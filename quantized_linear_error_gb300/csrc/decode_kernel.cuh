@@ -120,21 +120,23 @@ SPEAR_DEVINL void ec_prefetch(const DecodeParams& p, int ew, int lane) {
 // Bottleneck-MLP gate ("SPEAR", section 2.1A: gamma is a bottleneck MLP):
 // u = alpha * sigmoid(W2 relu(W1 z)) (.) z per token, by the four compensator
 // warps: z is staged transposed in shared memory (zs [M16][rank + 8], token
-// rows M .. M16 - 1 zero, M16 = Mp rounded up to 16) next to W1 and W2 (copied
-// there before the grid-dependency wait, rows padded by 8), the two products
-// run on warp MMAs (mlp_gate_logits), each warp taking one 16-token block and
-// half of the rank columns; u is written split into bf16 hi + lo like the elementwise
-// gates (zero for tokens M .. Mp - 1, and everywhere if z never arrived).
-// One (16-token block, half of the rank columns) item of the MLP gate. Not
+// rows M .. M16 - 1 zero, M16 = Mp rounded up to 16) next to W1 and W2 (their
+// asynchronous copies issued before the grid-dependency wait, rows padded by
+// 8), the two products run on warp MMAs (mlp_gate_logits), each of the four
+// warps taking one 16-token block and a quarter (M16 = 16) or half (M16 = 32)
+// of the rank columns (the hidden layer is computed by each); u is written
+// split into bf16 hi + lo like the elementwise gates (zero for tokens
+// M .. Mp - 1, and everywhere if z never arrived).
+// One (16-token block, part of the rank columns) item of the MLP gate. Not
 // inlined: its fragments would otherwise raise the register allocation of the
 // whole kernel, consumer loop included.
 template <int Mp>
-__device__ __noinline__ void ec_u_mlp_item(const float* zs, int zst, int tb, int half, int r, int gh, int M,
+__device__ __noinline__ void ec_u_mlp_item(const float* zs, int zst, int tb, int part, int parts, int r, int gh, int M,
                                            float alpha, bool arrived, const __nv_bfloat16* w1s,
                                            const __nv_bfloat16* w2s, int lane, __nv_bfloat16* uh,
                                            __nv_bfloat16* ul, int us) {
   const int nj8 = r / 8;
-  mlp_gate_logits(zs, zst, 16 * tb, r, gh, w1s, r + 8, w2s, gh + 8, lane, half * nj8 / 2, (half + 1) * nj8 / 2,
+  mlp_gate_logits(zs, zst, 16 * tb, r, gh, w1s, r + 8, w2s, gh + 8, lane, part * nj8 / parts, (part + 1) * nj8 / parts,
                   [&](int m, int j, float g0, float g1) {
                     if (m >= Mp) return;
                     const bool live = arrived && m < M;
@@ -178,9 +180,11 @@ SPEAR_DEVINL void ec_u_mlp(const DecodeParams& p, const float* z, bool arrived, 
       }
     }
   }
+  cp_async_wait_all();  // this thread's copies of W1 and W2 (the barrier below publishes them)
   ec_bar();
-  for (int item = ew; item < (M16 / 16) * 2; item += kEcWarps)
-    ec_u_mlp_item<Mp>(zs, zst, item >> 1, item & 1, r, p.gh, M, p.alpha, arrived,
+  constexpr int kParts = kEcWarps / (M16 / 16);  // one item per compensator warp
+  for (int item = ew; item < (M16 / 16) * kParts; item += kEcWarps)
+    ec_u_mlp_item<Mp>(zs, zst, item / kParts, item % kParts, kParts, r, p.gh, M, p.alpha, arrived,
                       reinterpret_cast<const __nv_bfloat16*>(zs + M16 * zst),
                       reinterpret_cast<const __nv_bfloat16*>(zs + M16 * zst) + p.gh * zst, lane, uh, ul, us);
 }
@@ -356,8 +360,8 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
         // after z^T: W1 [gh][rank + 8], then W2 [rank][gh + 8]
         constexpr int M16 = Mp < 16 ? 16 : Mp;
         __nv_bfloat16* w1s = reinterpret_cast<__nv_bfloat16*>(zs_mlp + M16 * (p.rank + 8));
-        stage_rows_padded(w1s, p.gw1, p.gh, p.rank, ew * 32 + lane, kEcWarps * 32);
-        stage_rows_padded(w1s + p.gh * (p.rank + 8), p.gw2, p.rank, p.gh, ew * 32 + lane, kEcWarps * 32);
+        stage_rows_padded_async(w1s, p.gw1, p.gh, p.rank, ew * 32 + lane, kEcWarps * 32);
+        stage_rows_padded_async(w1s + p.gh * (p.rank + 8), p.gw2, p.rank, p.gh, ew * 32 + lane, kEcWarps * 32);
       }
       asm volatile("griddepcontrol.wait;" ::: "memory");
       // Calls alternate between two z buffers. `epoch` (calls completed so

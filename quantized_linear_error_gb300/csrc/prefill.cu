@@ -296,18 +296,19 @@ SPEAR_DEVINL void add_z_partial(const GateArgs& g, uint32_t lane_base, int token
 // u' = bf16(alpha gamma(z) (.) z) for the 128-token tile starting at token
 // a0, from its z rows (row stride zst floats, in shared memory, or in global
 // memory when z_global: then read through L2; rows past M are zero). Run by
-// the four epilogue warps, warp q on tokens a0 + 32 q .. + 31.
-SPEAR_DEVINL void gate_rows(const GateArgs& g, const float* z, int zst, bool z_global, int a0, int q, int lane) {
+// the four epilogue warps, warp q on tokens a0 + 32 q .. + 31. The MLP gate
+// reads W1 [gh][w1s] and W2 [rank][w2s] from shared memory (stage_mlp_weights).
+SPEAR_DEVINL void gate_rows(const GateArgs& g, const float* z, int zst, bool z_global, int a0, int q, int lane,
+                            const __nv_bfloat16* w1, const __nv_bfloat16* w2) {
   const int r = g.rank;
   auto ld4 = [&](const float* ptr) {
     return z_global ? __ldcg(reinterpret_cast<const float4*>(ptr)) : *reinterpret_cast<const float4*>(ptr);
   };
   if (g.gate == SPEAR_GATE_MLP) {
     // Bottleneck-MLP gate on warp MMAs (mlp_gate_logits) for the warp's two
-    // 16-token blocks, W1 and W2 from global memory:
-    // u' = bf16(alpha sigmoid(W2 relu(W1 z)) (.) z).
+    // 16-token blocks: u' = bf16(alpha sigmoid(W2 relu(W1 z)) (.) z).
     for (int tb = 0; tb < 2; ++tb)
-      mlp_gate_logits(z, zst, 32 * q + 16 * tb, r, g.gh, g.gw1, r, g.gw2, g.gh, lane, 0, r / 8,
+      mlp_gate_logits(z, zst, 32 * q + 16 * tb, r, g.gh, w1, r + 8, w2, g.gh + 8, lane, 0, r / 8,
                       [&](int lr, int j, float g0, float g1) {
                         const int m = a0 + lr;
                         if (m >= g.M) return;
@@ -344,11 +345,28 @@ SPEAR_DEVINL void gate_rows(const GateArgs& g, const float* z, int zst, bool z_g
   }
 }
 
+// The MLP gate's W1 [gh][rank] and W2 [rank][gh] (constant since create) into
+// shared memory at dst, rows padded by 8 elements: W1 then W2. By the four
+// epilogue warps, which then synchronise. Read from global memory inside the
+// gate's MMA loops, each k16 step waited for its own L2 round trip.
+SPEAR_DEVINL void stage_mlp_weights(const GateArgs& g, __nv_bfloat16* dst) {
+  stage_rows_padded(dst, g.gw1, g.gh, g.rank, threadIdx.x - 64, 128);
+  stage_rows_padded(dst + (size_t)g.gh * (g.rank + 8), g.gw2, g.rank, g.gh, threadIdx.x - 64, 128);
+  epilogue_bar();
+}
+
+// Shared-memory bytes of stage_mlp_weights.
+__host__ __device__ inline size_t mlp_weight_bytes(int rank, int gh) {
+  return ((size_t)gh * (rank + 8) + (size_t)rank * (gh + 8)) * 2;
+}
+
 // The last K split of the 128-token tile starting at token a0 (pre_kernel):
-// u' from the fp32 sums of z in global memory, then z cleared for the next call.
-SPEAR_DEVINL void gate_tile(const GateArgs& g, int a0, int q, int lane) {
+// u' from the fp32 sums of z in global memory, then z cleared for the next
+// call. wbuf: free shared memory for the MLP gate's weights.
+SPEAR_DEVINL void gate_tile(const GateArgs& g, int a0, int q, int lane, __nv_bfloat16* wbuf) {
   const int r = g.rank;
-  gate_rows(g, g.zacc + (size_t)a0 * r, r, true, a0, q, lane);
+  if (g.gate == SPEAR_GATE_MLP) stage_mlp_weights(g, wbuf);
+  gate_rows(g, g.zacc + (size_t)a0 * r, r, true, a0, q, lane, wbuf, wbuf + (size_t)g.gh * (r + 8));
   __syncwarp();
   for (int rr = 0; rr < 32; ++rr) {
     const int m = a0 + 32 * q + rr;
@@ -462,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     epilogue_bar();
     if (last_split) {
-      gate_tile(p.ga, a0, q, lane);
+      gate_tile(p.ga, a0, q, lane, reinterpret_cast<__nv_bfloat16*>(stages));
       if (threadIdx.x == 64) p.tile_done[blockIdx.x] = 0;
     }
   }
@@ -936,10 +954,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           }
         }
         if (g.gate == SPEAR_GATE_MLP) {
-          // warp q's z rows are its own: gate its two 16-token blocks on warp MMAs
-          __syncwarp();
+          // warp q's z rows are its own: gate its two 16-token blocks on warp
+          // MMAs, W1 and W2 staged after the u' rows
+          __nv_bfloat16* w1 = utile + (size_t)128 * p.rank;
+          stage_mlp_weights(g, w1);
+          const __nv_bfloat16* w2 = w1 + (size_t)g.gh * (p.rank + 8);
           for (int tb = 0; tb < 2; ++tb)
-            mlp_gate_logits(zrows, zst, 32 * q + 16 * tb, p.rank, g.gh, g.gw1, p.rank, g.gw2, g.gh, lane, 0,
+            mlp_gate_logits(zrows, zst, 32 * q + 16 * tb, p.rank, g.gh, w1, p.rank + 8, w2, g.gh + 8, lane, 0,
                             p.rank / 8, [&](int lr, int j, float g0, float g1) {
                               const float* zr = zrows + lr * zst;
                               *reinterpret_cast<uint32_t*>(utile + (size_t)lr * p.rank + j) =
@@ -1244,9 +1265,10 @@ static spear_status_t launch_pre(spear_linear_s* h, const __nv_bfloat16* x, int 
 
 // The main kernel's launch plan (host only): the schedule fields of p, the
 // grid G and the dynamic shared memory. mode as for launch_main; r the rank
-// the launch uses (0 for mode 1); pre_ctas the SMs a preceding pre-kernel
-// holds; has_part whether the handle has the stream-K partial workspace.
-static spear_status_t plan_main(MainParams& p, int& G, size_t& smem, int K, int N, int nt128, int r, bool mlp_gate,
+// the launch uses (0 for mode 1); gh the MLP gate's hidden width (0 for the
+// elementwise gates); pre_ctas the SMs a preceding pre-kernel holds;
+// has_part whether the handle has the stream-K partial workspace.
+static spear_status_t plan_main(MainParams& p, int& G, size_t& smem, int K, int N, int nt128, int r, int gh,
                                 int M, int mode, int sm_count, int pre_ctas, bool has_part) {
   const int TN = prefill_tn(M);
   const bool prologue = mode == 0 && r > 0;
@@ -1299,8 +1321,9 @@ static spear_status_t plan_main(MainParams& p, int& G, size_t& smem, int K, int 
   }
   smem = std::max(kBarrierBytes + 1024 + (size_t)p.NS * p.stage_bytes, kOneCtaPerSmBytes);
   if (prologue) {
-    // an item's u' rows [128][rank] bf16 (the MLP gate: after z rows [128][rank + 8] fp32)
-    const size_t need = (size_t)128 * r * 2 + (mlp_gate ? (size_t)128 * (r + 8) * 4 : 0);
+    // an item's u' rows [128][rank] bf16 (the MLP gate: after z rows [128][rank + 8]
+    // fp32, and followed by the gate's weights)
+    const size_t need = (size_t)128 * r * 2 + (gh > 0 ? (size_t)128 * (r + 8) * 4 + mlp_weight_bytes(r, gh) : 0);
     smem = std::max(smem, kBarrierBytes + 1024 + need);
   }
   return SPEAR_OK;
@@ -1330,7 +1353,7 @@ static spear_status_t launch_main(spear_linear_s* h, const __nv_bfloat16* x, __n
   MainParams p{};
   int G = 0;
   size_t smem = 0;
-  const spear_status_t ps = plan_main(p, G, smem, K, N, h->nt128, r, h->gate == SPEAR_GATE_MLP, M, mode, h->sm_count,
+  const spear_status_t ps = plan_main(p, G, smem, K, N, h->nt128, r, h->gate == SPEAR_GATE_MLP ? h->gate_hidden : 0, M, mode, h->sm_count,
                                       pre_ctas, h->part != nullptr);
   if (ps != SPEAR_OK) return ps;
   p.wq = h->wq_pre;
@@ -1356,8 +1379,11 @@ static spear_status_t launch_main(spear_linear_s* h, const __nv_bfloat16* x, __n
 // contraction, and a separate split-K pre-kernel runs first. (Measured on
 // the mixed step's shapes: at 576 tokens the 4096 x 4096 and 11008 -> 4096
 // projections ran 30% faster with the pre-kernel, 4096 -> 11008 20% slower.)
-static bool prologue_pays(int K, int nt128, int rank, int M, int sm_count, bool has_part) {
+static bool prologue_pays(int K, int nt128, int rank, int gh, int M, int sm_count, bool has_part) {
   if (!has_part) return false;
+  // an item's epilogue buffers (u' rows; the MLP gate's z rows and weights) fit
+  const size_t need = (size_t)128 * rank * 2 + (gh > 0 ? (size_t)128 * (rank + 8) * 4 + mlp_weight_bytes(rank, gh) : 0);
+  if (kBarrierBytes + 1024 + need > (size_t)227 * 1024) return false;
   const int TN = prefill_tn(M), kbt = K / 64;
   const uint64_t tiles = (uint64_t)nt128 * ((M + TN - 1) / TN);
   const uint64_t share = tiles * (kbt + (rank + 63) / 64) / (uint64_t)sm_count;
@@ -1368,7 +1394,8 @@ static bool prologue_pays(int K, int nt128, int rank, int M, int sm_count, bool 
 
 spear_status_t spear_launch_prefill(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,
                                     cudaStream_t stream) {
-  if (h->rank > 0 && !prologue_pays(h->K, h->nt128, h->rank, M, h->sm_count, h->part != nullptr)) {
+  if (h->rank > 0 && !prologue_pays(h->K, h->nt128, h->rank, h->gate == SPEAR_GATE_MLP ? h->gate_hidden : 0, M,
+                                    h->sm_count, h->part != nullptr)) {
     int pre_ctas = 0;
     const spear_status_t st = launch_pre(h, x, M, stream, &pre_ctas);
     if (st != SPEAR_OK) return st;
@@ -1398,21 +1425,23 @@ spear_status_t spear_launch_prefill_concurrent(spear_linear_s* h, const __nv_bfl
 
 // Test surface: the prefill launch plan of a handle of this shape, computed
 // by the same host code as the launch (no device work).
-spear_status_t spear_prefill_schedule(int32_t N, int32_t K, int32_t rank, int32_t mlp_gate, int32_t M, int32_t sm_count,
-                                      int32_t with_workspace, int32_t* info, uint32_t* starts, int32_t starts_cap) {
-  if (N <= 0 || K <= 0 || K % 64 != 0 || rank < 0 || rank > 256 || M < 1 || sm_count < 1 || !info)
+spear_status_t spear_prefill_schedule(int32_t N, int32_t K, int32_t rank, int32_t gate_hidden, int32_t M,
+                                      int32_t sm_count, int32_t with_workspace, int32_t* info, uint32_t* starts,
+                                      int32_t starts_cap) {
+  if (N <= 0 || K <= 0 || K % 64 != 0 || rank < 0 || rank > 256 || M < 1 || sm_count < 1 || !info || gate_hidden < 0 ||
+      gate_hidden > kMaxGateHidden || gate_hidden % 16 != 0)
     return SPEAR_ERR_INVALID_ARG;
   const int nt128 = (N + 127) / 128;
   const bool has_part = with_workspace != 0;
   int mode = 0, pre_ctas = 0;
-  if (rank > 0 && !prologue_pays(K, nt128, rank, M, sm_count, has_part)) {
+  if (rank > 0 && !prologue_pays(K, nt128, rank, gate_hidden, M, sm_count, has_part)) {
     mode = 3;
     pre_ctas = ((M + 127) / 128) * pre_splits(K, M);
   }
   MainParams p{};
   int G = 0;
   size_t smem = 0;
-  const spear_status_t st = plan_main(p, G, smem, K, N, nt128, rank, mlp_gate != 0, M, mode, sm_count, pre_ctas, has_part);
+  const spear_status_t st = plan_main(p, G, smem, K, N, nt128, rank, gate_hidden, M, mode, sm_count, pre_ctas, has_part);
   if (st != SPEAR_OK) return st;
   const int32_t v[14] = {mode, G, p.TN, p.kpt, p.tail, (int32_t)p.units, p.pro_items, p.pro_d, p.NS,
                          (int32_t)p.stage_bytes, (int32_t)smem, pre_ctas, (int32_t)p.tmem_a,

@@ -294,18 +294,18 @@ PREFILL_SCHEDULE_FIELDS = ("mode", "G", "TN", "kpt", "tail", "units", "pro_items
                            "stage_bytes", "smem", "pre_ctas", "tmem_a", "max_contrib")
 
 
-def prefill_schedule(N: int, K: int, rank: int, M: int, sm_count: int, mlp_gate: bool = False,
+def prefill_schedule(N: int, K: int, rank: int, M: int, sm_count: int, gate_hidden: int = 0,
                      with_workspace: bool = True) -> dict:
     """The prefill launch plan for a layer of this shape (host only, no GPU):
     the fields of ``PREFILL_SCHEDULE_FIELDS`` plus ``starts``, the first unit
     of each main-kernel CTA's range (G + 1 entries)."""
     L = load()
     info = (ctypes.c_int32 * len(PREFILL_SCHEDULE_FIELDS))()
-    _check(L.spear_prefill_schedule(N, K, rank, int(mlp_gate), M, sm_count, int(with_workspace), info, None, 0),
+    _check(L.spear_prefill_schedule(N, K, rank, gate_hidden, M, sm_count, int(with_workspace), info, None, 0),
            "spear_prefill_schedule")
     out = dict(zip(PREFILL_SCHEDULE_FIELDS, list(info)))
     starts = (ctypes.c_uint32 * (out["G"] + 1))()
-    _check(L.spear_prefill_schedule(N, K, rank, int(mlp_gate), M, sm_count, int(with_workspace), info, starts,
+    _check(L.spear_prefill_schedule(N, K, rank, gate_hidden, M, sm_count, int(with_workspace), info, starts,
                                     out["G"] + 1), "spear_prefill_schedule")
     out["starts"] = list(starts)
     return out

@@ -28,31 +28,32 @@ from quantized_linear_error_gb300 import build, spear
 SMS = 152
 SMEM_MAX = 227 * 1024
 
-# (N, K, rank, M, mlp_gate): the prefill shapes of the workloads, then small
-# and ragged ones.
+# (N, K, rank, M, gate_hidden): the prefill shapes of the workloads, then
+# small and ragged ones (gate_hidden > 0: the bottleneck-MLP gate).
 SHAPES = [
-    (14336, 4096, 128, 2048, False),  # Llama-3-8B gate / up
-    (14336, 4096, 128, 2048, True),   # the same with the learned MLP gate
-    (4096, 14336, 128, 2048, False),  # Llama-3-8B down
-    (4096, 4096, 64, 320, False),     # 32-layer stack, 64 decode + 256 prefill tokens
-    (11008, 4096, 64, 320, False),
-    (4096, 11008, 64, 320, False),
-    (4096, 4096, 64, 576, False),
-    (11008, 4096, 64, 576, False),
-    (4096, 11008, 64, 576, False),
-    (4096, 4096, 64, 1088, False),
-    (11008, 4096, 64, 1088, False),
-    (4096, 11008, 64, 1088, False),
-    (4096, 4096, 0, 1088, False),     # layers without a compensator
-    (11008, 4096, 0, 576, False),
-    (28672, 8192, 256, 2048, False),  # Llama-70B MLP at a prefill token count
-    (8192, 28672, 256, 600, False),
-    (2048, 2048, 32, 40, False),
-    (2048, 2048, 32, 200, False),
-    (200, 192, 32, 33, False),
-    (128, 64, 0, 33, False),
-    (384, 640, 96, 1000, True),
-    (4096, 4096, 256, 4096, False),
+    (14336, 4096, 128, 2048, 0),      # Llama-3-8B gate / up
+    (14336, 4096, 128, 2048, 16),     # the same with the bottleneck-MLP gate
+    (4096, 14336, 128, 2048, 0),      # Llama-3-8B down
+    (4096, 4096, 64, 320, 0),         # 32-layer stack, 64 decode + 256 prefill tokens
+    (11008, 4096, 64, 320, 0),
+    (4096, 11008, 64, 320, 0),
+    (4096, 4096, 64, 576, 0),
+    (11008, 4096, 64, 576, 0),
+    (4096, 11008, 64, 576, 0),
+    (4096, 4096, 64, 1088, 0),
+    (11008, 4096, 64, 1088, 0),
+    (4096, 11008, 64, 1088, 0),
+    (4096, 4096, 0, 1088, 0),         # layers without a compensator
+    (11008, 4096, 0, 576, 0),
+    (28672, 8192, 256, 2048, 0),      # Llama-70B MLP at a prefill token count
+    (8192, 28672, 256, 600, 0),
+    (2048, 2048, 32, 40, 0),
+    (2048, 2048, 32, 200, 0),
+    (200, 192, 32, 33, 0),
+    (128, 64, 0, 33, 0),
+    (384, 640, 96, 1000, 64),
+    (4096, 4096, 256, 4096, 0),
+    (14336, 4096, 256, 2048, 64),     # MLP gate whose prologue buffers would not fit
 ]
 
 
@@ -62,8 +63,8 @@ def lib():
     return spear.load()
 
 
-def _plan(N, K, r, M, gate, sms=SMS, ws=True):
-    return spear.prefill_schedule(N, K, r, M, sms, mlp_gate=gate, with_workspace=ws)
+def _plan(N, K, r, M, gh, sms=SMS, ws=True):
+    return spear.prefill_schedule(N, K, r, M, sms, gate_hidden=gh, with_workspace=ws)
 
 
 def _tiles(d, N, M):
@@ -140,8 +141,8 @@ def test_resources_and_residency(lib, N, K, r, M, gate):
     else:
         assert d["pre_ctas"] == 0
         assert d["pro_items"] == ((M + 127) // 128 if r > 0 else 0)
-        if r > 0:  # an item's u' rows (and the MLP gate's z rows) fit next to the barriers
-            need = 128 * r * 2 + (128 * (r + 8) * 4 if gate else 0)
+        if r > 0:  # an item's u' rows (and the MLP gate's z rows and weights) fit next to the barriers
+            need = 128 * r * 2 + (128 * (r + 8) * 4 + (gate * (r + 8) + r * (gate + 8)) * 2 if gate else 0)
             assert need + 1024 < d["smem"]
 
 
@@ -168,18 +169,22 @@ def test_projection_placement(lib):
     """Where the projection runs: in the prologue when an item weighs at most
     3/4 of a CTA's share; else in the split-K pre-kernel (measured choices on
     the 32-layer stack's shapes at 576 tokens)."""
-    assert _plan(14336, 4096, 128, 2048, False)["mode"] == 0
-    assert _plan(11008, 4096, 64, 576, False)["mode"] == 0
-    assert _plan(4096, 4096, 64, 576, False)["mode"] == 3
-    assert _plan(4096, 11008, 64, 576, False)["mode"] == 3
-    assert _plan(4096, 4096, 0, 576, False)["mode"] == 0
+    assert _plan(14336, 4096, 128, 2048, 0)["mode"] == 0
+    assert _plan(11008, 4096, 64, 576, 0)["mode"] == 0
+    assert _plan(4096, 4096, 64, 576, 0)["mode"] == 3
+    assert _plan(4096, 11008, 64, 576, 0)["mode"] == 3
+    assert _plan(4096, 4096, 0, 576, 0)["mode"] == 0
+    # rank 256 with a 64-wide MLP gate: z rows, u' rows and the gate's
+    # weights need more than 227 KB, so the pre-kernel runs instead
+    assert _plan(14336, 4096, 256, 2048, 0)["mode"] == 0
+    assert _plan(14336, 4096, 256, 2048, 64)["mode"] == 3
 
 
 def test_without_partial_workspace_one_cta_per_tile(lib):
     """Handles sized for decode token counts hold no partial-tile workspace:
     then each CTA runs one whole tile and the projection is a pre-kernel."""
     for N, K, r, M in [(4096, 4096, 64, 300), (2048, 2048, 32, 40), (4096, 4096, 0, 600)]:
-        d = _plan(N, K, r, M, False, ws=False)
+        d = _plan(N, K, r, M, 0, ws=False)
         tiles = _tiles(d, N, M)
         assert d["G"] == tiles
         assert d["starts"] == [c * d["kpt"] for c in range(tiles + 1)]
@@ -189,7 +194,7 @@ def test_without_partial_workspace_one_cta_per_tile(lib):
 
 @pytest.mark.parametrize("sms", [1, 2, 7, 76, 132, 148, 152])
 def test_other_sm_counts(lib, sms):
-    for N, K, r, M, gate in [(4096, 4096, 64, 1088, False), (14336, 4096, 128, 2048, True), (200, 192, 32, 33, False)]:
+    for N, K, r, M, gate in [(4096, 4096, 64, 1088, 0), (14336, 4096, 128, 2048, 16), (200, 192, 32, 33, 0)]:
         d = _plan(N, K, r, M, gate, sms=sms)
         assert 1 <= d["G"] <= max(1, sms - d["pre_ctas"])
         owner, _, runs = _walk(d)
@@ -202,7 +207,8 @@ def test_rejects_bad_shapes(lib):
     info = (ctypes.c_int32 * 14)()
     L = spear.load()
     for args in [(0, 64, 0, 0, 1, 152, 1), (128, 100, 0, 0, 1, 152, 1), (128, 64, 300, 0, 1, 152, 1),
-                 (128, 64, 0, 0, 0, 152, 1), (128, 64, 0, 0, 1, 0, 1)]:
+                 (128, 64, 0, 0, 0, 152, 1), (128, 64, 0, 0, 1, 0, 1), (128, 64, 32, 24, 1, 152, 1),
+                 (128, 64, 32, 80, 1, 152, 1)]:
         assert L.spear_prefill_schedule(*args, info, None, 0) == spear.SPEAR_ERR_INVALID_ARG
     assert L.spear_prefill_schedule(128, 64, 0, 0, 1, 152, 1, None, None, 0) == spear.SPEAR_ERR_INVALID_ARG
     starts = (ctypes.c_uint32 * 1)()
