@@ -395,10 +395,20 @@ def measure_other_configs(args, stream, time_graphs, dev, hbm_peak, bf16_peak, w
         specs = wl.config_linears(5)
         base = {s5.name.split("/")[-1]: wl.make_weights(s5, 0) for s5 in wl.llama7b_layer("c5/", rank=64)}
         mmax = max(wl.CONFIG_TOKENS[5])
-        hs = []
-        for s5 in specs:
+        def weights_of(s5):
             w = base[s5.name.split("/")[-1]]
-            hs.append(spear.from_weights(w if s5.rank else no_ec(w), max_tokens=mmax, stream=stream))
+            return w if s5.rank else no_ec(w)
+
+        # one handle per projection (224 launches per step), and the same stack
+        # with q/k/v and gate/up, which read the same x, as grouped handles
+        # (128 launches, as in the decode layer set)
+        hs = [spear.from_weights(weights_of(s5), max_tokens=mmax, stream=stream) for s5 in specs]
+        hg = []
+        for layer in range(len(specs) // 7):
+            for i, j in GROUPS:
+                ws = [weights_of(s5) for s5 in specs[7 * layer + i: 7 * layer + j]]
+                hg.append(spear.grouped_from_weights(ws, max_tokens=mmax, stream=stream) if len(ws) > 1
+                          else spear.from_weights(ws[0], max_tokens=mmax, stream=stream))
         res = {}
         ec_stream = torch.cuda.Stream()
         for h in hs:
@@ -406,10 +416,12 @@ def measure_other_configs(args, stream, time_graphs, dev, hbm_peak, bf16_peak, w
         for M in wl.CONFIG_TOKENS[5]:
             xs = {K: dev(wl.make_x(K, M, base["q" if K == 4096 else "down"].outliers, 0, f"c5/x{K}"))
                   for K in (4096, 11008)}
-            ys = {N: torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for N in (4096, 11008)}
-            g = graph_of([lambda h=h, s5=s5: h.forward_prefill(xs[s5.K], ys[s5.N], stream=stream)
-                          for h, s5 in zip(hs, specs)])
+            ys = {N: torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for N in (4096, 11008, 12288, 22016)}
+            g = graph_of([lambda h=h: h.forward_prefill(xs[h.K], ys[h.N], stream=stream) for h in hg])
             t = time_graphs([g], max(3, args.steps // 200), 3)
+            del g
+            g = graph_of([lambda h=h: h.forward_prefill(xs[h.K], ys[h.N], stream=stream) for h in hs])
+            ts = time_graphs([g], max(3, args.steps // 200), 3)
             del g
             g = graph_of([lambda h=h, s5=s5: h.forward_prefill_concurrent(xs[s5.K], ys[s5.N], stream=stream,
                                                                            ec_stream=ec_stream)
@@ -419,16 +431,21 @@ def measure_other_configs(args, stream, time_graphs, dev, hbm_peak, bf16_peak, w
             fl = sum(s5.flops(M) for s5 in specs)
             res[str(M - 64)] = {"tokens": M, "ms_per_step": t, "tokens_per_s": M / (t / 1e3),
                                 "tflops": fl / (t / 1e3) / 1e12, "frac_bf16_peak": fl / (t / 1e3) / 1e12 / bf16_peak,
+                                "separate": {"ms_per_step": ts, "frac_bf16_peak": fl / (ts / 1e3) / 1e12 / bf16_peak},
                                 "concurrent_ec": {"ms_per_step": tc,
                                                   "frac_bf16_peak": fl / (tc / 1e3) / 1e12 / bf16_peak}}
-        for h in hs:
+        for h in hs + hg:
             if h.check() != spear.SPEAR_OK:
                 raise SystemExit("config 5 device status error")
             h.close()
         out["5"] = {"workload": "32-layer Llama-7B-shaped stack (224 linears), INT4 g128, EC r64 on layers "
                                 f"{wl.ec_layer_indices(0)}, 64 decode tokens + prefill chunk C, one CUDA graph "
-                                "per step", "by_chunk": res}
-        del hs
+                                "per step",
+                    "arrangement": "q/k/v and gate/up (which read the same x) as grouped handles: 128 prefill "
+                                   "launches per step; 'separate': one handle per projection (224); "
+                                   "'concurrent_ec': separate handles, compensator on a second stream",
+                    "by_chunk": res}
+        del hs, hg
         out["scheduler"] = measure_scheduler(args, stream, time_graphs, dev, base)
     return out
 
