@@ -169,11 +169,13 @@ spear_status_t spear_linear_forward_host(spear_linear_t h, const void* x_host, v
                                          int32_t M, cudaStream_t stream);
 
 /* End-to-end forward of a batch of calls on HOST buffers with one
- * synchronisation: for i = 0 .. n-1, in order on `stream`, copies x_host[i]
- * (bf16 [Ms[i]][K of hs[i]]) into hs[i]'s staging buffer, runs
- * spear_linear_forward on it and copies the result into y_host[i] (bf16
- * [Ms[i]][N of hs[i]]); then synchronises `stream` once. A handle may appear
- * several times (its staging buffers are reused in stream order). Every
+ * synchronisation: call i copies x_host[i] (bf16 [Ms[i]][K of hs[i]]) into
+ * hs[i]'s staging buffer, runs spear_linear_forward on it and copies the
+ * result into y_host[i] (bf16 [Ms[i]][N of hs[i]]), all on `stream`; then
+ * `stream` is synchronised once. The calls go in order, in runs of distinct
+ * handles: a run's input copies, then its forwards back to back, then its
+ * result copies. A handle may appear several times (it then starts a new
+ * run, since its staging buffers are reused in stream order). Every
  * argument is checked before anything is enqueued: INVALID_ARG for a null
  * array or handle, Ms[i] outside 0 .. max_tokens of hs[i], or null buffers
  * with Ms[i] > 0. Pinned host memory gives asynchronous copies. */

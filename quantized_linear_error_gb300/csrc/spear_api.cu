@@ -404,16 +404,29 @@ spear_status_t spear_linear_forward_host_batch(const spear_linear_t* hs, const v
     if (!h || Ms[i] < 0 || Ms[i] > h->max_tokens) return SPEAR_ERR_INVALID_ARG;
     if (Ms[i] > 0 && (!x_host[i] || !y_host[i])) return SPEAR_ERR_INVALID_ARG;
   }
-  for (int32_t i = 0; i < n; ++i) {
-    const spear_linear_t h = hs[i];
-    const int32_t M = Ms[i];
-    if (M == 0) continue;
-    if (cudaMemcpyAsync(h->x_stage, x_host[i], (size_t)M * h->K * 2, cudaMemcpyHostToDevice, stream) != cudaSuccess)
-      return SPEAR_ERR_CUDA;
-    spear_status_t s = spear_linear_forward(h, h->x_stage, h->y_stage, M, stream);
-    if (s != SPEAR_OK) return s;
-    if (cudaMemcpyAsync(y_host[i], h->y_stage, (size_t)M * h->N * 2, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-      return SPEAR_ERR_CUDA;
+  // Runs of calls on distinct handles: all inputs up, the forwards back to
+  // back (so that each kernel's programmatic launch overlaps the previous
+  // one's tail, which a copy between them would prevent), all results down.
+  // A handle that appears again starts the next run: the calls share its
+  // staging buffers.
+  for (int32_t i = 0; i < n;) {
+    int32_t j = i + 1;
+    for (bool dup = false; j < n && !dup; j += dup ? 0 : 1)
+      for (int32_t k = i; k < j && !dup; ++k) dup = hs[k] == hs[j];
+    for (int32_t k = i; k < j; ++k)
+      if (Ms[k] > 0 && cudaMemcpyAsync(hs[k]->x_stage, x_host[k], (size_t)Ms[k] * hs[k]->K * 2, cudaMemcpyHostToDevice,
+                                       stream) != cudaSuccess)
+        return SPEAR_ERR_CUDA;
+    for (int32_t k = i; k < j; ++k) {
+      if (Ms[k] == 0) continue;
+      const spear_status_t s = spear_linear_forward(hs[k], hs[k]->x_stage, hs[k]->y_stage, Ms[k], stream);
+      if (s != SPEAR_OK) return s;
+    }
+    for (int32_t k = i; k < j; ++k)
+      if (Ms[k] > 0 && cudaMemcpyAsync(y_host[k], hs[k]->y_stage, (size_t)Ms[k] * hs[k]->N * 2, cudaMemcpyDeviceToHost,
+                                       stream) != cudaSuccess)
+        return SPEAR_ERR_CUDA;
+    i = j;
   }
   return cudaStreamSynchronize(stream) == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
 }
