@@ -1330,10 +1330,10 @@ static spear_status_t plan_main(MainParams& p, int& G, size_t& smem, int K, int 
 }
 
 // Main kernel. mode 0: compensator prologue, W x and the K-tail, bf16 y;
-// mode 1: W x only, fp32 result into h->y32; mode 2: the K-tail only (u'
-// complete), added to h->y32, bf16 y; mode 3: W x and the K-tail with u'
-// from the pre-kernel launched just before on the same stream, which runs on
-// pre_ctas SMs.
+// mode 1: W x only, fp32 result into h->y32, next to the pre-kernel on
+// another stream (pre_ctas SMs); mode 2: the K-tail only (u' complete), added
+// to h->y32, bf16 y; mode 3: W x and the K-tail with u' from the pre-kernel
+// launched just before on the same stream, which runs on pre_ctas SMs.
 static spear_status_t launch_main(spear_linear_s* h, const __nv_bfloat16* x, __nv_bfloat16* y, int M,
                                   cudaStream_t stream, int mode, int pre_ctas) {
   static std::atomic<uint64_t> configured{0};
@@ -1416,7 +1416,9 @@ spear_status_t spear_launch_prefill_concurrent(spear_linear_s* h, const __nv_bfl
   int pre_ctas = 0;
   spear_status_t st = launch_pre(h, x, M, ec_stream, &pre_ctas);
   if (st != SPEAR_OK) return st;
-  st = launch_main(h, x, y, M, stream, 1, 0);
+  // the main contraction leaves the pre-kernel's SMs free: its stream-K
+  // owners wait for later CTAs, which must all be resident
+  st = launch_main(h, x, y, M, stream, 1, pre_ctas);
   if (st != SPEAR_OK) return st;
   if (cudaEventRecord(h->ev_join, ec_stream) != cudaSuccess || cudaStreamWaitEvent(stream, h->ev_join, 0) != cudaSuccess)
     return SPEAR_ERR_CUDA;
