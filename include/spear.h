@@ -214,6 +214,24 @@ spear_status_t spear_linear_check(spear_linear_t h, cudaStream_t stream);
  * launch) dependency that the hardware resolves; it has no arrival to skip. */
 spear_status_t spear_linear_debug_set(spear_linear_t h, int64_t wait_ns, int32_t skip_arrive);
 
+/* Test surface: the launch plan spear_linear_forward_decode uses for a handle
+ * of this shape ("SPEAR", section 2.2A: the decode phase as one fused kernel),
+ * computed by the same host code as the launch, with no device work.
+ *   N, K: output and input width (as spear_linear_create accepts them);
+ *   rank_b, n_members: each member's compensator rank and the member count
+ *     (1 for spear_linear_create, 2..8 for a grouped handle with N split
+ *     evenly); group_size: 128 or 0 (per output channel);
+ *   gate_hidden: the MLP gate's hidden width (16, 32, 48 or 64), else 0;
+ *   1 <= M <= 32; sm_count: SMs of the device.
+ * info (13 int32 entries, caller-owned): grid, P (16-row tiles per CTA), NW
+ * (consumer warps), T (tiles per warp), MT (8-token tiles), KW (warps along
+ * K), KC (channels per stage), NS (stages), stage_bytes, smem (dynamic
+ * shared memory), n_stages (stages over K), threads, bytes_x (x box bytes).
+ * Errors: INVALID_ARG (bad shape or null info), UNSUPPORTED (as create or the
+ * launch would report it). */
+spear_status_t spear_decode_schedule(int32_t N, int32_t K, int32_t rank_b, int32_t n_members, int32_t group_size,
+                                     int32_t gate_hidden, int32_t M, int32_t sm_count, int32_t* info);
+
 /* Test surface: the launch plan spear_linear_forward_prefill uses for a layer
  * of this shape ("SPEAR", section 3.3: the compensator's projection fused
  * ahead of the weight contraction, its output GEMM as the K-tail), computed

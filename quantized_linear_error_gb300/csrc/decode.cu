@@ -43,7 +43,7 @@ DecodeKernelRef kernel_for(int NW, int MT, int T, bool pc, bool ec) {
 // Everything a decode launch needs except the x tensor map.
 struct DecodeLaunch {
   DecodeParams p;
-  int grid = 0, NW = 0, MT = 0;
+  int grid = 0, NW = 0, MT = 0, T = 0;
   size_t smem = 0;
   DecodeKernelRef kernel;
 };
@@ -76,10 +76,6 @@ spear_status_t decode_config(const spear_linear_s* h, int M, DecodeLaunch* out) 
   p.nt16 = h->nt16;
   p.P = P;
   p.KW = KW;
-  p.KC = KC;
-  p.bytes_x = (uint32_t)(KC * Mp * 2);
-  p.stage_bytes = (uint32_t)((p.bytes_x + P * L.stage_tile_bytes(KC) + 1023) / 1024 * 1024);
-  p.n_stages = (h->K + KC - 1) / KC;
   p.wait_ns = h->wait_ns;
   p.skip_arrive = h->skip_arrive;
   p.gw1 = h->gate_w1;
@@ -100,18 +96,68 @@ spear_status_t decode_config(const spear_linear_s* h, int M, DecodeLaunch* out) 
   const size_t pc_bytes = h->per_channel ? (size_t)P * 64 : 0;
   const size_t b_bytes = ec ? (size_t)P * (h->rank_b / 16) * 512 + 16 : 0;
   // barriers, alignment slack, per-channel words, u (hi and lo)
-  const size_t fixed = kBarrierBytes + 1024 + pc_bytes + u_bytes + mlp_bytes + b_bytes;
-  const size_t budget = kSmemCap > fixed ? kSmemCap - fixed : 0;
-  int NS = (int)(budget / p.stage_bytes);
-  if (NS > kMaxStages) NS = kMaxStages;
-  if (NS > p.n_stages) NS = p.n_stages;
-  while ((size_t)NS * p.stage_bytes < red_bytes) ++NS;  // the reduction reuses the stage area
+  const size_t base = kBarrierBytes + 1024 + pc_bytes + u_bytes + mlp_bytes;
+
+  // The pipeline for kc channels per stage: stage size, stages next to the
+  // fixed buffers. The B fragments of the CTA's tiles live next to the stages
+  // for the whole call, unless that costs stages (rank 256: 8 KB per tile);
+  // then they are copied into the stage area once the W loop has released it,
+  // behind the partial sums (the reduction reuses the stage area too).
+  struct StagePlan {
+    int KC, n_stages, NS;
+    uint32_t stage_bytes, b_late_off;
+    size_t fixed;
+  };
+  auto stage_plan = [&](int kc) {
+    StagePlan sp;
+    sp.KC = kc;
+    sp.stage_bytes = (uint32_t)(((size_t)kc * Mp * 2 + P * L.stage_tile_bytes(kc) + 1023) / 1024 * 1024);
+    sp.n_stages = (h->K + kc - 1) / kc;
+    auto stages_next_to = [&](size_t fixed, size_t area) {
+      const size_t budget = kSmemCap > fixed ? kSmemCap - fixed : 0;
+      int ns = (int)(budget / sp.stage_bytes);
+      if (ns > kMaxStages) ns = kMaxStages;
+      if (ns > sp.n_stages) ns = sp.n_stages;
+      while ((size_t)ns * sp.stage_bytes < area) ++ns;
+      return ns;
+    };
+    sp.fixed = base + b_bytes;
+    sp.NS = stages_next_to(sp.fixed, red_bytes);
+    sp.b_late_off = 0;
+    if (ec) {
+      const size_t red_al = (red_bytes + 127) / 128 * 128;
+      const int ns_late = stages_next_to(base, red_al + b_bytes);
+      if (ns_late > sp.NS && base + (size_t)ns_late * sp.stage_bytes <= 227 * 1024) {
+        sp.fixed = base;
+        sp.NS = ns_late;
+        sp.b_late_off = (uint32_t)red_al;
+      }
+    }
+    return sp;
+  };
+  StagePlan sp = stage_plan(KC);
+  // One unit per K warp and stage where two would leave a single stage (x
+  // boxes of 16 or 32 tokens at two tiles per CTA): double buffering pays
+  // there, while elsewhere the two-unit stages measured faster.
+  if (sp.NS < 2 && sp.n_stages > 1 && (KC / 2) % kDecodeRun == 0) {
+    const StagePlan half = stage_plan(KC / 2);
+    if (half.NS >= 2) sp = half;
+  }
+  KC = sp.KC;
+  p.KC = KC;
+  p.bytes_x = (uint32_t)(KC * Mp * 2);
+  p.stage_bytes = sp.stage_bytes;
+  p.n_stages = sp.n_stages;
+  p.b_late_off = sp.b_late_off;
+  const size_t fixed = sp.fixed;
+  const int NS = sp.NS;
   if (NS < 1 || fixed + (size_t)NS * p.stage_bytes > 227 * 1024) return SPEAR_ERR_UNSUPPORTED;
   p.NS = NS;
   out->smem = fixed + (size_t)NS * p.stage_bytes;
   out->grid = (h->nt16 + P - 1) / P;
   out->NW = NW;
   out->MT = MT;
+  out->T = T;
   out->kernel = kernel_for(NW, MT, T, h->per_channel, ec);
   if (!out->kernel.fn) return SPEAR_ERR_UNSUPPORTED;
   return SPEAR_OK;
@@ -165,5 +211,52 @@ spear_status_t spear_decode_check_residency(spear_linear_s* h) {
       return SPEAR_ERR_CUDA;
     if ((long)per_sm * h->sm_count < d.grid) return SPEAR_ERR_UNSUPPORTED;
   }
+  return SPEAR_OK;
+}
+
+// Test surface: the decode launch plan of a handle of this shape, computed by
+// the same host code as the launch (decode_config), with no device work.
+spear_status_t spear_decode_schedule(int32_t N, int32_t K, int32_t rank_b, int32_t n_members, int32_t group_size,
+                                     int32_t gate_hidden, int32_t M, int32_t sm_count, int32_t* info) {
+  if (N <= 0 || K <= 0 || K % 128 != 0 || N % 8 != 0 || (group_size != 0 && group_size != 128) || rank_b < 0 ||
+      rank_b % 16 != 0 || n_members < 1 || n_members > kMaxGroup || n_members * rank_b > 256 || gate_hidden < 0 ||
+      gate_hidden > kMaxGateHidden || gate_hidden % 16 != 0 || (gate_hidden > 0 && rank_b == 0) || M < 1 ||
+      M > kDecodeMaxTokens || sm_count < 1 || !info)
+    return SPEAR_ERR_INVALID_ARG;
+  spear_linear_s h;
+  h.sm_count = sm_count;
+  h.K = K;
+  h.N = N;
+  h.per_channel = group_size == 0;
+  h.G = h.per_channel ? K : group_size;
+  h.n_groups = K / h.G;
+  h.n_members = n_members;
+  h.rank_b = rank_b;
+  h.rank = n_members * rank_b;
+  for (int i = 0; i <= n_members; ++i) h.row_start[i] = (int)((int64_t)N * i / n_members);
+  h.gate = gate_hidden > 0 ? SPEAR_GATE_MLP : SPEAR_GATE_SIGMOID;
+  h.gate_hidden = gate_hidden;
+  h.max_tokens = kDecodeMaxTokens;
+  const int nt16_rows = (N + 15) / 16;
+  if ((nt16_rows + sm_count - 1) / sm_count > kDecodeMaxTilesPerCta) return SPEAR_ERR_UNSUPPORTED;
+  h.dec_P = decode_tiles_per_cta(nt16_rows, sm_count);
+  h.nt16 = (nt16_rows + h.dec_P - 1) / h.dec_P * h.dec_P;
+  DecodeLaunch d;
+  const spear_status_t st = decode_config(&h, M, &d);
+  if (st != SPEAR_OK) return st;
+  const int32_t v[13] = {d.grid,
+                         d.p.P,
+                         d.NW,
+                         d.T,
+                         d.MT,
+                         d.p.KW,
+                         d.p.KC,
+                         d.p.NS,
+                         (int32_t)d.p.stage_bytes,
+                         (int32_t)d.smem,
+                         d.p.n_stages,
+                         (d.NW + 1 + kEcWarps) * 32,
+                         (int32_t)d.p.bytes_x};
+  for (int i = 0; i < 13; ++i) info[i] = v[i];
   return SPEAR_OK;
 }

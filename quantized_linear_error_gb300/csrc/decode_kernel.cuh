@@ -29,6 +29,7 @@ struct DecodeParams {
   float alpha;
   int nt16, P, KW, KC, NS, n_stages;
   uint32_t bytes_x, stage_bytes;  // x box bytes (KC * Mp * 2), bytes per stage buffer
+  uint32_t b_late_off;            // nonzero: B fragments copied to the stage area at this offset after the W loop
   uint64_t wait_ns;
   int skip_arrive;
   const __nv_bfloat16* gw1;  // SPEAR_GATE_MLP: W1 [gh][rank]
@@ -250,9 +251,12 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
   float* zs_mlp = reinterpret_cast<float*>(ul + Mp * us);  // MLP gate: z^T [M16][rank + 8]
   constexpr int M16 = Mp < 16 ? 16 : Mp;
   // B fragments of this CTA's tiles [Pc][rank / 16][32] uint4 (16-byte aligned)
+  // (or, with b_late_off, in the stage area behind the partial sums)
   const uint32_t bbuf_s =
-      (smem_u32(zs_mlp + (p.gh > 0 ? M16 * (p.rank + 8) : 0)) +
-       (p.gh > 0 ? (uint32_t)(p.gh * (p.rank + 8) + p.rank * (p.gh + 8)) * 2u : 0u) + 15u) & ~15u;
+      p.b_late_off ? smem_u32(stages) + p.b_late_off
+                   : (smem_u32(zs_mlp + (p.gh > 0 ? M16 * (p.rank + 8) : 0)) +
+                      (p.gh > 0 ? (uint32_t)(p.gh * (p.rank + 8) + p.rank * (p.gh + 8)) * 2u : 0u) + 15u) &
+                         ~15u;
 
   const uint32_t stages_s = smem_u32(stages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -329,12 +333,17 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
         issue_weights(i);
         issue_x(i);
       }
+      const unsigned bbytes = EC ? (unsigned)(Pc * (p.rank_b / 16) * 512) : 0u;
+      const uint4* bsrc = p.b_frag + (size_t)tile0 * (p.rank_b / 16) * 32;
       if (EC) {
         // B fragments of this CTA's tiles (contiguous, constant since create)
-        // into shared memory for the final up-projection.
-        const unsigned bbytes = (unsigned)(Pc * (p.rank_b / 16) * 512);
-        mbar_arrive_expect_tx(bbar, bbytes);
-        bulk_g2s_shared_u32(bbuf_s, p.b_frag + (size_t)tile0 * (p.rank_b / 16) * 32, bbytes, bbar);
+        // into shared memory for the final up-projection (late: into L2 now)
+        if (p.b_late_off) {
+          prefetch_l2(bsrc, bbytes);
+        } else {
+          mbar_arrive_expect_tx(bbar, bbytes);
+          bulk_g2s_shared_u32(bbuf_s, bsrc, bbytes, bbar);
+        }
       }
       for (int i = prefetch; i < p.n_stages; ++i) {
         const int slot = i % p.NS;
@@ -344,6 +353,18 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
         }
         issue_weights(i);
         issue_x(i);
+      }
+      if (EC && p.b_late_off) {
+        // the stage area is free once the last NS stages are released
+        bool free = true;
+        for (int i = max(0, p.n_stages - p.NS); free && i < p.n_stages; ++i)
+          free = mbar_wait_bounded(&empty[i % p.NS], (i / p.NS) & 1, p.wait_ns);
+        if (free) {
+          mbar_arrive_expect_tx(bbar, bbytes);
+          bulk_g2s_shared_u32(bbuf_s, bsrc, bbytes, bbar);
+        } else {
+          atomicOr(&p.sync->status, kStatusTimeoutPipe);
+        }
       }
     }
     return;

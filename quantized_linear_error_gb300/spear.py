@@ -84,6 +84,8 @@ def load(path: Path | None = None):
     L.spear_sched_destroy.restype = c_int
     L.spear_quantize_rtn.argtypes = [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, H]
     L.spear_quantize_rtn.restype = c_int
+    L.spear_decode_schedule.argtypes = [c_int32] * 8 + [c_void_p]
+    L.spear_decode_schedule.restype = c_int
     L.spear_prefill_schedule.argtypes = [c_int32] * 7 + [c_void_p, c_void_p, c_int32]
     L.spear_prefill_schedule.restype = c_int
     L.spear_status_string.argtypes = [c_int]
@@ -288,6 +290,21 @@ def quantize_rtn(w, group_size=128, stream=None):
     _check(load().spear_quantize_rtn(_ptr(w), int(N), int(K), int(group_size), _ptr(q), _ptr(s), _ptr(z),
                                      _stream(stream)), "spear_quantize_rtn")
     return q, s, z
+
+
+DECODE_SCHEDULE_FIELDS = ("grid", "P", "NW", "T", "MT", "KW", "KC", "NS", "stage_bytes", "smem", "n_stages",
+                          "threads", "bytes_x")
+
+
+def decode_schedule(N: int, K: int, M: int, sm_count: int, rank_b: int = 0, n_members: int = 1,
+                    group_size: int = 128, gate_hidden: int = 0) -> dict:
+    """The decode launch plan for a handle of this shape (host only, no GPU):
+    the fields of ``DECODE_SCHEDULE_FIELDS``."""
+    L = load()
+    info = (ctypes.c_int32 * len(DECODE_SCHEDULE_FIELDS))()
+    _check(L.spear_decode_schedule(N, K, rank_b, n_members, group_size, gate_hidden, M, sm_count, info),
+           "spear_decode_schedule")
+    return dict(zip(DECODE_SCHEDULE_FIELDS, list(info)))
 
 
 PREFILL_SCHEDULE_FIELDS = ("mode", "G", "TN", "kpt", "tail", "units", "pro_items", "pro_d", "NS",
