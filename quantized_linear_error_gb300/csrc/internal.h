@@ -99,6 +99,10 @@ struct spear_linear_s {
   // fp32 main result [max_tokens][N] and the fork / join events
   float* y32 = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  // host-buffer batches: copy streams (inputs up, results down) and the
+  // per-handle events that order them with the forwards
+  cudaStream_t copy_in = nullptr, copy_out = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_x_ready = nullptr, ev_done = nullptr, ev_y_taken = nullptr;
   __nv_bfloat16* x_stage = nullptr;  // host-path staging [max_tokens][K]
   __nv_bfloat16* y_stage = nullptr;  // host-path staging [max_tokens][N]
 

@@ -63,8 +63,10 @@ void free_all(spear_linear_s* h) {
                   h->b_pre,  h->ws,      h->x_stage, h->y_stage, h->gate_w1, h->gate_w2, h->y32};
   for (void* p : ptrs)
     if (p) cudaFree(p);
-  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
-  if (h->ev_join) cudaEventDestroy(h->ev_join);
+  for (cudaEvent_t ev : {h->ev_fork, h->ev_join, h->ev_start, h->ev_x_ready, h->ev_done, h->ev_y_taken})
+    if (ev) cudaEventDestroy(ev);
+  for (cudaStream_t st : {h->copy_in, h->copy_out})
+    if (st) cudaStreamDestroy(st);
 }
 
 spear_status_t validate(const spear_linear_desc_t* d) {
@@ -181,6 +183,10 @@ spear_status_t create_impl(const spear_linear_desc_t* d, const GroupInfo& g, cud
   A(alloc(&h->ws, ws_bytes));
   A(alloc(&h->x_stage, mt * K * 2));
   A(alloc(&h->y_stage, mt * (size_t)h->N * 2));
+  for (cudaStream_t* st : {&h->copy_in, &h->copy_out})
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(st, cudaStreamNonBlocking);
+  for (cudaEvent_t* ev : {&h->ev_start, &h->ev_x_ready, &h->ev_done, &h->ev_y_taken})
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     cudaGetLastError();
     free_all(h);
@@ -404,30 +410,37 @@ spear_status_t spear_linear_forward_host_batch(const spear_linear_t* hs, const v
     if (!h || Ms[i] < 0 || Ms[i] > h->max_tokens) return SPEAR_ERR_INVALID_ARG;
     if (Ms[i] > 0 && (!x_host[i] || !y_host[i])) return SPEAR_ERR_INVALID_ARG;
   }
-  // Runs of calls on distinct handles: all inputs up, the forwards back to
-  // back (so that each kernel's programmatic launch overlaps the previous
-  // one's tail, which a copy between them would prevent), all results down.
-  // A handle that appears again starts the next run: the calls share its
-  // staging buffers.
-  for (int32_t i = 0; i < n;) {
-    int32_t j = i + 1;
-    for (bool dup = false; j < n && !dup; j += dup ? 0 : 1)
-      for (int32_t k = i; k < j && !dup; ++k) dup = hs[k] == hs[j];
-    for (int32_t k = i; k < j; ++k)
-      if (Ms[k] > 0 && cudaMemcpyAsync(hs[k]->x_stage, x_host[k], (size_t)Ms[k] * hs[k]->K * 2, cudaMemcpyHostToDevice,
-                                       stream) != cudaSuccess)
-        return SPEAR_ERR_CUDA;
-    for (int32_t k = i; k < j; ++k) {
-      if (Ms[k] == 0) continue;
-      const spear_status_t s = spear_linear_forward(hs[k], hs[k]->x_stage, hs[k]->y_stage, Ms[k], stream);
-      if (s != SPEAR_OK) return s;
-    }
-    for (int32_t k = i; k < j; ++k)
-      if (Ms[k] > 0 && cudaMemcpyAsync(y_host[k], hs[k]->y_stage, (size_t)Ms[k] * hs[k]->N * 2, cudaMemcpyDeviceToHost,
-                                       stream) != cudaSuccess)
-        return SPEAR_ERR_CUDA;
-    i = j;
+  // Inputs go up on one copy stream and results down on another (those of
+  // hs[0]), so that copies overlap the forwards on `stream`. Per handle,
+  // events order each call's steps: its input copy after the previous
+  // forward on the handle has read the staging buffer (ev_done), its forward
+  // after that copy (ev_x_ready) and after the previous result left the
+  // staging buffer (ev_y_taken), its result copy after the forward. Every
+  // wait is on an earlier call, so nothing waits in a cycle; the copy streams
+  // start after the work already on `stream`.
+  cudaStream_t cin = hs[0]->copy_in, cout = hs[0]->copy_out;
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  if (!ok(cudaEventRecord(hs[0]->ev_start, stream)) || !ok(cudaStreamWaitEvent(cin, hs[0]->ev_start, 0)) ||
+      !ok(cudaStreamWaitEvent(cout, hs[0]->ev_start, 0)))
+    return SPEAR_ERR_CUDA;
+  for (int32_t k = 0; k < n; ++k) {
+    const spear_linear_t h = hs[k];
+    if (Ms[k] == 0) continue;
+    bool again = false;  // an earlier call of this batch used the handle
+    for (int32_t j = 0; j < k && !again; ++j) again = hs[j] == h && Ms[j] > 0;
+    if ((again && !ok(cudaStreamWaitEvent(cin, h->ev_done, 0))) ||
+        !ok(cudaMemcpyAsync(h->x_stage, x_host[k], (size_t)Ms[k] * h->K * 2, cudaMemcpyHostToDevice, cin)) ||
+        !ok(cudaEventRecord(h->ev_x_ready, cin)) || !ok(cudaStreamWaitEvent(stream, h->ev_x_ready, 0)) ||
+        (again && !ok(cudaStreamWaitEvent(stream, h->ev_y_taken, 0))))
+      return SPEAR_ERR_CUDA;
+    const spear_status_t s = spear_linear_forward(h, h->x_stage, h->y_stage, Ms[k], stream);
+    if (s != SPEAR_OK) return s;
+    if (!ok(cudaEventRecord(h->ev_done, stream)) || !ok(cudaStreamWaitEvent(cout, h->ev_done, 0)) ||
+        !ok(cudaMemcpyAsync(y_host[k], h->y_stage, (size_t)Ms[k] * h->N * 2, cudaMemcpyDeviceToHost, cout)) ||
+        !ok(cudaEventRecord(h->ev_y_taken, cout)))
+      return SPEAR_ERR_CUDA;
   }
+  if (!ok(cudaStreamSynchronize(cin)) || !ok(cudaStreamSynchronize(cout))) return SPEAR_ERR_CUDA;
   return cudaStreamSynchronize(stream) == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
 }
 
