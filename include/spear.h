@@ -172,15 +172,17 @@ spear_status_t spear_linear_forward_host(spear_linear_t h, const void* x_host, v
  * synchronisation: call i copies x_host[i] (bf16 [Ms[i]][K of hs[i]]) into
  * hs[i]'s staging buffer, runs spear_linear_forward on it and copies the
  * result into y_host[i] (bf16 [Ms[i]][N of hs[i]]); the call returns once
- * every result is in host memory. The forwards run in order on `stream`; the
- * copies run on two copy streams of hs[0] (created with the handle), after
- * the work already on `stream`, and overlap the forwards: a call's input
- * copy waits only for the previous forward on the same handle (which has
- * read its staging buffer), its forward for that copy and for the previous
- * result of the handle to be copied out. A handle may appear several times.
- * Every argument is checked before anything is enqueued: INVALID_ARG for a null
- * array or handle, Ms[i] outside 0 .. max_tokens of hs[i], or null buffers
- * with Ms[i] > 0. Pinned host memory gives asynchronous copies. */
+ * every result is in host memory. The forwards run in order on `stream`.
+ * The copies run on two copy streams of hs[0], after the work already on
+ * `stream`, and overlap the forwards: a call's input copy waits only for the
+ * previous forward on the same handle (which has read its staging buffer),
+ * its forward for that copy and for the previous result of the handle to be
+ * copied out. A handle may appear several times. The copy streams and a
+ * handle's four events are made on its first batch and destroyed with it.
+ * Every argument is checked before anything is enqueued: INVALID_ARG for a
+ * null array or handle, Ms[i] outside 0 .. max_tokens of hs[i], or null
+ * buffers with Ms[i] > 0; CUDA if a stream or event cannot be made. Pinned
+ * host memory gives asynchronous copies. */
 spear_status_t spear_linear_forward_host_batch(const spear_linear_t* hs, const void* const* x_host,
                                                void* const* y_host, const int32_t* Ms, int32_t n,
                                                cudaStream_t stream);

@@ -183,10 +183,6 @@ spear_status_t create_impl(const spear_linear_desc_t* d, const GroupInfo& g, cud
   A(alloc(&h->ws, ws_bytes));
   A(alloc(&h->x_stage, mt * K * 2));
   A(alloc(&h->y_stage, mt * (size_t)h->N * 2));
-  for (cudaStream_t* st : {&h->copy_in, &h->copy_out})
-    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(st, cudaStreamNonBlocking);
-  for (cudaEvent_t* ev : {&h->ev_start, &h->ev_x_ready, &h->ev_done, &h->ev_y_taken})
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     cudaGetLastError();
     free_all(h);
@@ -399,6 +395,18 @@ spear_status_t spear_linear_forward_host(spear_linear_t h, const void* x_host, v
   return cudaStreamSynchronize(stream) == cudaSuccess ? SPEAR_OK : SPEAR_ERR_CUDA;
 }
 
+// The copy streams and events of the host-buffer batch path, made on a
+// handle's first batch (most handles never use that path).
+static cudaError_t host_batch_sync_objects(spear_linear_s* h, bool streams) {
+  cudaError_t e = cudaSuccess;
+  for (cudaEvent_t* ev : {&h->ev_start, &h->ev_x_ready, &h->ev_done, &h->ev_y_taken})
+    if (e == cudaSuccess && !*ev) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+  if (streams)
+    for (cudaStream_t* st : {&h->copy_in, &h->copy_out})
+      if (e == cudaSuccess && !*st) e = cudaStreamCreateWithFlags(st, cudaStreamNonBlocking);
+  return e;
+}
+
 spear_status_t spear_linear_forward_host_batch(const spear_linear_t* hs, const void* const* x_host,
                                                void* const* y_host, const int32_t* Ms, int32_t n,
                                                cudaStream_t stream) {
@@ -418,8 +426,10 @@ spear_status_t spear_linear_forward_host_batch(const spear_linear_t* hs, const v
   // staging buffer (ev_y_taken), its result copy after the forward. Every
   // wait is on an earlier call, so nothing waits in a cycle; the copy streams
   // start after the work already on `stream`.
-  cudaStream_t cin = hs[0]->copy_in, cout = hs[0]->copy_out;
   auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  for (int32_t k = 0; k < n; ++k)
+    if (!ok(host_batch_sync_objects(hs[k], k == 0))) return SPEAR_ERR_CUDA;
+  cudaStream_t cin = hs[0]->copy_in, cout = hs[0]->copy_out;
   if (!ok(cudaEventRecord(hs[0]->ev_start, stream)) || !ok(cudaStreamWaitEvent(cin, hs[0]->ev_start, 0)) ||
       !ok(cudaStreamWaitEvent(cout, hs[0]->ev_start, 0)))
     return SPEAR_ERR_CUDA;
