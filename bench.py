@@ -502,10 +502,12 @@ def measure_scheduler(args, stream, time_graphs, dev, base):
     sched = spear.ChunkScheduler(dens, toks, table)
     cands = list(range(64, 2049, 64))
     checks = []
+    # the table's step times vary by ~2% from run to run: picks keep 3% headroom
+    headroom = 0.03
     for d in (0.25, 0.75):
         for itl in (16.0, 22.0):
-            c = sched.pick_chunk(n_dec, d, itl, cands)
-            row = {"density": d, "itl_ms": itl, "picked_chunk": c,
+            c = sched.pick_chunk(n_dec, d, itl * (1.0 - headroom), cands)
+            row = {"density": d, "itl_ms": itl, "headroom": headroom, "picked_chunk": c,
                    "predicted_ms": sched.predict(n_dec + c, d) if c else None,
                    "measured_ms": step_ms(d, n_dec + c) if c else None}
             row["meets_slo"] = row["measured_ms"] is not None and row["measured_ms"] <= itl
