@@ -117,6 +117,25 @@ def test_config4_per_channel(idx):
     _check(with_spec(w, alpha=30.0), 16, rows)
 
 
+@pytest.mark.parametrize("cfg,idx,M,sms", [(2, 3, 16, None), (2, 6, 16, None), (4, 0, 32, None), (4, 1, 32, None)])
+def test_stage_plans_late_b_and_half_stages(cfg, idx, M, sms):
+    """The plans that keep at least two stages: the o and down projections at
+    16 tokens and config 4's down projection at 32 take one 128-channel unit
+    per K warp and stage; config 4's up projection at 32 copies its B
+    fragments (rank 256) into the stage area after the W loop. The plan is
+    asserted through the host query, then the result against the oracle
+    (compensator as is, and dominant)."""
+    sp = wl.config_linears(cfg)[idx]
+    w = wl.make_weights(sp, 5)
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    d = spear.decode_schedule(sp.N, sp.K, M, n_sm, rank_b=sp.rank, group_size=sp.group_size)
+    assert d["NS"] >= 2 and d["n_stages"] > 1
+    rows = sample_rows(sp.N, 192, idx)
+    lin = spear.from_weights(w, max_tokens=32)
+    _check(w, M, rows, lin=lin)
+    _check(codes_equal_zeros(w), M, rows)
+
+
 # ---------------------------------------------------------------- boundary and bounded waits
 def test_decode_rejects_too_many_tokens():
     w = wl.make_weights(SMALL[0], 6)
