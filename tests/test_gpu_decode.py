@@ -117,8 +117,8 @@ def test_config4_per_channel(idx):
     _check(with_spec(w, alpha=30.0), 16, rows)
 
 
-@pytest.mark.parametrize("cfg,idx,M,sms", [(2, 3, 16, None), (2, 6, 16, None), (4, 0, 32, None), (4, 1, 32, None)])
-def test_stage_plans_late_b_and_half_stages(cfg, idx, M, sms):
+@pytest.mark.parametrize("cfg,idx,M", [(2, 3, 16), (2, 6, 16), (4, 0, 32), (4, 1, 32)])
+def test_stage_plans_late_b_and_half_stages(cfg, idx, M):
     """The plans that keep at least two stages: the o and down projections at
     16 tokens and config 4's down projection at 32 take one 128-channel unit
     per K warp and stage; config 4's up projection at 32 copies its B
