@@ -221,8 +221,8 @@ class SpearLinear:
 
 def forward_host_batch(linears, xs_host, ys_host, stream=None) -> None:
     """spear_linear_forward_host_batch over (SpearLinear, host x, host y)
-    triples: every call's copies and kernels in order on one stream, one
-    synchronisation at the end."""
+    triples: the forwards in order on `stream`, the copies on the first
+    handle's copy streams overlapping them, one synchronisation at the end."""
     n = len(linears)
     hs = (c_void_p * n)(*[lin.h.value for lin in linears])
     xp = (c_void_p * n)(*[x.data_ptr() for x in xs_host])
