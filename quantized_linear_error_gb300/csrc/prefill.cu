@@ -294,16 +294,14 @@ SPEAR_DEVINL void add_z_partial(const GateArgs& g, uint32_t lane_base, int token
 }
 
 // u' = bf16(alpha gamma(z) (.) z) for the 128-token tile starting at token
-// a0, from its z rows (row stride zst floats, in shared memory, or in global
-// memory when z_global: then read through L2; rows past M are zero). Run by
-// the four epilogue warps, warp q on tokens a0 + 32 q .. + 31. The MLP gate
-// reads W1 [gh][w1s] and W2 [rank][w2s] from shared memory (stage_mlp_weights).
-SPEAR_DEVINL void gate_rows(const GateArgs& g, const float* z, int zst, bool z_global, int a0, int q, int lane,
+// a0, from its z rows in global memory (row stride zst floats, read through
+// L2; rows past M are zero). Run by the four epilogue warps, warp q on tokens
+// a0 + 32 q .. + 31. The MLP gate reads W1 [gh][rank + 8] and W2
+// [rank][gh + 8] from shared memory (stage_mlp_weights).
+SPEAR_DEVINL void gate_rows(const GateArgs& g, const float* z, int zst, int a0, int q, int lane,
                             const __nv_bfloat16* w1, const __nv_bfloat16* w2) {
   const int r = g.rank;
-  auto ld4 = [&](const float* ptr) {
-    return z_global ? __ldcg(reinterpret_cast<const float4*>(ptr)) : *reinterpret_cast<const float4*>(ptr);
-  };
+  auto ld4 = [&](const float* ptr) { return __ldcg(reinterpret_cast<const float4*>(ptr)); };
   if (g.gate == SPEAR_GATE_MLP) {
     // Bottleneck-MLP gate on warp MMAs (mlp_gate_logits) for the warp's two
     // 16-token blocks: u' = bf16(alpha sigmoid(W2 relu(W1 z)) (.) z).
@@ -313,8 +311,7 @@ SPEAR_DEVINL void gate_rows(const GateArgs& g, const float* z, int zst, bool z_g
                         const int m = a0 + lr;
                         if (m >= g.M) return;
                         const float* zr = z + (size_t)lr * zst;
-                        const float z0 = z_global ? __ldcg(zr + j) : zr[j];
-                        const float z1 = z_global ? __ldcg(zr + j + 1) : zr[j + 1];
+                        const float z0 = __ldcg(zr + j), z1 = __ldcg(zr + j + 1);
                         *reinterpret_cast<uint32_t*>(g.u + (size_t)m * r + j) =
                             pack_bf16x2(g.alpha * z0 * (1.0f / (1.0f + expf(-g0))),
                                         g.alpha * z1 * (1.0f / (1.0f + expf(-g1))));
@@ -366,7 +363,7 @@ __host__ __device__ inline size_t mlp_weight_bytes(int rank, int gh) {
 SPEAR_DEVINL void gate_tile(const GateArgs& g, int a0, int q, int lane, __nv_bfloat16* wbuf) {
   const int r = g.rank;
   if (g.gate == SPEAR_GATE_MLP) stage_mlp_weights(g, wbuf);
-  gate_rows(g, g.zacc + (size_t)a0 * r, r, true, a0, q, lane, wbuf, wbuf + (size_t)g.gh * (r + 8));
+  gate_rows(g, g.zacc + (size_t)a0 * r, r, a0, q, lane, wbuf, wbuf + (size_t)g.gh * (r + 8));
   __syncwarp();
   for (int rr = 0; rr < 32; ++rr) {
     const int m = a0 + 32 * q + rr;
