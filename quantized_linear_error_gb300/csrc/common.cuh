@@ -275,21 +275,6 @@ SPEAR_DEVINL uint32_t pack_bf16x2(float lo, float hi);
 // Copy a bf16 [rows][cols] matrix (cols a multiple of 8, 16-byte aligned rows)
 // into shared memory with row stride cols + 8 (16-byte chunks, all loads of a
 // thread's share in flight before any store): the MLP gate's weights.
-// The same copy with 16-byte cp.async (the copying threads do not wait for
-// the loads; each waits with cp_async_wait_all() before a barrier that makes
-// the rows visible to the others).
-SPEAR_DEVINL void stage_rows_padded_async(__nv_bfloat16* dst, const __nv_bfloat16* src, int rows, int cols, int tid,
-                                          int nthreads) {
-  const int c8 = cols / 8, n = rows * c8;
-  for (int i = tid; i < n; i += nthreads)
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst + (i / c8) * (cols + 8) + (i % c8) * 8)),
-                 "l"(reinterpret_cast<const uint4*>(src) + i)
-                 : "memory");
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
-SPEAR_DEVINL void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 SPEAR_DEVINL void stage_rows_padded(__nv_bfloat16* dst, const __nv_bfloat16* src, int rows, int cols, int tid,
                                     int nthreads) {
   const int c8 = cols / 8, n = rows * c8;

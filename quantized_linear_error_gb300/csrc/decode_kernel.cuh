@@ -121,13 +121,13 @@ SPEAR_DEVINL void ec_prefetch(const DecodeParams& p, int ew, int lane) {
 // Bottleneck-MLP gate ("SPEAR", section 2.1A: gamma is a bottleneck MLP):
 // u = alpha * sigmoid(W2 relu(W1 z)) (.) z per token, by the four compensator
 // warps: z is staged transposed in shared memory (zs [M16][rank + 8], token
-// rows M .. M16 - 1 zero, M16 = Mp rounded up to 16) next to W1 and W2 (their
-// asynchronous copies issued before the grid-dependency wait, rows padded by
-// 8), the two products run on warp MMAs (mlp_gate_logits), each of the four
-// warps taking one 16-token block and a quarter (M16 = 16) or half (M16 = 32)
-// of the rank columns (the hidden layer is computed by each); u is written
-// split into bf16 hi + lo like the elementwise gates (zero for tokens
-// M .. Mp - 1, and everywhere if z never arrived).
+// rows M .. M16 - 1 zero, M16 = Mp rounded up to 16) next to W1 and W2
+// (copied there, rows padded by 8, by three of the warps while the fourth
+// waits for the grid), the two products run on warp MMAs (mlp_gate_logits),
+// each of the four warps taking one 16-token block and a quarter (M16 = 16)
+// or half (M16 = 32) of the rank columns (the hidden layer is computed by
+// each); u is written split into bf16 hi + lo like the elementwise gates
+// (zero for tokens M .. Mp - 1, and everywhere if z never arrived).
 // One (16-token block, part of the rank columns) item of the MLP gate. Not
 // inlined: its fragments would otherwise raise the register allocation of the
 // whole kernel, consumer loop included.
@@ -181,7 +181,6 @@ SPEAR_DEVINL void ec_u_mlp(const DecodeParams& p, const float* z, bool arrived, 
       }
     }
   }
-  cp_async_wait_all();  // this thread's copies of W1 and W2 (the barrier below publishes them)
   ec_bar();
   constexpr int kParts = kEcWarps / (M16 / 16);  // one item per compensator warp
   for (int item = ew; item < (M16 / 16) * kParts; item += kEcWarps)
@@ -377,14 +376,6 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
       const int ew = warp - NW - 1;
       volatile int* ec_flag = reinterpret_cast<volatile int*>(smem + 512);
       ec_prefetch(p, ew, lane);
-      if (p.gate == SPEAR_GATE_MLP) {
-        // the MLP gate's weights (constant since create) into shared memory,
-        // after z^T: W1 [gh][rank + 8], then W2 [rank][gh + 8]
-        constexpr int M16 = Mp < 16 ? 16 : Mp;
-        __nv_bfloat16* w1s = reinterpret_cast<__nv_bfloat16*>(zs_mlp + M16 * (p.rank + 8));
-        stage_rows_padded_async(w1s, p.gw1, p.gh, p.rank, ew * 32 + lane, kEcWarps * 32);
-        stage_rows_padded_async(w1s + p.gh * (p.rank + 8), p.gw2, p.rank, p.gh, ew * 32 + lane, kEcWarps * 32);
-      }
       asm volatile("griddepcontrol.wait;" ::: "memory");
       // Calls alternate between two z buffers. `epoch` (calls completed so
       // far) is read by every CTA before its arrival and advanced by the last
@@ -427,6 +418,17 @@ __global__ void __launch_bounds__((NW + 1 + kEcWarps) * 32, 1)
         const int n4 = p.rank * 8;  // float4 of [rank][32]
         const int c0 = (int)((long)blockIdx.x * n4 / gridDim.x), c1 = (int)((long)(blockIdx.x + 1) * n4 / gridDim.x);
         for (int i = c0 + (ew - 1) * 32 + lane; i < c1; i += (kEcWarps - 1) * 32) zn[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p.gate == SPEAR_GATE_MLP) {
+          // and the MLP gate's weights (constant since create) into shared
+          // memory after z^T: W1 [gh][rank + 8], then W2 [rank][gh + 8].
+          // (Copied before the grid-dependency wait, they delayed the
+          // projection by ~1 us.)
+          constexpr int M16 = Mp < 16 ? 16 : Mp;
+          __nv_bfloat16* w1s = reinterpret_cast<__nv_bfloat16*>(zs_mlp + M16 * (p.rank + 8));
+          const int tid = (ew - 1) * 32 + lane, nt = (kEcWarps - 1) * 32;
+          stage_rows_padded(w1s, p.gw1, p.gh, p.rank, tid, nt);
+          stage_rows_padded(w1s + p.gh * (p.rank + 8), p.gw2, p.rank, p.gh, tid, nt);
+        }
       }
       ec_bar();
       const bool arrived = *ec_flag != 0;
