@@ -97,3 +97,32 @@ def test_rejects_bad_shapes(lib):
     assert L.spear_decode_schedule(128, 128, 0, 1, 128, 0, 1, SMS, None) == spear.SPEAR_ERR_INVALID_ARG
     # more rows than 16 tiles per CTA on every SM
     assert L.spear_decode_schedule(16 * 16 * 4 + 16, 128, 0, 1, 128, 0, 1, 4, info) == spear.SPEAR_ERR_UNSUPPORTED
+
+
+def test_random_shapes(lib):
+    """A seeded sweep of shapes beyond the workloads: every plan valid, and
+    two or more stages wherever K needs them at ranks up to 64 without the
+    MLP gate (at rank 128-256 with a 64-wide gate, or 16 tiles per CTA at
+    rank 256, the compensator's buffers can leave room for one)."""
+    import random
+    rng = random.Random(1)
+    checked = 0
+    for _ in range(600):
+        N = rng.choice([8, 16, 136, 200, 520, 1032, 2048, 4096, 4104, 8192, 11008, 12288, 22016, 28672, 36864])
+        K = 128 * rng.randint(1, 230)
+        gs, n, M = rng.choice([0, 128]), rng.choice([1, 1, 2, 3, 4]), rng.randint(1, 32)
+        rb = rng.choice([0, 16, 32, 64, 128, 256])
+        gh = rng.choice([0, 0, 16, 64]) if rb and n == 1 else 0
+        if N % n or n * rb > 256:
+            continue
+        try:
+            d = spear.decode_schedule(N, K, M, SMS, rank_b=rb, n_members=n, group_size=gs, gate_hidden=gh)
+        except spear.SpearError as e:
+            assert e.status == spear.SPEAR_ERR_UNSUPPORTED  # more than 16 tiles per CTA
+            continue
+        checked += 1
+        assert d["grid"] <= SMS and d["smem"] <= SMEM_MAX and d["NS"] >= 1 and d["threads"] <= 1024
+        assert d["grid"] * d["P"] >= (N + 15) // 16 and d["KC"] % 256 == 0 and d["bytes_x"] <= 64 * 1024
+        if rb <= 64 and gh == 0 and d["n_stages"] > 1:
+            assert d["NS"] >= 2, (N, K, gs, n, rb, M, d)
+    assert checked > 300

@@ -213,3 +213,28 @@ def test_rejects_bad_shapes(lib):
     assert L.spear_prefill_schedule(128, 64, 0, 0, 1, 152, 1, None, None, 0) == spear.SPEAR_ERR_INVALID_ARG
     starts = (ctypes.c_uint32 * 1)()
     assert L.spear_prefill_schedule(4096, 4096, 64, 0, 2048, 152, 1, info, starts, 1) == spear.SPEAR_ERR_INVALID_ARG
+
+
+def test_random_shapes(lib):
+    """A seeded sweep of shapes beyond the workloads, with and without the
+    stream-K workspace: every split partitions the units without starting
+    inside a K-tail; stream-K grids are resident next to the pre-kernel and
+    their owners' partials fit; one-CTA-per-tile grids have no partials."""
+    import random
+    rng = random.Random(2)
+    for _ in range(300):
+        N = rng.choice([8, 136, 200, 520, 1032, 4096, 4104, 11008, 12288, 14336, 22016, 28672])
+        K = 64 * rng.randint(1, 460)
+        r = rng.choice([0, 16, 32, 64, 128, 192, 256])
+        gh = rng.choice([0, 0, 16, 64]) if r else 0
+        M, ws = rng.randint(33, 4096), rng.random() < 0.9
+        d = spear.prefill_schedule(N, K, r, M, SMS, gate_hidden=gh, with_workspace=ws)
+        s = d["starts"]
+        assert s[0] == 0 and s[-1] == d["units"] and all(b > a for a, b in zip(s, s[1:]))
+        assert all(b % d["kpt"] == 0 or b % d["kpt"] >= d["tail"] for b in s[:-1])
+        assert d["smem"] <= SMEM_MAX and d["NS"] >= 2 and d["tmem_a"] + 32 * d["NS"] <= 512
+        if ws:
+            assert d["G"] + d["pre_ctas"] <= SMS
+            assert d["max_contrib"] * 32 * 512 <= d["NS"] * d["stage_bytes"] or d["G"] == 1
+        else:
+            assert d["max_contrib"] == 0 and all(x % d["kpt"] == 0 for x in s)
